@@ -1,0 +1,210 @@
+/*
+ * CPU oracle for exact QSA block selection -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg load
+ * this file's library. It shares no code, header, table or helper with the
+ * CUDA path; it is a plain, slow, FP64 restatement of what the selection
+ * computes, written from the pages:
+ *
+ *  - "#3108 optimize exact QSA block scoring and top-k selection on gfx12",
+ *    Summary items 1 and 4: a block score is the sum over the 4 query heads
+ *    of the head's dot product with the block's summary key (the "4-head
+ *    block score" assembled from per-head 32-lane reductions);
+ *  - "#337 gfx12 QSA select", What items 1-2: only the batch's active blocks
+ *    are scored and selected, never the capacity; the top-k is exact (the
+ *    page reports selections equal to the reference in 256/256 queries),
+ *    and an FP64 reference gates the scorer;
+ *  - ties are broken by lower block id, and the selected ids are returned in
+ *    ascending block-id order (reading taken where the pages are silent).
+ *
+ * Score (fp32 keys):  S[i][b] = sum_{h<4} sum_{d<128} q[i][h][d] * kblk[b][d]
+ * in double precision: each head's dot product accumulates in natural d
+ * order, and the heads are added in order 0..3. Every product of two floats
+ * is exact in double, so S carries only the rounding of the additions.
+ *
+ * Score (int8 keys): the key element is kq8[b][d] * scale[b], scale an IEEE
+ * binary16 value; the product (8-bit by 11-bit significands) is exact in
+ * double, and the sum is formed exactly as above.
+ *
+ * Selection: sort the pairs (S, id) by S descending, then id ascending (a
+ * strict total order), keep the first min(k, active) ids, sort them
+ * ascending, and fill the remaining k - active slots (if any) with -1. A NaN
+ * score ranks below every number; -0.0 and +0.0 compare equal (and so tie).
+ */
+#include "qsa_oracle.h"
+
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define QSA_H 4
+#define QSA_D 128
+
+int qsa_oracle_default_threads(void) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n < 1 ? 1 : (int)n;
+}
+
+/* ---- row-parallel driver (rows are independent) ---------------------- */
+
+typedef void (*row_fn)(void *ctx, long row);
+
+typedef struct {
+    row_fn fn;
+    void *ctx;
+    long nrows;
+    int tid, nthreads;
+} row_job;
+
+static void *row_worker(void *arg) {
+    row_job *j = (row_job *)arg;
+    for (long r = j->tid; r < j->nrows; r += j->nthreads) j->fn(j->ctx, r);
+    return NULL;
+}
+
+static void for_each_row(row_fn fn, void *ctx, long nrows, int nthreads) {
+    if (nthreads <= 0) nthreads = qsa_oracle_default_threads();
+    if (nthreads > nrows) nthreads = (int)(nrows > 0 ? nrows : 1);
+    if (nthreads == 1) {
+        for (long r = 0; r < nrows; ++r) fn(ctx, r);
+        return;
+    }
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    row_job *jobs = (row_job *)malloc(sizeof(row_job) * (size_t)nthreads);
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t].fn = fn; jobs[t].ctx = ctx; jobs[t].nrows = nrows;
+        jobs[t].tid = t; jobs[t].nthreads = nthreads;
+        pthread_create(&th[t], NULL, row_worker, &jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    free(th);
+    free(jobs);
+}
+
+/* ---- IEEE 754 binary16 -> double (from the format's definition) ------- */
+
+double qsa_oracle_half_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int m = h & 0x3FF;
+    double v;
+    if (e == 0)            v = ldexp((double)m, -24);                 /* zero / subnormal */
+    else if (e == 0x1F)    v = (m == 0) ? INFINITY : NAN;             /* inf / NaN        */
+    else                   v = ldexp((double)(1024 + m), e - 25);     /* normal           */
+    return sign ? -v : v;
+}
+
+/* ---- block scores ----------------------------------------------------- */
+
+typedef struct {
+    const float *q;
+    const float *kblk;
+    const int8_t *kq8;
+    const uint16_t *kscale;
+    long active;
+    double *S;
+} score_ctx;
+
+static void score_row_f32(void *vctx, long i) {
+    const score_ctx *c = (const score_ctx *)vctx;
+    const float *qi = c->q + (size_t)i * QSA_H * QSA_D;
+    double *Si = c->S + (size_t)i * (size_t)c->active;
+    for (long b = 0; b < c->active; ++b) {
+        const float *kb = c->kblk + (size_t)b * QSA_D;
+        double total = 0.0;
+        for (int h = 0; h < QSA_H; ++h) {
+            const float *qh = qi + h * QSA_D;
+            double dot = 0.0;
+            for (int d = 0; d < QSA_D; ++d) dot += (double)qh[d] * (double)kb[d];
+            total += dot;
+        }
+        Si[b] = total;
+    }
+}
+
+static void score_row_q8(void *vctx, long i) {
+    const score_ctx *c = (const score_ctx *)vctx;
+    const float *qi = c->q + (size_t)i * QSA_H * QSA_D;
+    double *Si = c->S + (size_t)i * (size_t)c->active;
+    for (long b = 0; b < c->active; ++b) {
+        const int8_t *kb = c->kq8 + (size_t)b * QSA_D;
+        double scale = qsa_oracle_half_to_double(c->kscale[b]);
+        double total = 0.0;
+        for (int h = 0; h < QSA_H; ++h) {
+            const float *qh = qi + h * QSA_D;
+            double dot = 0.0;
+            for (int d = 0; d < QSA_D; ++d) dot += (double)qh[d] * ((double)kb[d] * scale);
+            total += dot;
+        }
+        Si[b] = total;
+    }
+}
+
+void qsa_oracle_scores(const float *q, const float *kblk, long nq, long active,
+                       double *S, int nthreads) {
+    score_ctx c = {q, kblk, NULL, NULL, active, S};
+    for_each_row(score_row_f32, &c, nq, nthreads);
+}
+
+void qsa_oracle_scores_q8(const float *q, const int8_t *kq8, const uint16_t *kscale,
+                          long nq, long active, double *S, int nthreads) {
+    score_ctx c = {q, NULL, kq8, kscale, active, S};
+    for_each_row(score_row_q8, &c, nq, nthreads);
+}
+
+/* ---- exact top-k by full sort ---------------------------------------- */
+
+typedef struct { double s; int32_t id; } scored_id;
+
+/* Strict total order: higher score first, then lower id; NaN below all. */
+static int by_score_desc_id_asc(const void *pa, const void *pb) {
+    const scored_id *a = (const scored_id *)pa, *b = (const scored_id *)pb;
+    int a_nan = isnan(a->s), b_nan = isnan(b->s);
+    if (a_nan != b_nan) return a_nan ? 1 : -1;
+    if (!a_nan && a->s > b->s) return -1;
+    if (!a_nan && a->s < b->s) return 1;
+    return (a->id < b->id) ? -1 : (a->id > b->id);
+}
+
+static int by_id_asc(const void *pa, const void *pb) {
+    int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
+    return (a > b) - (a < b);
+}
+
+typedef struct {
+    const double *S64;
+    const float *S32;
+    long active, k;
+    int32_t *ids;
+} topk_ctx;
+
+static void topk_row(void *vctx, long i) {
+    const topk_ctx *c = (const topk_ctx *)vctx;
+    long n = c->active;
+    scored_id *pairs = (scored_id *)malloc(sizeof(scored_id) * (size_t)(n > 0 ? n : 1));
+    for (long b = 0; b < n; ++b) {
+        pairs[b].s = c->S64 ? c->S64[(size_t)i * n + b] : (double)c->S32[(size_t)i * n + b];
+        pairs[b].id = (int32_t)b;
+    }
+    qsort(pairs, (size_t)n, sizeof(scored_id), by_score_desc_id_asc);
+    long m = c->k < n ? c->k : n;
+    int32_t *out = c->ids + (size_t)i * (size_t)c->k;
+    for (long j = 0; j < m; ++j) out[j] = pairs[j].id;
+    qsort(out, (size_t)m, sizeof(int32_t), by_id_asc);
+    for (long j = m; j < c->k; ++j) out[j] = -1;
+    free(pairs);
+}
+
+void qsa_oracle_topk_f64(const double *S, long nq, long active, long k, int32_t *ids,
+                         int nthreads) {
+    topk_ctx c = {S, NULL, active, k, ids};
+    for_each_row(topk_row, &c, nq, nthreads);
+}
+
+void qsa_oracle_topk_f32(const float *scores, long nq, long active, long k, int32_t *ids,
+                         int nthreads) {
+    topk_ctx c = {NULL, scores, active, k, ids};
+    for_each_row(topk_row, &c, nq, nthreads);
+}

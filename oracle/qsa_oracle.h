@@ -1,0 +1,39 @@
+/*
+ * CPU oracle for exact QSA block selection -- TEST INFRASTRUCTURE ONLY.
+ * Declarations for qsa_oracle.c; nothing outside the tests, the smoke check
+ * and the benchmark's CPU-baseline leg includes or links this.
+ *
+ * Layouts (all row-major, host memory owned by the caller):
+ *   q       float  [nq][4][128]
+ *   kblk    float  [>= active][128]
+ *   kq8     int8   [>= active][128], kscale uint16 (IEEE binary16) [>= active]
+ *   S       double [nq][active]      (scores, written)
+ *   scores  float  [nq][active]      (given fp32 scores, read)
+ *   ids     int32  [nq][k]           (written: ascending ids, -1 padding)
+ * nthreads <= 0 uses every online core.
+ */
+#ifndef QSA_ORACLE_H
+#define QSA_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+int qsa_oracle_default_threads(void);
+double qsa_oracle_half_to_double(uint16_t h);
+void qsa_oracle_scores(const float *q, const float *kblk, long nq, long active,
+                       double *S, int nthreads);
+void qsa_oracle_scores_q8(const float *q, const int8_t *kq8, const uint16_t *kscale,
+                          long nq, long active, double *S, int nthreads);
+void qsa_oracle_topk_f64(const double *S, long nq, long active, long k, int32_t *ids,
+                         int nthreads);
+void qsa_oracle_topk_f32(const float *scores, long nq, long active, long k, int32_t *ids,
+                         int nthreads);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

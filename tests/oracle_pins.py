@@ -1,0 +1,273 @@
+"""Pins for the CPU oracle: checks against facts fixed outside the oracle.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with something the pages or the mathematics fix:
+
+- brute force over every k-subset of tiny rows (the unique subset that
+  dominates its complement under "higher score, then lower id");
+- hand-derived scores with closed forms (one-hot queries, all-tie rows);
+- exact integer arithmetic (numpy int64) and library float64 matmul;
+- numpy's binary16 conversion over all 65,536 bit patterns;
+- invariants of an exact selection, padding and capacity independence;
+- a hand-computed golden fixture (``golden/hand_scores.json``).
+
+The definition being pinned: score = sum over the 4 query heads of the
+head's dot product with the block's summary key, over active blocks only
+("#3108 optimize exact QSA block scoring and top-k selection on gfx12",
+Summary items 1 and 4; "#337 gfx12 QSA select", What items 1-2); the top-k
+is exact with ties broken by lower block id and ids returned ascending.
+
+``test_oracle_mutants.py`` runs every pin against deliberately broken
+builds of the oracle to show that the pins catch plausible mistakes.
+"""
+
+from __future__ import annotations
+
+import itertools
+import json
+import os
+
+import numpy as np
+
+H, D = 4, 128
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed: int) -> np.random.Generator:
+    # test-local randomness for pin construction only (never a parity input)
+    return np.random.default_rng(seed)
+
+
+def _dominates(vals: np.ndarray, subset: tuple[int, ...]) -> bool:
+    """True iff every member beats every non-member (value desc, id asc)."""
+    inside = set(subset)
+    def rank(i):
+        v = vals[i]
+        return (0 if np.isnan(v) else 1, -0.0 if np.isnan(v) else float(v), -i)
+    for i in inside:
+        for j in range(len(vals)):
+            if j not in inside and not rank(i) > rank(j):
+                return False
+    return True
+
+
+def brute_force_topk(vals: np.ndarray, k: int) -> np.ndarray:
+    n = len(vals)
+    m = min(k, n)
+    winners = [s for s in itertools.combinations(range(n), m) if _dominates(vals, s)]
+    assert len(winners) == 1, f"expected exactly one dominating subset, got {len(winners)}"
+    out = np.full(k, -1, dtype=np.int32)
+    out[:m] = sorted(winners[0])
+    return out
+
+
+def pin_brute_force_topk(o) -> None:
+    r = _rng(11)
+    rows = []
+    for n in range(1, 10):
+        rows.append(r.normal(size=n))                                   # distinct
+        rows.append(r.integers(-2, 3, size=n).astype(np.float64))       # many ties
+        rows.append(np.where(r.random(n) < 0.5, 0.0, -0.0))             # +-0 ties
+    rows.append(np.array([1.0, np.nan, 1.0, -np.inf, np.inf, np.nan, -1.0]))
+    for vals in rows:
+        n = len(vals)
+        for k in range(1, n + 3):
+            want = brute_force_topk(vals, k)
+            got32 = o.topk_f32(vals.astype(np.float32)[None, :], k)[0]
+            got64 = o.topk_f64(vals[None, :], k)[0]
+            assert np.array_equal(got32, want), (vals, k, got32, want)
+            assert np.array_equal(got64, want), (vals, k, got64, want)
+
+
+def _onehot_workload(nq: int, active: int):
+    """q[i][h] = e_{4i+h}; kblk[b][d] = b - d.  Then
+    S[i][b] = sum_h kblk[b][4i+h] = sum_h (b - 4i - h) = 4b - 16i - 6."""
+    q = np.zeros((nq, H, D), dtype=np.float32)
+    for i in range(nq):
+        for h in range(H):
+            q[i, h, 4 * i + h] = 1.0
+    b = np.arange(active, dtype=np.float32)[:, None]
+    d = np.arange(D, dtype=np.float32)[None, :]
+    return q, (b - d).astype(np.float32)
+
+
+def pin_closed_form_onehot(o) -> None:
+    nq, active = 5, 300
+    q, kblk = _onehot_workload(nq, active)
+    S = o.scores(q, kblk, active)
+    i = np.arange(nq)[:, None]
+    b = np.arange(active)[None, :]
+    assert np.array_equal(S, (4 * b - 16 * i - 6).astype(np.float64))
+    for k in (1, 7, 64, 299, 300, 301):
+        ids = o.topk_f64(S, k)
+        m = min(k, active)
+        want = np.concatenate([np.arange(active - m, active), -np.ones(k - m)]).astype(np.int32)
+        assert all(np.array_equal(row, want) for row in ids), (k, ids[0][:8])
+
+
+def pin_all_ties_lower_id(o) -> None:
+    """Every block holds the same key, so every score ties; the lower-id
+    rule then selects ids 0..k-1. The same key with a sign flip on odd
+    blocks splits the row into two tie groups."""
+    nq, active = 3, 50
+    q = np.tile(np.arange(1, H + 1, dtype=np.float32)[None, :, None], (nq, 1, D))
+    key = (np.arange(D) % 7 - 3).astype(np.float32)
+    kblk = np.tile(key, (active, 1))
+    S = o.scores(q, kblk, active)
+    assert np.all(S == S[0, 0]) and S[0, 0] == 10.0 * float(np.sum(key))
+    for k in (1, 10, 49, 50):
+        assert all(np.array_equal(r, np.arange(k)) for r in o.topk_f64(S, k))
+    sgn = np.where(np.arange(active) % 2 == 0, 1.0, -1.0).astype(np.float32)
+    key2 = np.ones(D, dtype=np.float32)
+    kblk2 = (sgn[:, None] * key2[None, :]).astype(np.float32)
+    S2 = o.scores(q, kblk2, active)
+    ids = o.topk_f64(S2, 30)
+    want = np.concatenate([np.arange(0, active, 2), np.arange(1, 11, 2)])
+    assert all(np.array_equal(r, np.sort(want)) for r in ids), ids[0]
+
+
+def pin_integer_exact(o) -> None:
+    """Integer-valued inputs: compare with exact int64 arithmetic (numpy
+    einsum on int64) and a library sort (numpy lexsort)."""
+    r = _rng(7)
+    for nq, active, k in ((3, 97, 10), (4, 256, 255), (2, 33, 40)):
+        q = r.integers(-8, 9, size=(nq, H, D))
+        kb = r.integers(-8, 9, size=(active, D))
+        S = o.scores(q.astype(np.float32), kb.astype(np.float32), active)
+        exact = np.einsum("ihd,bd->ib", q.astype(np.int64), kb.astype(np.int64))
+        assert np.array_equal(S, exact.astype(np.float64))
+        ids = o.topk_f64(S, k)
+        for i in range(nq):
+            order = np.lexsort((np.arange(active), -exact[i]))
+            m = min(k, active)
+            want = np.concatenate([np.sort(order[:m]), -np.ones(k - m)]).astype(np.int32)
+            assert np.array_equal(ids[i], want)
+
+
+def pin_float_vs_numpy(o) -> None:
+    """Random fp32 inputs: FP64 scores agree with numpy's float64 matmul to
+    rounding (1e-12 of the row scale); ids agree with a lexsort of the
+    oracle's own scores."""
+    r = _rng(5)
+    nq, active, k = 6, 777, 31
+    q = r.normal(size=(nq, H, D)).astype(np.float32)
+    kb = r.standard_t(3, size=(active, D)).astype(np.float32)
+    S = o.scores(q, kb, active)
+    ref = np.einsum("ihd,bd->ib", q.astype(np.float64), kb.astype(np.float64))
+    scale = np.abs(ref).max(axis=1, keepdims=True)
+    assert np.all(np.abs(S - ref) <= 1e-12 * scale)
+    ids = o.topk_f64(S, k)
+    for i in range(nq):
+        order = np.lexsort((np.arange(active), -S[i]))
+        assert np.array_equal(ids[i], np.sort(order[:k]))
+
+
+def pin_half_to_double(o) -> None:
+    """All 65,536 binary16 patterns against numpy's float16 conversion."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([o.half_to_double(int(h)) for h in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def pin_q8_scores(o) -> None:
+    """int8 keys times binary16 scales: exact against int64 arithmetic when
+    q is integer-valued and the scales are powers of two; within rounding
+    of numpy float64 otherwise."""
+    r = _rng(3)
+    nq, active = 3, 200
+    kq = r.integers(-127, 128, size=(active, D)).astype(np.int8)
+    e = r.integers(-10, -2, size=active)
+    sc = (2.0 ** e).astype(np.float16).view(np.uint16)
+    qi = r.integers(-8, 9, size=(nq, H, D))
+    S = o.scores_q8(qi.astype(np.float32), kq, sc, active)
+    exact = np.einsum("ihd,bd->ib", qi.astype(np.int64), kq.astype(np.int64)).astype(np.float64)
+    assert np.array_equal(S, exact * (2.0 ** e)[None, :])
+    sc2 = r.uniform(1e-3, 1e-1, size=active).astype(np.float16)
+    qf = r.normal(size=(nq, H, D)).astype(np.float32)
+    S2 = o.scores_q8(qf, kq, sc2.view(np.uint16), active)
+    ref = np.einsum("ihd,bd->ib", qf.astype(np.float64),
+                    kq.astype(np.float64) * sc2.astype(np.float64)[:, None])
+    assert np.all(np.abs(S2 - ref) <= 1e-12 * np.abs(ref).max(axis=1, keepdims=True))
+
+
+def pin_padding_and_empty(o) -> None:
+    S = np.array([[3.0, 1.0, 2.0], [0.0, 0.0, -1.0]])
+    assert np.array_equal(o.topk_f64(S, 5), [[0, 1, 2, -1, -1], [0, 1, 2, -1, -1]])
+    assert np.array_equal(o.topk_f64(S, 2), [[0, 2], [0, 1]])
+    assert np.array_equal(o.topk_f64(np.zeros((2, 0)), 3), -np.ones((2, 3), dtype=np.int32))
+
+
+def pin_capacity_independence(o) -> None:
+    """Only the first ``active`` key rows are read: NaN-filled capacity rows
+    change nothing."""
+    r = _rng(9)
+    nq, active, cap = 2, 40, 47
+    q = r.normal(size=(nq, H, D)).astype(np.float32)
+    kb = r.normal(size=(cap, D)).astype(np.float32)
+    kb_nan = kb.copy()
+    kb_nan[active:] = np.nan
+    S1 = o.scores(q, kb[:active].copy(), active)
+    S2 = o.scores(q, kb_nan, active)
+    assert S2.shape == (nq, active) and np.array_equal(S1, S2)
+    kq = r.integers(-127, 128, size=(cap, D)).astype(np.int8)
+    sc = np.full(cap, 0x7E00, dtype=np.uint16)
+    sc[:active] = np.float16(0.01).view(np.uint16)
+    assert not np.isnan(o.scores_q8(q, kq, sc, active)).any()
+
+
+def pin_selection_invariants(o) -> None:
+    """Exactness: unique, in-range ids; min(k, active) of them; every
+    selected score >= every unselected one; boundary ties to lower ids."""
+    r = _rng(13)
+    for active, k in ((500, 50), (64, 64), (1000, 1)):
+        S = np.round(r.normal(size=(4, active)) * 4) / 4      # coarse grid: many ties
+        ids = o.topk_f64(S, k)
+        for i in range(S.shape[0]):
+            sel = ids[i][ids[i] >= 0]
+            assert len(sel) == min(k, active) and len(np.unique(sel)) == len(sel)
+            assert np.all(np.diff(sel) > 0) and sel.min() >= 0 and sel.max() < active
+            mask = np.zeros(active, bool)
+            mask[sel] = True
+            if (~mask).any():
+                lo_in, hi_out = S[i][mask].min(), S[i][~mask].max()
+                assert lo_in >= hi_out
+                if lo_in == hi_out:
+                    tied_in = np.nonzero(mask & (S[i] == lo_in))[0]
+                    tied_out = np.nonzero(~mask & (S[i] == lo_in))[0]
+                    assert tied_in.max() < tied_out.min()
+
+
+def pin_golden_hand(o) -> None:
+    """Hand-derived scores and selections (see the fixture's derivation)."""
+    with open(os.path.join(GOLDEN, "hand_scores.json")) as f:
+        g = json.load(f)
+    nq, active = g["nq"], g["active"]
+    q = np.zeros((nq, H, D), dtype=np.float32)
+    for i, h, d, v in g["q_nonzero"]:
+        q[i, h, d] = v
+    kb = np.zeros((active, D), dtype=np.float32)
+    for b, d, v in g["kblk_nonzero"]:
+        kb[b, d] = v
+    S = o.scores(q, kb, active)
+    assert np.array_equal(S, np.array(g["scores"], dtype=np.float64)), S
+    for k, want in g["topk"].items():
+        assert np.array_equal(o.topk_f64(S, int(k)), np.array(want, dtype=np.int32)), (k, want)
+
+
+ALL_PINS = [
+    pin_brute_force_topk,
+    pin_closed_form_onehot,
+    pin_all_ties_lower_id,
+    pin_integer_exact,
+    pin_float_vs_numpy,
+    pin_half_to_double,
+    pin_q8_scores,
+    pin_padding_and_empty,
+    pin_capacity_independence,
+    pin_selection_invariants,
+    pin_golden_hand,
+]

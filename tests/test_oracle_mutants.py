@@ -1,0 +1,65 @@
+"""Negative controls for the oracle's pins (CPU only).
+
+Each case plants one plausible mistake in a copy of the oracle's C source
+(a dropped head, a wrong sign, a wrong stride, a reversed tie rule, ...),
+builds it into a temporary library, and requires that at least one pin
+fails. A mutation whose target text is missing fails the test, so the list
+cannot silently go stale when the oracle changes.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+MUTANTS = {
+    "dropped_head": ("h < QSA_H; ++h", "h < QSA_H - 1; ++h"),
+    "wrong_sign": ("dot += (double)qh[d] * (double)kb[d]", "dot -= (double)qh[d] * (double)kb[d]"),
+    "head_stride": ("qi + h * QSA_D", "qi + h"),
+    "short_d_loop": ("for (int d = 0; d < QSA_D; ++d) dot += (double)qh[d] * (double)kb[d]",
+                     "for (int d = 1; d < QSA_D; ++d) dot += (double)qh[d] * (double)kb[d]"),
+    "tie_to_higher_id": ("return (a->id < b->id) ? -1 : (a->id > b->id);",
+                         "return (a->id > b->id) ? -1 : (a->id < b->id);"),
+    "ascending_scores": ("if (!a_nan && a->s > b->s) return -1;", "if (!a_nan && a->s < b->s) return -1;"),
+    "nan_ranks_first": ("if (a_nan != b_nan) return a_nan ? 1 : -1;",
+                        "if (a_nan != b_nan) return a_nan ? -1 : 1;"),
+    "ids_in_rank_order": ("qsort(out, (size_t)m, sizeof(int32_t), by_id_asc);", ""),
+    "zero_padding": ("for (long j = m; j < c->k; ++j) out[j] = -1;",
+                     "for (long j = m; j < c->k; ++j) out[j] = 0;"),
+    "half_bias": ("ldexp((double)(1024 + m), e - 25)", "ldexp((double)(1024 + m), e - 24)"),
+    "half_subnormal": ("ldexp((double)m, -24)", "ldexp((double)m, -25)"),
+    "scale_dropped": ("((double)kb[d] * scale)", "((double)kb[d])"),
+    "float_key_trunc": ("(double)c->S32[(size_t)i * n + b]", "(double)(int)c->S32[(size_t)i * n + b]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    with open(oracle.SOURCE) as f:
+        src = f.read()
+    assert old in src, f"mutation target for {name} not found in the oracle source"
+    mut = tmp_path / "qsa_oracle_mutant.c"
+    mut.write_text(src.replace(old, new))
+    # the mutant includes the oracle's own header from the oracle directory
+    lib = oracle.build(force=True, source=str(mut), out=str(tmp_path / "libmutant.so"))
+    o = oracle.Oracle(lib)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(o)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    with open(oracle.SOURCE) as f:
+        src = f.read()
+    cp = tmp_path / "qsa_oracle_copy.c"
+    cp.write_text(src)
+    o = oracle.Oracle(oracle.build(force=True, source=str(cp), out=str(tmp_path / "libcopy.so")))
+    for pin in oracle_pins.ALL_PINS:
+        pin(o)
+    assert os.path.exists(tmp_path / "libcopy.so")
