@@ -1,0 +1,126 @@
+/*
+ * qsa.h -- exact QSA block selection on one GB300 (sm_103a): block scoring
+ * and an exact per-query top-k, as a C ABI over caller-owned device memory.
+ *
+ * What is computed (the "QSA select" step of query-aware sparse attention):
+ * each query is 4 query heads of D = 128 fp32 values that share one KV head.
+ * The KV cache is cut into 4-cell blocks, each summarised by one key of 128
+ * values. A query's score for a block is the sum over its 4 heads of the
+ * head's dot product with the block key; only the first `active_blocks`
+ * blocks exist for this batch, whatever the cache capacity. The top-k then
+ * keeps, per query, the k highest-scoring block ids exactly.
+ * Passages: "#3108 optimize exact QSA block scoring and top-k selection on
+ * gfx12", Summary items 1, 2 and 4 (4-head block score, radix top-k,
+ * bitwise parity of scores and ids); "#337 gfx12 QSA select", What items 1-2
+ * (select over the active blocks, not the capacity `max_context/4 + 2`;
+ * split-bf16 tensor-core scorer with the hi*hi products in their own
+ * accumulator; FP64 gate at 1e-6 of the score scale).
+ *
+ * Conventions for every call below:
+ *  - All pointers are DEVICE pointers owned by the caller; the library keeps
+ *    no state between calls (beyond a per-device error word, see
+ *    qsa_get_device_error), allocates nothing, never synchronises, and
+ *    enqueues its kernels on `stream` (0 = the legacy default stream).
+ *  - Every pointer that is dereferenced must be 16-byte aligned.
+ *  - Arguments are checked before anything is launched; a bad argument
+ *    returns QSA_ERR_INVALID and launches nothing. A launch failure returns
+ *    QSA_ERR_CUDA. Errors of already-enqueued work surface as CUDA errors of
+ *    the stream, as for any kernel.
+ *  - Calls with no work (nq == 0, or active_blocks == 0 for the scorers)
+ *    return QSA_OK without touching memory; pointers may then be NULL.
+ *  - Inputs are expected to be finite. A NaN score ranks below every number
+ *    in the top-k; -0.0 and +0.0 are equal (and therefore tie).
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QSA_OK = 0,
+    QSA_ERR_INVALID = 1,      /* bad argument; nothing was launched            */
+    QSA_ERR_UNSUPPORTED = 2,  /* valid, but beyond this library's size limits  */
+    QSA_ERR_CUDA = 3          /* a CUDA runtime call or launch failed          */
+} qsa_status;
+
+/* Head dimension and query heads per KV head (fixed). */
+#define QSA_D 128
+#define QSA_HEADS 4
+
+/* Largest active_blocks the top-k accepts (8 CTAs x 49,152 keys). */
+#define QSA_TOPK_MAX_ACTIVE 393216
+
+/*
+ * Block scores, fp32 summary keys.
+ *   scores[i][b] = sum_{h<4} sum_{d<128} q[i][h][d] * kblk[b][d],  b < active_blocks
+ * q       fp32 [nq][4][128], contiguous.
+ * kblk    fp32 [max_blocks][128], block-major; only rows < active_blocks are read.
+ * scores  fp32 [nq][active_blocks], written; row stride = active_blocks.
+ * max_blocks is the key buffer's capacity (validation only: active_blocks <=
+ * max_blocks); the launch is sized from active_blocks alone.
+ * Accuracy: |scores - exact| <= 1e-6 * max_b |exact[i][b]| per row for
+ * finite inputs; scores are exact when every product and partial sum is an
+ * integer below 2^24 in magnitude.
+ * ("#3108 ...", Summary item 4; "#337 ...", What items 1-2.)
+ */
+qsa_status qsa_block_scores(const float *q, const float *kblk, int nq, int max_blocks,
+                            int active_blocks, float *scores, cudaStream_t stream);
+
+/*
+ * Block scores, int8 summary keys with one IEEE binary16 scale per block
+ * (the engine's `--kv int8` cache form; key element = kblk_q8[b][d] *
+ * kscale_f16[b], exact in fp32).
+ * kblk_q8    int8   [max_blocks][128]
+ * kscale_f16 uint16 [max_blocks] (binary16 bit patterns; 2-byte aligned suffices)
+ * Other arguments, layouts and accuracy as qsa_block_scores.
+ * ("#3108 ...", End-to-End `--kv int8`; "#337 ...", What: `--kv int8`.)
+ */
+qsa_status qsa_block_scores_q8(const float *q, const int8_t *kblk_q8, const uint16_t *kscale_f16,
+                               int nq, int max_blocks, int active_blocks, float *scores,
+                               cudaStream_t stream);
+
+/*
+ * Block scores on the CUDA cores (FP32 FMA, head-summed query, natural d
+ * order) -- the same contract as qsa_block_scores; kept as the measured
+ * alternative to the tensor-core scorer. kblk_q8/kscale_f16 may be given
+ * instead of kblk (then kblk must be NULL) for the int8 key form.
+ */
+qsa_status qsa_block_scores_ffma(const float *q, const float *kblk, const int8_t *kblk_q8,
+                                 const uint16_t *kscale_f16, int nq, int max_blocks,
+                                 int active_blocks, float *scores, cudaStream_t stream);
+
+/*
+ * Exact per-query top-k of packed scores.
+ * scores  fp32  [nq][active_blocks] (row stride = active_blocks).
+ * ids     int32 [nq][k], written: for each row, the ids of the k highest
+ *         scores in ascending id order; among equal scores the lower block
+ *         id is taken first. If k > active_blocks the row holds all
+ *         active_blocks ids ascending followed by -1 (active_blocks == 0
+ *         gives a row of -1).
+ * k >= 1 and active_blocks <= QSA_TOPK_MAX_ACTIVE (else QSA_ERR_UNSUPPORTED).
+ * ("#3108 ...", Summary item 2: radix-bin top-k; "#337 ...", What item 1:
+ * the active block count, not the capacity, bounds the selection.)
+ */
+qsa_status qsa_block_topk(const float *scores, int nq, int active_blocks, int k, int32_t *ids,
+                          cudaStream_t stream);
+
+/*
+ * Reads and clears the current device's error word: nonzero when a kernel
+ * of this library gave up a bounded wait (its outputs are then invalid).
+ * Synchronises `stream`. *code receives the word.
+ */
+qsa_status qsa_get_device_error(uint32_t *code, cudaStream_t stream);
+
+/* Static description of a status code. */
+const char *qsa_status_string(qsa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H */

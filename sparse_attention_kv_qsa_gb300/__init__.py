@@ -1,0 +1,16 @@
+"""Exact QSA block selection on GB300: block scoring and per-query top-k.
+
+The computation lives in ``libqsa.so`` (CUDA kernels for sm_103a behind the C
+ABI of ``include/qsa.h``); ``qsa`` is its Python binding and ``workloads``
+the seeded synthetic input generator.
+"""
+
+from .qsa import (  # noqa: F401
+    QSAError,
+    block_scores,
+    block_scores_ffma,
+    block_scores_q8,
+    block_select,
+    block_topk,
+    device_error,
+)

@@ -1,0 +1,115 @@
+// C ABI of the QSA selection library: argument checks, then launches on the
+// caller's stream. Declarations and the contract: include/qsa.h.
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "../../include/qsa.h"
+#include "qsa_internal.cuh"
+
+namespace qsa {
+
+int device_sm_count() {
+    static std::mutex mu;
+    static std::vector<int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= static_cast<int>(cache.size())) cache.resize(dev + 1, 0);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace qsa
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+qsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA; }
+
+// Largest nq the scorer grid accepts (grid.y = ceil(nq / 128) <= 65535).
+constexpr long long MAX_NQ = 65535LL * 128;
+
+qsa_status check_score_args(const float *q, int nq, int max_blocks, int active_blocks,
+                            const float *scores) {
+    if (nq < 0 || max_blocks < 0 || active_blocks < 0 || active_blocks > max_blocks) return QSA_ERR_INVALID;
+    if (nq == 0 || active_blocks == 0) return QSA_OK;
+    if (q == nullptr || scores == nullptr) return QSA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(scores)) return QSA_ERR_INVALID;
+    if (nq > MAX_NQ) return QSA_ERR_UNSUPPORTED;
+    return QSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qsa_status qsa_block_scores(const float *q, const float *kblk, int nq, int max_blocks, int active_blocks,
+                            float *scores, cudaStream_t stream) {
+    qsa_status s = check_score_args(q, nq, max_blocks, active_blocks, scores);
+    if (s != QSA_OK || nq == 0 || active_blocks == 0) return s;
+    if (kblk == nullptr || !aligned16(kblk)) return QSA_ERR_INVALID;
+    return from_cuda(qsa::launch_scores_ffma(q, kblk, nullptr, nullptr, nq, active_blocks, scores, stream));
+}
+
+qsa_status qsa_block_scores_q8(const float *q, const int8_t *kblk_q8, const uint16_t *kscale_f16, int nq,
+                               int max_blocks, int active_blocks, float *scores, cudaStream_t stream) {
+    qsa_status s = check_score_args(q, nq, max_blocks, active_blocks, scores);
+    if (s != QSA_OK || nq == 0 || active_blocks == 0) return s;
+    if (kblk_q8 == nullptr || kscale_f16 == nullptr || !aligned16(kblk_q8)) return QSA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(kscale_f16) & 1u) != 0) return QSA_ERR_INVALID;
+    return from_cuda(
+        qsa::launch_scores_ffma(q, nullptr, kblk_q8, kscale_f16, nq, active_blocks, scores, stream));
+}
+
+qsa_status qsa_block_scores_ffma(const float *q, const float *kblk, const int8_t *kblk_q8,
+                                 const uint16_t *kscale_f16, int nq, int max_blocks, int active_blocks,
+                                 float *scores, cudaStream_t stream) {
+    qsa_status s = check_score_args(q, nq, max_blocks, active_blocks, scores);
+    if (s != QSA_OK || nq == 0 || active_blocks == 0) return s;
+    const bool f32 = kblk != nullptr;
+    const bool i8 = kblk_q8 != nullptr || kscale_f16 != nullptr;
+    if (f32 == i8) return QSA_ERR_INVALID;
+    if (f32 && !aligned16(kblk)) return QSA_ERR_INVALID;
+    if (i8 && (kblk_q8 == nullptr || kscale_f16 == nullptr || !aligned16(kblk_q8) ||
+               (reinterpret_cast<uintptr_t>(kscale_f16) & 1u) != 0))
+        return QSA_ERR_INVALID;
+    return from_cuda(
+        qsa::launch_scores_ffma(q, kblk, kblk_q8, kscale_f16, nq, active_blocks, scores, stream));
+}
+
+qsa_status qsa_block_topk(const float *scores, int nq, int active_blocks, int k, int32_t *ids,
+                          cudaStream_t stream) {
+    if (nq < 0 || active_blocks < 0 || k < 1) return QSA_ERR_INVALID;
+    if (nq == 0) return QSA_OK;
+    if (ids == nullptr || !aligned16(ids)) return QSA_ERR_INVALID;
+    if (active_blocks > QSA_TOPK_MAX_ACTIVE) return QSA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(nq) * k > (1LL << 40)) return QSA_ERR_UNSUPPORTED;
+    if (k >= active_blocks) return from_cuda(qsa::launch_topk_all(nq, active_blocks, k, ids, stream));
+    if (scores == nullptr || !aligned16(scores)) return QSA_ERR_INVALID;
+    if (static_cast<long long>(nq) * 8 > 0x7FFFFFFFLL) return QSA_ERR_UNSUPPORTED;
+    return from_cuda(qsa::launch_topk(scores, nq, active_blocks, k, ids, stream));
+}
+
+qsa_status qsa_get_device_error(uint32_t *code, cudaStream_t stream) {
+    if (code == nullptr) return QSA_ERR_INVALID;
+    *code = 0;
+    return from_cuda(qsa::topk_error_read_clear(code, stream));
+}
+
+const char *qsa_status_string(qsa_status status) {
+    switch (status) {
+        case QSA_OK: return "QSA_OK";
+        case QSA_ERR_INVALID: return "QSA_ERR_INVALID: invalid argument (nothing launched)";
+        case QSA_ERR_UNSUPPORTED: return "QSA_ERR_UNSUPPORTED: size beyond this library's limits";
+        case QSA_ERR_CUDA: return "QSA_ERR_CUDA: a CUDA call or launch failed";
+    }
+    return "QSA_ERR_UNKNOWN";
+}
+
+}  // extern "C"

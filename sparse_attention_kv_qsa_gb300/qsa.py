@@ -1,0 +1,184 @@
+"""Python binding of the C ABI in include/qsa.h (argument marshalling only).
+
+Every step of the selection runs in ``libqsa.so``'s CUDA kernels; this module
+checks tensor shapes, dtypes and devices, allocates outputs with torch, and
+passes raw device pointers and the current CUDA stream. There is no fallback:
+if the library is missing, importing the functions raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+D = 128
+HEADS = 4
+TOPK_MAX_ACTIVE = 393216
+
+QSA_OK, QSA_ERR_INVALID, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
+
+EXPORTED = ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
+            "qsa_get_device_error", "qsa_status_string")
+
+
+class QSAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded ``libqsa.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                               "(the QSA kernels have no fallback)")
+        L = ctypes.CDLL(path)
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        L.qsa_block_scores.argtypes = [vp, vp, i, i, i, vp, vp]
+        L.qsa_block_scores_q8.argtypes = [vp, vp, vp, i, i, i, vp, vp]
+        L.qsa_block_scores_ffma.argtypes = [vp, vp, vp, vp, i, i, i, vp, vp]
+        L.qsa_block_topk.argtypes = [vp, i, i, i, vp, vp]
+        L.qsa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+        L.qsa_status_string.argtypes = [i]
+        L.qsa_status_string.restype = ctypes.c_char_p
+        for f in ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
+                  "qsa_get_device_error"):
+            getattr(L, f).restype = i
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().qsa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != QSA_OK:
+        raise QSAError(status, what)
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None or t.numel() == 0 else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+
+
+def _scores_out(q: torch.Tensor, active_blocks: int, out: torch.Tensor | None) -> torch.Tensor:
+    nq = q.shape[0]
+    if out is None:
+        return torch.empty((nq, active_blocks), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, 2)
+    if tuple(out.shape) != (nq, active_blocks):
+        raise ValueError(f"out must have shape {(nq, active_blocks)}")
+    return out
+
+
+def _check_q(q: torch.Tensor) -> None:
+    _need(q, "q", torch.float32, 3)
+    if tuple(q.shape[1:]) != (HEADS, D):
+        raise ValueError(f"q must be [nq, {HEADS}, {D}]")
+
+
+def block_scores(q: torch.Tensor, kblk: torch.Tensor, active_blocks: int,
+                 out: torch.Tensor | None = None) -> torch.Tensor:
+    """``qsa_block_scores``: fp32 scores ``[nq, active_blocks]`` for fp32 keys
+    ``kblk[max_blocks, 128]`` (only the first ``active_blocks`` rows are read)."""
+    _check_q(q)
+    _need(kblk, "kblk", torch.float32, 2)
+    if kblk.shape[1] != D:
+        raise ValueError("kblk must be [max_blocks, 128]")
+    out = _scores_out(q, active_blocks, out)
+    _check(lib().qsa_block_scores(_ptr(q), _ptr(kblk), q.shape[0], kblk.shape[0], active_blocks,
+                                  _ptr(out), _stream(q)), "qsa_block_scores")
+    return out
+
+
+def block_scores_q8(q: torch.Tensor, kblk_q8: torch.Tensor, kscale_f16: torch.Tensor, active_blocks: int,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+    """``qsa_block_scores_q8``: int8 keys ``[max_blocks, 128]`` with one
+    binary16 scale per block (float16 or int16/uint16-viewed tensor)."""
+    _check_q(q)
+    _need(kblk_q8, "kblk_q8", torch.int8, 2)
+    if kscale_f16.dtype not in (torch.float16, torch.int16, torch.uint16):
+        raise ValueError("kscale_f16 must hold binary16 values")
+    if not kscale_f16.is_cuda or kscale_f16.dim() != 1 or not kscale_f16.is_contiguous():
+        raise ValueError("kscale_f16 must be a contiguous 1-d CUDA tensor")
+    if kblk_q8.shape[1] != D or kscale_f16.shape[0] < kblk_q8.shape[0]:
+        raise ValueError("kblk_q8 must be [max_blocks, 128] with max_blocks scales")
+    out = _scores_out(q, active_blocks, out)
+    _check(lib().qsa_block_scores_q8(_ptr(q), _ptr(kblk_q8), _ptr(kscale_f16), q.shape[0], kblk_q8.shape[0],
+                                     active_blocks, _ptr(out), _stream(q)), "qsa_block_scores_q8")
+    return out
+
+
+def block_scores_ffma(q: torch.Tensor, active_blocks: int, kblk: torch.Tensor | None = None,
+                      kblk_q8: torch.Tensor | None = None, kscale_f16: torch.Tensor | None = None,
+                      out: torch.Tensor | None = None) -> torch.Tensor:
+    """``qsa_block_scores_ffma``: the CUDA-core scorer (fp32 or int8 keys)."""
+    _check_q(q)
+    if kblk is not None:
+        _need(kblk, "kblk", torch.float32, 2)
+        max_blocks = kblk.shape[0]
+    else:
+        _need(kblk_q8, "kblk_q8", torch.int8, 2)
+        max_blocks = kblk_q8.shape[0]
+    out = _scores_out(q, active_blocks, out)
+    _check(lib().qsa_block_scores_ffma(_ptr(q), _ptr(kblk), _ptr(kblk_q8), _ptr(kscale_f16), q.shape[0],
+                                       max_blocks, active_blocks, _ptr(out), _stream(q)),
+           "qsa_block_scores_ffma")
+    return out
+
+
+def block_topk(scores: torch.Tensor, k: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """``qsa_block_topk``: int32 ids ``[nq, k]``, ascending per row, ties to
+    the lower block id, ``-1`` padding when ``k > active_blocks``."""
+    _need(scores, "scores", torch.float32, 2)
+    nq, active = scores.shape
+    if out is None:
+        out = torch.empty((nq, k), dtype=torch.int32, device=scores.device)
+    else:
+        _need(out, "out", torch.int32, 2)
+        if tuple(out.shape) != (nq, k):
+            raise ValueError(f"out must have shape {(nq, k)}")
+    _check(lib().qsa_block_topk(_ptr(scores), nq, active, k, _ptr(out), _stream(scores)), "qsa_block_topk")
+    return out
+
+
+def block_select(q: torch.Tensor, kblk: torch.Tensor, active_blocks: int, k: int,
+                 scores_out: torch.Tensor | None = None, ids_out: torch.Tensor | None = None):
+    """Scores then top-k, both on the current stream: ``(scores, ids)``."""
+    s = block_scores(q, kblk, active_blocks, scores_out)
+    return s, block_topk(s, k, ids_out)
+
+
+def device_error(device: torch.device | None = None) -> int:
+    """Reads and clears the library's device error word (synchronises)."""
+    code = ctypes.c_uint32(0)
+    stream = torch.cuda.current_stream(device).cuda_stream
+    _check(lib().qsa_get_device_error(ctypes.byref(code), stream), "qsa_get_device_error")
+    return int(code.value)

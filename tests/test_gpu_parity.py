@@ -1,0 +1,198 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Every workload is seeded and synthetic; the oracle computes every expected
+value on the host. Score gate: 1e-6 of each row's largest |score|; ids:
+bit-exact against the oracle's top-k of the GPU's own fp32 scores, and the
+near-tie rule against the FP64 oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+import qsa_cases
+import sparse_attention_kv_qsa_gb300 as qsa
+from sparse_attention_kv_qsa_gb300 import workloads as w
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle.get()
+
+
+def to_dev(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def gpu_scores(W, dev, scorer="default"):
+    q = to_dev(W.q, dev)
+    if W.kblk is not None:
+        kb = to_dev(W.kblk, dev)
+        if scorer == "ffma":
+            s = qsa.block_scores_ffma(q, W.active, kblk=kb)
+        else:
+            s = qsa.block_scores(q, kb, W.active)
+    else:
+        kq = to_dev(W.kq8, dev)
+        ks = to_dev(W.kscale.view(np.int16), dev)
+        if scorer == "ffma":
+            s = qsa.block_scores_ffma(q, W.active, kblk_q8=kq, kscale_f16=ks)
+        else:
+            s = qsa.block_scores_q8(q, kq, ks, W.active)
+    return s
+
+
+def oracle_scores(o, W):
+    if W.kblk is not None:
+        return o.scores(W.q, W.kblk, W.active)
+    return o.scores_q8(W.q, W.kq8, W.kscale, W.active)
+
+
+def check_select(o, W, s_dev, k=None, S_ref=None):
+    k = W.k if k is None else k
+    ids = qsa.block_topk(s_dev, k).cpu().numpy()
+    S_gpu = s_dev.cpu().numpy()
+    S_ref = oracle_scores(o, W) if S_ref is None else S_ref
+    parity.check_scores(S_gpu, S_ref)
+    assert np.array_equal(ids, o.topk_f32(S_gpu, k)), "ids differ from the exact top-k of the GPU scores"
+    parity.check_ids_near_tie(ids, S_ref, o.topk_f64(S_ref, k), k)
+    return S_gpu, S_ref, ids
+
+
+SCORERS = ["default", "ffma"]
+
+
+@pytest.mark.parametrize("scorer", SCORERS)
+def test_tiny_planted_ties(dev, o, scorer):
+    W = qsa_cases.tiny_with_ties(o)
+    S_gpu, S_ref, ids = check_select(o, W, gpu_scores(W, dev, scorer))
+    want = o.topk_f64(S_ref, W.k)
+    for i, g in enumerate(W.meta["tie_groups"]):
+        assert np.all(S_gpu[i][g] == S_gpu[i][g[0]]), "identical keys scored differently"
+        assert [b in ids[i] for b in g] == [b in want[i] for b in g]
+
+
+@pytest.mark.parametrize("scorer", SCORERS)
+@pytest.mark.parametrize("nq,active,max_blocks", [
+    (8, 1024, 1024), (5, 1003, 1100), (1, 17, 17), (130, 4099, 4101), (256, 8192, 65538), (3, 65536, 65538)])
+def test_integer_inputs_bit_exact(dev, o, scorer, nq, active, max_blocks):
+    W = w.integer_valued(nq, active, max_blocks)
+    S_gpu = gpu_scores(W, dev, scorer).cpu().numpy()
+    S_ref = o.scores(W.q, W.kblk, W.active)
+    assert np.array_equal(S_gpu.astype(np.float64), S_ref)
+
+
+@pytest.mark.parametrize("scorer", SCORERS)
+def test_mid_skewed(dev, o, scorer):
+    W = w.mid()
+    check_select(o, W, gpu_scores(W, dev, scorer))
+
+
+def test_long_needles(dev, o):
+    W = qsa_cases.long_with_needles(o)
+    _, _, ids = check_select(o, W, gpu_scores(W, dev))
+    for i in range(W.nq):
+        assert set(W.meta["needles"][i]) <= set(ids[i]), f"query {i} lost a needle"
+
+
+@pytest.mark.parametrize("scorer", SCORERS)
+def test_full_capacity_k_sweep(dev, o, scorer):
+    W = w.full()
+    s = gpu_scores(W, dev, scorer)
+    S_ref = o.scores(W.q, W.kblk, W.active)
+    for k in (512, 64, 256, 1024):
+        check_select(o, W, s, k=k, S_ref=S_ref)
+
+
+@pytest.mark.parametrize("scorer", SCORERS)
+@pytest.mark.parametrize("nq", [1, 4])
+@pytest.mark.parametrize("cells", [2048, 16384, 65536, 262144])
+def test_decode_int8_keys(dev, o, scorer, nq, cells):
+    W = w.decode(nq, cells)
+    check_select(o, W, gpu_scores(W, dev, scorer))
+
+
+@pytest.mark.parametrize("scorer", SCORERS)
+@pytest.mark.parametrize("nq,active,k", [(3, 4099, 100), (129, 777, 5), (2, 131, 130)])
+def test_int8_ragged(dev, o, scorer, nq, active, k):
+    W = w.int8_case(nq, active, k, max_blocks=active + 3)
+    check_select(o, W, gpu_scores(W, dev, scorer))
+
+
+def _tie_heavy(nq, active, seed):
+    u = w.u32(seed, 11, nq * active).reshape(nq, active)
+    s = ((u % 7).astype(np.float32) - 3.0) * 0.5          # 7 values: heavy ties
+    s[(u >> 8) % 5 == 0] = 0.0
+    s[(u >> 12) % 5 == 0] = -0.0
+    fine = w.normal32(seed, 12, nq * active).reshape(nq, active)
+    mix = ((u >> 16) % 3 == 0)
+    s[mix] = fine[mix]
+    return np.ascontiguousarray(s)
+
+
+@pytest.mark.parametrize("nq,active,k", [
+    (1, 1, 1), (2, 2, 1), (3, 3, 2), (4, 31, 30), (5, 1000, 1), (6, 1000, 999), (3, 4097, 64),
+    (2, 8193, 4096), (7, 16385, 512), (1, 65536, 128), (4, 65536, 512), (200, 5003, 77),
+    (2, 100003, 1000), (2, 393216, 1000), (1, 393213, 2)])
+def test_topk_exact_on_given_scores(dev, o, nq, active, k):
+    S = _tie_heavy(nq, active, seed=active * 31 + k)
+    ids = qsa.block_topk(to_dev(S, dev), k).cpu().numpy()
+    assert np.array_equal(ids, o.topk_f32(S, k))
+    parity.check_ids_valid(ids, active, k)
+
+
+def test_topk_nan_ranks_lowest(dev, o):
+    S = _tie_heavy(3, 3001, seed=5)
+    S[0, ::3] = np.nan
+    S[1, :] = np.nan
+    S[1, 17] = -np.inf
+    S[2, 5] = np.inf
+    ids = qsa.block_topk(to_dev(S, dev), 1500).cpu().numpy()
+    assert np.array_equal(ids, o.topk_f32(S, 1500))
+
+
+@pytest.mark.parametrize("active,k", [(10, 10), (10, 13), (1, 4), (0, 3)])
+def test_topk_k_at_least_active(dev, o, active, k):
+    S = _tie_heavy(3, max(active, 1), seed=3)[:, :active].copy()
+    ids = qsa.block_topk(to_dev(S, dev), k).cpu().numpy()
+    assert np.array_equal(ids, o.topk_f32(S, k))
+
+
+def test_outputs_stay_in_bounds(dev, o):
+    """Canary words after the scores and ids must survive; capacity rows
+    (NaN) must not be read."""
+    W = w.normal_case(nq=37, active=2051, k=100, max_blocks=2300)
+    q, kb = to_dev(W.q, dev), to_dev(W.kblk, dev)
+    n_s, n_i = W.nq * W.active, W.nq * W.k
+    buf_s = torch.full((n_s + 64,), 12345.0, dtype=torch.float32, device=dev)
+    buf_i = torch.full((n_i + 64,), 777, dtype=torch.int32, device=dev)
+    s = buf_s[:n_s].view(W.nq, W.active)
+    ids = buf_i[:n_i].view(W.nq, W.k)
+    qsa.block_scores(q, kb, W.active, out=s)
+    qsa.block_topk(s, W.k, out=ids)
+    assert torch.all(buf_s[n_s:] == 12345.0) and torch.all(buf_i[n_i:] == 777)
+    check_select(o, W, s)
+
+
+def test_side_stream(dev, o):
+    W = w.normal_case(nq=9, active=3000, k=50)
+    st = torch.cuda.Stream(dev)
+    q, kb = to_dev(W.q, dev), to_dev(W.kblk, dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        s, ids = qsa.block_select(q, kb, W.active, W.k)
+    st.synchronize()
+    check_select(o, W, s)
+
+
+def test_no_kernel_reported_a_timeout(dev):
+    assert qsa.device_error(dev) == 0
