@@ -1,0 +1,405 @@
+"""Benchmark: QSA block scoring + exact top-k at 262,144 cells x 256 queries.
+
+One step = one pass of the whole selection path on resident inputs:
+qsa_block_scores (256 queries x 4 heads x D=128 against 65,536 active
+summary keys of a 65,538-block capacity) then qsa_block_topk (k=512). The
+inputs are the seeded synthetic full-capacity workload: q and keys
+Student-t(3) at unit variance.
+
+Prints ONE JSON line (rank 0). ``value`` is query-blocks per second over all
+ranks; ``ms_per_step`` the device time of one step (CUDA events on the
+launching stream, L2 flushed before every step and the flush untimed);
+``roofline`` describes the dominant kernel; ``e2e`` repeats the measurement
+through the public API with host buffers (pinned H2D of q and the active
+keys, D2H of the ids, all inside the timed region); ``cpu_baseline`` times
+the CPU oracle on this machine's cores.
+
+``--impl reference`` times the CPU oracle itself as the reference arm.
+Under torchrun each rank runs an independent replica (no collective on the
+data path); timing is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "score+top-k ms/call and query·blocks/s at 256 queries, 262K cells; % of roofline"
+UNIT = "query·blocks/s"
+WORKLOAD = ("full_262k: 262,144 cells = 65,536 active blocks (capacity 65,538), nq=256 queries x 4 heads "
+            "x D=128 fp32, q and keys Student-t(3) at unit variance, top k=512")
+PROFILES = os.path.join(ROOT, "profiles")
+CSRC = os.path.join(ROOT, "sparse_attention_kv_qsa_gb300", "csrc")
+
+# Algorithmic traffic and work at this workload (the selection path's
+# definition, counted once): q 256*4*128*4 B, keys 65,536*128*4 B, scores
+# 256*65,536*4 B written then read, ids 256*512*4 B written.
+NQ, ACTIVE, MAX_BLOCKS, K = 256, 65536, 65538, 512
+
+
+def algorithmic(nq: int, active: int, k: int) -> dict:
+    q_b = nq * 4 * 128 * 4
+    key_b = active * 128 * 4
+    s_b = nq * active * 4
+    id_b = nq * k * 4
+    return {
+        "score_bytes": q_b + key_b + s_b,
+        "topk_bytes": s_b + id_b,
+        "step_bytes": q_b + key_b + 2 * s_b + id_b,
+        "flops_per_head_form": 1024 * nq * active,
+        "flops_head_summed": 256 * nq * active,
+    }
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "sm_max_mhz": float(d.get("sm_max_mhz", 2070.0)), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def source_sha(fname: str) -> str:
+    with open(os.path.join(CSRC, fname), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, fname: str):
+    """DRAM bytes per launch of `kernel` from profiles/dram_traffic.txt, or
+    None when absent or taken on a different source of the kernel."""
+    p = os.path.join(PROFILES, "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    sha = source_sha(fname)
+    with open(p) as f:
+        for line in f:
+            m = dict(re.findall(r"(\w+)=(\S+)", line))
+            if m.get("kernel") == kernel and m.get("source_sha") == sha and "dram_bytes_per_launch" in m:
+                return float(m["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l.split(", ") for l in self.lines if l and l[0].isdigit()]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4) if len(r) > 5 + j and r[5 + j] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def cpu_oracle_baseline(W, budget_s: float = 20.0, nq_sample: int | None = None) -> dict:
+    import oracle
+    o = oracle.get()
+    cores = o.default_threads()
+    nq_s = W.nq if nq_sample is None else nq_sample
+    t0 = time.perf_counter()
+    S = o.scores(W.q[:nq_s], W.kblk, W.active, nthreads=cores)
+    o.topk_f64(S, W.k, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": nq_s * W.active / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{nq_s} queries x {W.active} blocks, k={W.k}: FP64 scoring + full-sort top-k, "
+                      f"{cores} threads, one pass, {dt:.2f} s"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return None
+    from sparse_attention_kv_qsa_gb300 import workloads
+    import oracle
+    W = workloads.full(k=args.k)
+    o = oracle.get()
+    cores = o.default_threads()
+    # each step: a bounded sample sized so warm-up + steps take ~<= 2 minutes
+    per_step = max(0.02, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    t0 = time.perf_counter()
+    S = o.scores(W.q[:cores], W.kblk, W.active, nthreads=cores)
+    o.topk_f64(S, W.k, nthreads=cores)
+    t_rows = (time.perf_counter() - t0)
+    # sample cores queries x `blocks` blocks per step
+    blocks = int(max(2 * W.k, min(W.active, W.active * per_step / max(t_rows, 1e-9))))
+    nq_s = cores
+
+    def step():
+        S = o.scores(W.q[:nq_s], W.kblk, blocks, nthreads=cores)
+        o.topk_f64(S, W.k, nthreads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = args.steps * nq_s * blocks / dt
+    sample = (f"{nq_s} queries x {blocks} blocks per step (k={W.k}), FP64 scoring + full-sort top-k on "
+              f"{cores} host threads")
+    return {"metric": METRIC, "impl": "reference", "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "nq": NQ, "active_blocks": ACTIVE,
+                                            "max_blocks": MAX_BLOCKS, "k": args.k},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--k", type=int, default=K)
+    ap.add_argument("--scorer", default="default", choices=["default", "ffma"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-flush", action="store_true", help="warm L2 (back-to-back steps)")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import sparse_attention_kv_qsa_gb300 as qsa
+    from sparse_attention_kv_qsa_gb300 import workloads
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    W = workloads.full(k=args.k)
+    q = torch.from_numpy(W.q).to(dev)
+    kblk = torch.from_numpy(W.kblk).to(dev)
+    scores = torch.empty((W.nq, W.active), dtype=torch.float32, device=dev)
+    ids = torch.empty((W.nq, W.k), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+
+    if args.scorer == "ffma":
+        def score():
+            qsa.block_scores_ffma(q, W.active, kblk=kblk, out=scores)
+    else:
+        def score():
+            qsa.block_scores(q, kblk, W.active, out=scores)
+
+    def topk():
+        qsa.block_topk(scores, W.k, out=ids)
+
+    for i in range(args.warmup):
+        if not args.no_flush:
+            flush.fill_(float(i))
+        score()
+        topk()
+    torch.cuda.synchronize()
+
+    K_ = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_)]
+    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(K_):
+        if not args.no_flush:
+            flush.fill_(float(i))
+        ev[i][0].record(stream)
+        score()
+        ev[i][1].record(stream)
+        topk()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    t_score = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K_)]
+    t_topk = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K_)]
+    step_ms_local = sum(a + b for a, b in zip(t_score, t_topk)) / K_
+    step_ms = max_over_ranks(step_ms_local, world, dev)
+    if qsa.device_error(dev) != 0:
+        raise SystemExit("a QSA kernel reported a timed-out wait; results invalid")
+
+    alg = algorithmic(W.nq, W.active, W.k)
+    peaks = load_peaks()
+    units_per_step = W.nq * W.active
+    value = world * units_per_step / (step_ms * 1e-3)
+    score_us = 1e3 * statistics.mean(t_score)
+    topk_us = 1e3 * statistics.mean(t_topk)
+
+    # Dominant kernel and its roofline.
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    fp32_peak_tflops = sm_count * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+    scorer_kernel, scorer_src = (("scores_ffma_kernel", "scores_ffma.cu") if args.scorer == "ffma"
+                                 else qsa.default_scorer_kernel())
+    if score_us >= topk_us:
+        if scorer_kernel == "scores_ffma_kernel":
+            achieved = alg["flops_head_summed"] / (score_us * 1e-6) / 1e12
+            roof = {"kernel": scorer_kernel, "bound": "alu", "achieved": achieved, "peak": fp32_peak_tflops,
+                    "unit": "TFLOP/s", "frac": achieved / fp32_peak_tflops,
+                    "peak_note": f"FP32 FMA: {sm_count} SMs x 128 lanes x 2 FLOP x {peaks['sm_max_mhz']:.0f} MHz"}
+        else:
+            achieved = alg["score_bytes"] / (score_us * 1e-6) / 1e9
+            roof = {"kernel": scorer_kernel, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                    "peak_note": f"{peaks['source']} HBM copy bandwidth"}
+        roof["traffic"] = recorded_traffic(scorer_kernel, scorer_src)
+    else:
+        achieved = alg["topk_bytes"] / (topk_us * 1e-6) / 1e9
+        roof = {"kernel": "topk_cluster_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "peak_note": f"{peaks['source']} HBM copy bandwidth",
+                "traffic": recorded_traffic("topk_cluster_kernel", "topk.cu")}
+    floor_us = 1e6 * alg["step_bytes"] / (peaks["hbm_gbs"] * 1e9)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K_, "warmup": args.warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "nq": W.nq, "active_blocks": W.active, "max_blocks": W.max_blocks,
+                   "k": W.k, "scorer": scorer_kernel,
+                   "l2": "warm (no flush)" if args.no_flush else
+                         f"flushed before every step by a {2 * l2 >> 20} MiB write, flush untimed",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "kernels_us": {"scores": score_us, "topk": topk_us,
+                       "scores_p50": 1e3 * statistics.median(t_score), "topk_p50": 1e3 * statistics.median(t_topk)},
+        "roofline": roof,
+        "step_roofline": {"floor_us": floor_us, "frac": floor_us / (step_ms * 1e3),
+                          "note": "algorithmic step bytes at the HBM peak (the step's binding roof when "
+                                  "scoring runs on tensor cores)"},
+        "gpu_launches": 2 * K_,
+        "clocks": clocks,
+        "pages_context": {"r9700_score_plus_topk_ms": 2.8, "r9700_qblocks_per_s": 6.0e9,
+                          "note": "AMD R9700 (gfx1201) numbers from the pages; context only"},
+    }
+
+    # End to end through the public API with host buffers.
+    if not args.no_e2e:
+        q_h = torch.from_numpy(W.q).pin_memory()
+        k_h = torch.from_numpy(np.ascontiguousarray(W.kblk[:W.active])).pin_memory()
+        ids_h = torch.empty((W.nq, W.k), dtype=torch.int32).pin_memory()
+        q_d = torch.empty_like(q_h, device=dev)
+        k_d = torch.empty((W.max_blocks, 128), dtype=torch.float32, device=dev)
+
+        def e2e_step():
+            q_d.copy_(q_h, non_blocking=True)
+            k_d[:W.active].copy_(k_h, non_blocking=True)
+            s = qsa.block_scores(q_d, k_d, W.active, out=scores)
+            qsa.block_topk(s, W.k, out=ids)
+            ids_h.copy_(ids, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e = min(args.e2e_steps, K_)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for i in range(n_e):
+            if not args.no_flush:
+                flush.fill_(float(i))
+            e0.record(stream)
+            e2e_step()
+            e1.record(stream)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1)
+        e_ms = max_over_ranks(tot / n_e, world, dev)
+        assert np.array_equal(ids_h.numpy(), ids.cpu().numpy())
+        line["e2e"] = {"value": world * units_per_step / (e_ms * 1e-3), "unit": UNIT, "ms_per_step": e_ms,
+                       "steps": n_e, "h2d_bytes_per_step": q_h.numel() * 4 + k_h.numel() * 4,
+                       "d2h_bytes_per_step": ids_h.numel() * 4}
+
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_baseline(W)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -12,5 +12,6 @@ from .qsa import (  # noqa: F401
     block_scores_q8,
     block_select,
     block_topk,
+    default_scorer_kernel,
     device_error,
 )

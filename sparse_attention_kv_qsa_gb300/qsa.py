@@ -182,3 +182,8 @@ def device_error(device: torch.device | None = None) -> int:
     stream = torch.cuda.current_stream(device).cuda_stream
     _check(lib().qsa_get_device_error(ctypes.byref(code), stream), "qsa_get_device_error")
     return int(code.value)
+
+
+def default_scorer_kernel() -> tuple[str, str]:
+    """(kernel name, source file) of the scorer behind qsa_block_scores."""
+    return "scores_ffma_kernel", "scores_ffma.cu"
