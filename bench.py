@@ -330,10 +330,10 @@ def main():
         roof["traffic"] = recorded_traffic(scorer_kernel, scorer_src)
     else:
         achieved = alg["topk_bytes"] / (topk_us * 1e-6) / 1e9
-        roof = {"kernel": "topk_cluster_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+        roof = {"kernel": "topk_row_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "peak_note": f"{peaks['source']} HBM copy bandwidth",
-                "traffic": recorded_traffic("topk_cluster_kernel", "topk.cu")}
+                "traffic": recorded_traffic("topk_row_kernel", "topk.cu")}
     floor_us = 1e6 * alg["step_bytes"] / (peaks["hbm_gbs"] * 1e9)
 
     line = {

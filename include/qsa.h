@@ -28,8 +28,9 @@
  *    the stream, as for any kernel.
  *  - Calls with no work (nq == 0, or active_blocks == 0 for the scorers)
  *    return QSA_OK without touching memory; pointers may then be NULL.
- *  - Inputs are expected to be finite. A NaN score ranks below every number
- *    in the top-k; -0.0 and +0.0 are equal (and therefore tie).
+ *  - Inputs are expected to be finite. In the top-k a NaN score counts as
+ *    -infinity (it ties with -inf, below every finite score); -0.0 and +0.0
+ *    are equal (and therefore tie).
  */
 #ifndef QSA_H
 #define QSA_H
@@ -52,7 +53,7 @@ typedef enum {
 #define QSA_D 128
 #define QSA_HEADS 4
 
-/* Largest active_blocks the top-k accepts (8 CTAs x 49,152 keys). */
+/* Largest active_blocks the top-k accepts (its per-row bitmaps live in shared memory). */
 #define QSA_TOPK_MAX_ACTIVE 393216
 
 /*

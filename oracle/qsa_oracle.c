@@ -29,7 +29,8 @@
  * Selection: sort the pairs (S, id) by S descending, then id ascending (a
  * strict total order), keep the first min(k, active) ids, sort them
  * ascending, and fill the remaining k - active slots (if any) with -1. A NaN
- * score ranks below every number; -0.0 and +0.0 compare equal (and so tie).
+ * score counts as -infinity (so it ties with -inf and ranks below every
+ * finite score); -0.0 and +0.0 compare equal (and so tie).
  */
 #include "qsa_oracle.h"
 
@@ -158,13 +159,15 @@ void qsa_oracle_scores_q8(const float *q, const int8_t *kq8, const uint16_t *ksc
 
 typedef struct { double s; int32_t id; } scored_id;
 
-/* Strict total order: higher score first, then lower id; NaN below all. */
+/* A NaN score counts as -infinity (it ties with -inf); -0.0 == +0.0. */
+static double rank_value(double s) { return isnan(s) ? -INFINITY : s; }
+
+/* Strict total order: higher score first, then lower id. */
 static int by_score_desc_id_asc(const void *pa, const void *pb) {
     const scored_id *a = (const scored_id *)pa, *b = (const scored_id *)pb;
-    int a_nan = isnan(a->s), b_nan = isnan(b->s);
-    if (a_nan != b_nan) return a_nan ? 1 : -1;
-    if (!a_nan && a->s > b->s) return -1;
-    if (!a_nan && a->s < b->s) return 1;
+    double va = rank_value(a->s), vb = rank_value(b->s);
+    if (va > vb) return -1;
+    if (va < vb) return 1;
     return (a->id < b->id) ? -1 : (a->id > b->id);
 }
 

@@ -17,7 +17,7 @@ cudaError_t launch_scores_ffma(const float *q, const float *kblk, const int8_t *
                                const uint16_t *kscale, int nq, int active, float *scores,
                                cudaStream_t stream);
 
-// Exact top-k (k < active); rows handled by thread-block clusters.
+// Exact top-k (k < active); one CTA per row.
 cudaError_t launch_topk(const float *scores, int nq, int active, int k, int32_t *ids,
                         cudaStream_t stream);
 

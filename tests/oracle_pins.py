@@ -42,8 +42,8 @@ def _dominates(vals: np.ndarray, subset: tuple[int, ...]) -> bool:
     """True iff every member beats every non-member (value desc, id asc)."""
     inside = set(subset)
     def rank(i):
-        v = vals[i]
-        return (0 if np.isnan(v) else 1, -0.0 if np.isnan(v) else float(v), -i)
+        v = -np.inf if np.isnan(vals[i]) else float(vals[i])   # NaN counts as -inf
+        return (v, -i)
     for i in inside:
         for j in range(len(vals)):
             if j not in inside and not rank(i) > rank(j):
@@ -69,6 +69,7 @@ def pin_brute_force_topk(o) -> None:
         rows.append(r.integers(-2, 3, size=n).astype(np.float64))       # many ties
         rows.append(np.where(r.random(n) < 0.5, 0.0, -0.0))             # +-0 ties
     rows.append(np.array([1.0, np.nan, 1.0, -np.inf, np.inf, np.nan, -1.0]))
+    rows.append(np.array([np.nan, -np.inf, 2.0, np.nan, -np.inf]))
     for vals in rows:
         n = len(vals)
         for k in range(1, n + 3):

@@ -150,6 +150,22 @@ def test_topk_exact_on_given_scores(dev, o, nq, active, k):
     parity.check_ids_valid(ids, active, k)
 
 
+@pytest.mark.parametrize("m", [2047, 2048, 2049, 6000])
+def test_topk_candidate_list_capacity(dev, o, m):
+    """The leading-digit bin holds m keys: at and below the candidate-list
+    capacity (2,048) the refinement runs on the list, above it on the row."""
+    active = 10003
+    S = np.full((2, active), -1.0, dtype=np.float32)
+    S[:, :100] = 4.0 + np.arange(100, dtype=np.float32) * 0.01
+    vals = (1.0 + np.arange(m, dtype=np.float64) * 2.0 ** -20).astype(np.float32)
+    S[0, 100:100 + m] = vals
+    S[1, 100:100 + m] = vals[::-1]
+    S[1, 100 + m // 3] = S[1, 100 + m // 2]          # an exact tie inside the bin
+    for k in (100 + m // 2, 100 + m - 1, 101):
+        ids = qsa.block_topk(to_dev(S, dev), k).cpu().numpy()
+        assert np.array_equal(ids, o.topk_f32(S, k)), (m, k)
+
+
 def test_topk_nan_ranks_lowest(dev, o):
     S = _tie_heavy(3, 3001, seed=5)
     S[0, ::3] = np.nan

@@ -21,9 +21,8 @@ MUTANTS = {
                      "for (int d = 1; d < QSA_D; ++d) dot += (double)qh[d] * (double)kb[d]"),
     "tie_to_higher_id": ("return (a->id < b->id) ? -1 : (a->id > b->id);",
                          "return (a->id > b->id) ? -1 : (a->id < b->id);"),
-    "ascending_scores": ("if (!a_nan && a->s > b->s) return -1;", "if (!a_nan && a->s < b->s) return -1;"),
-    "nan_ranks_first": ("if (a_nan != b_nan) return a_nan ? 1 : -1;",
-                        "if (a_nan != b_nan) return a_nan ? -1 : 1;"),
+    "ascending_scores": ("if (va > vb) return -1;", "if (va < vb) return -1;"),
+    "nan_ranks_first": ("isnan(s) ? -INFINITY : s", "isnan(s) ? INFINITY : s"),
     "ids_in_rank_order": ("qsort(out, (size_t)m, sizeof(int32_t), by_id_asc);", ""),
     "zero_padding": ("for (long j = m; j < c->k; ++j) out[j] = -1;",
                      "for (long j = m; j < c->k; ++j) out[j] = 0;"),
