@@ -54,7 +54,7 @@ qsa_status qsa_block_scores(const float *q, const float *kblk, int nq, int max_b
     qsa_status s = check_score_args(q, nq, max_blocks, active_blocks, scores);
     if (s != QSA_OK || nq == 0 || active_blocks == 0) return s;
     if (kblk == nullptr || !aligned16(kblk)) return QSA_ERR_INVALID;
-    return from_cuda(qsa::launch_scores_ffma(q, kblk, nullptr, nullptr, nq, active_blocks, scores, stream));
+    return from_cuda(qsa::launch_scores_tc(q, kblk, nullptr, nullptr, nq, active_blocks, scores, stream));
 }
 
 qsa_status qsa_block_scores_q8(const float *q, const int8_t *kblk_q8, const uint16_t *kscale_f16, int nq,
@@ -63,8 +63,7 @@ qsa_status qsa_block_scores_q8(const float *q, const int8_t *kblk_q8, const uint
     if (s != QSA_OK || nq == 0 || active_blocks == 0) return s;
     if (kblk_q8 == nullptr || kscale_f16 == nullptr || !aligned16(kblk_q8)) return QSA_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(kscale_f16) & 1u) != 0) return QSA_ERR_INVALID;
-    return from_cuda(
-        qsa::launch_scores_ffma(q, nullptr, kblk_q8, kscale_f16, nq, active_blocks, scores, stream));
+    return from_cuda(qsa::launch_scores_tc(q, nullptr, kblk_q8, kscale_f16, nq, active_blocks, scores, stream));
 }
 
 qsa_status qsa_block_scores_ffma(const float *q, const float *kblk, const int8_t *kblk_q8,
@@ -99,7 +98,11 @@ qsa_status qsa_block_topk(const float *scores, int nq, int active_blocks, int k,
 qsa_status qsa_get_device_error(uint32_t *code, cudaStream_t stream) {
     if (code == nullptr) return QSA_ERR_INVALID;
     *code = 0;
-    return from_cuda(qsa::topk_error_read_clear(code, stream));
+    uint32_t a = 0, b = 0;
+    cudaError_t e = qsa::topk_error_read_clear(&a, stream);
+    if (e == cudaSuccess) e = qsa::tc_error_read_clear(&b, stream);
+    *code = a | (b << 8);
+    return from_cuda(e);
 }
 
 const char *qsa_status_string(qsa_status status) {

@@ -17,6 +17,11 @@ cudaError_t launch_scores_ffma(const float *q, const float *kblk, const int8_t *
                                const uint16_t *kscale, int nq, int active, float *scores,
                                cudaStream_t stream);
 
+// Scores on the tensor cores (3-way bf16 split; int8 keys: one slice).
+// Exactly one of kblk / (kq8, kscale) is non-null.
+cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,
+                             int nq, int active, float *scores, cudaStream_t stream);
+
 // Exact top-k (k < active); one CTA per row.
 cudaError_t launch_topk(const float *scores, int nq, int active, int k, int32_t *ids,
                         cudaStream_t stream);
@@ -26,5 +31,6 @@ cudaError_t launch_topk_all(int nq, int active, int k, int32_t *ids, cudaStream_
 
 // Error words of the kernels (bounded waits that gave up); read and clear.
 cudaError_t topk_error_read_clear(uint32_t *word, cudaStream_t stream);
+cudaError_t tc_error_read_clear(uint32_t *word, cudaStream_t stream);
 
 }  // namespace qsa

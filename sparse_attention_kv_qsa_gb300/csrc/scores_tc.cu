@@ -1,0 +1,414 @@
+// Block scoring on the 5th-generation tensor cores (tcgen05, TMEM), with
+// fp32 operands split exactly into three bf16 slices.
+//
+//   score[i][b] = sum_{h<4} sum_{d<128} q[i][h][d] * key[b][d]
+//               = sum_{d<128} s[i][d] * key[b][d],   s[i][d] = ((q0 + q1) + q2) + q3
+//
+// Passages: "#3108 optimize exact QSA block scoring and top-k selection on
+// gfx12", Summary items 1 and 4 (the 4-head block score); "#337 gfx12 QSA
+// select", What item 2 (a tensor-core scorer splits each fp32 operand into
+// three exact 8-bit-mantissa bf16 slices hi/mid/lo, sums the six products of
+// order <= 2, keeps hi*hi in its own accumulator and the five corrections in
+// another, and adds the two once at the end).
+//
+// Split: hi = x with the low 16 bits cleared, r = x - hi (exact), mid = r
+// with the low 16 bits cleared, lo = r - mid (exact, at most 8 significant
+// bits), so x = hi + mid + lo exactly for normal x. The dropped products
+// (mid*lo, lo*mid, lo*lo) are of relative order 2^-24.
+//
+// int8 keys (times one binary16 scale per block) are exact in one bf16 slice,
+// so that form needs three products; the scale multiplies the sum.
+//
+// GB300 mapping, one persistent CTA per SM, CTAs grouped by 128 queries:
+//  - MMA D[query][block] = A[query][d] . B[block][d], M = 128 queries,
+//    N = 64 blocks per tile, K = 16 per instruction.
+//  - A: the group's head-summed queries, three slices resident in TMEM
+//    (192 of the 512 columns), written once by the epilogue warps.
+//  - B: key tiles. A producer warp streams raw key rows (contiguous, 16 KiB
+//    = 32 fp32 rows per copy) into a 4-slot shared-memory ring with bulk
+//    async copies; 8 converter warps split them into three 128-byte-swizzled
+//    K-major bf16 slices in a 2-stage ring (2 x 48 KiB).
+//  - One thread issues tcgen05.mma into two accumulators (hi*hi;
+//    corrections) per tile, double-buffered (4 x 64 TMEM columns), and
+//    signals stages with tcgen05.commit.
+//  - 4 epilogue warps (thread = query row) read the accumulators, add them,
+//    write the row's 64 scores to a padded shared-memory row and send it to
+//    global memory with one 256-byte bulk async store per row.
+//  - Key rows at or beyond `active` are never read; the grid comes from
+//    `active` and nq alone.
+// Every mbarrier wait is bounded; a timeout sets the error word.
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "qsa_internal.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int TILE_N = 64;                     // key blocks per tile (MMA N)
+constexpr int QGROUP = 128;                    // queries per CTA group (MMA M)
+constexpr int RAW_ROWS = 32;                   // key rows per raw copy
+constexpr int RAW_SLOTS = 4;
+constexpr int RAW_SLOT_BYTES = RAW_ROWS * D * 4;    // 16 KiB (fp32 rows)
+constexpr int KS_SUB_BYTES = TILE_N * 128;          // one slice, one K-half: 64 rows x 128 B
+constexpr int KS_STAGE_BYTES = 6 * KS_SUB_BYTES;    // 3 slices x 2 K-halves = 48 KiB
+constexpr int OUT_ROW_BYTES = TILE_N * 4 + 16;      // padded: conflict-free 16-byte stores
+constexpr int PRODUCER_WARP = 0, MMA_WARP = 1;
+constexpr int EPI_WARP0 = 2, EPI_WARPS = 4;
+constexpr int CONV_WARP0 = EPI_WARP0 + EPI_WARPS, CONV_WARPS = 8;
+constexpr int TC_THREADS = (CONV_WARP0 + CONV_WARPS) * 32;   // 448
+constexpr int CONV_THREADS = CONV_WARPS * 32;
+constexpr int EPI_THREADS = EPI_WARPS * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t A_COLS_PER_SLICE = D / 2;   // 64 columns: 128 bf16 packed in pairs
+constexpr uint32_t ACC_COL0 = 3 * A_COLS_PER_SLICE;   // 192: accumulators after the query slices
+constexpr uint32_t ACC_STAGE_COLS = 2 * TILE_N;       // hi*hi and corrections, 64 columns each
+
+// Shared memory, from a 1,024-byte-aligned base.
+constexpr int KS_OFF = 0;                                   // 2 x 48 KiB
+constexpr int RAW_OFF = KS_OFF + 2 * KS_STAGE_BYTES;        // 4 x 16 KiB
+constexpr int OUT_OFF = RAW_OFF + RAW_SLOTS * RAW_SLOT_BYTES;
+constexpr int BAR_OFF = OUT_OFF + QGROUP * OUT_ROW_BYTES;
+
+struct TcBarriers {
+    uint64_t raw_full[RAW_SLOTS];   // producer -> converters (bulk copy landed)
+    uint64_t raw_empty[RAW_SLOTS];  // converters -> producer
+    uint64_t ks_full[2];            // converters -> MMA: key slices written
+    uint64_t ks_empty[2];           // MMA -> converters: key slices consumed
+    uint64_t acc_full[2];           // MMA -> epilogue
+    uint64_t acc_empty[2];          // epilogue -> MMA
+    uint64_t a_ready;               // query slices in TMEM
+    uint32_t tmem_base;
+};
+
+constexpr size_t TC_SMEM = BAR_OFF + sizeof(TcBarriers) + 1024;
+
+__device__ uint32_t g_tc_error;
+
+__device__ __forceinline__ void wait_or_flag(uint64_t *bar, uint32_t parity) {
+    if (!mbar_wait(bar, parity)) atomicOr(&g_tc_error, 1u);
+}
+
+// x = hi + mid + lo, each an fp32 bit pattern whose low 16 bits are zero
+// (a bf16 in the upper half).
+__device__ __forceinline__ void split3(float x, uint32_t &hi, uint32_t &mid, uint32_t &lo) {
+    hi = __float_as_uint(x) & 0xFFFF0000u;
+    const float r = __fsub_rn(x, __uint_as_float(hi));
+    mid = __float_as_uint(r) & 0xFFFF0000u;
+    lo = __float_as_uint(__fsub_rn(r, __uint_as_float(mid)));
+}
+
+// bf16x2 word from the upper halves of two fp32 patterns (a in the low half).
+__device__ __forceinline__ uint32_t pack2(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632); }
+
+// Byte offset of 16-byte chunk c (8 bf16) of row r in a 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    return static_cast<uint32_t>(r) * 128u + (static_cast<uint32_t>(c ^ (r & 7)) << 4);
+}
+
+template <bool kInt8>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    scores_tc_kernel(const float *__restrict__ q, const float *__restrict__ kblk,
+                     const int8_t *__restrict__ kq8, const __half *__restrict__ kscale, int nq, int active,
+                     int ntiles, int ctas_per_group, float *__restrict__ scores) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    const uint32_t base = raw + pad;
+    TcBarriers *bars = reinterpret_cast<TcBarriers *>(smem_raw + pad + BAR_OFF);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int group = blockIdx.x / ctas_per_group;
+    const int j0 = blockIdx.x % ctas_per_group;
+    const int q0 = group * QGROUP;
+    const int qn = min(QGROUP, nq - q0);
+    const int nlocal = j0 < ntiles ? (ntiles - 1 - j0) / ctas_per_group + 1 : 0;
+    constexpr int ROW_BYTES = kInt8 ? D : D * 4;
+    const char *keys = kInt8 ? reinterpret_cast<const char *>(kq8) : reinterpret_cast<const char *>(kblk);
+    auto tile_b0 = [&](int li) { return (j0 + li * ctas_per_group) * TILE_N; };
+
+    if (tid == 0) {
+        for (int s = 0; s < RAW_SLOTS; ++s) {
+            mbar_init(&bars->raw_full[s], 1);
+            mbar_init(&bars->raw_empty[s], CONV_THREADS);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->ks_full[s], CONV_THREADS);
+            mbar_init(&bars->ks_empty[s], 1);
+            mbar_init(&bars->acc_full[s], 1);
+            mbar_init(&bars->acc_empty[s], EPI_THREADS);
+        }
+        mbar_init(&bars->a_ready, EPI_THREADS);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == MMA_WARP) {
+        tmem_alloc(&bars->tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();  // barriers initialised, TMEM allocated
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == PRODUCER_WARP) {
+        // ---- raw key rows -> ring (bulk async copies) --------------------------
+        if (lane == 0) {
+            const int npieces = 2 * nlocal;
+            for (int p = 0; p < npieces; ++p) {
+                const int slot = p & (RAW_SLOTS - 1);
+                wait_or_flag(&bars->raw_empty[slot], ((p / RAW_SLOTS) & 1) ^ 1);
+                const int row0 = tile_b0(p >> 1) + (p & 1) * RAW_ROWS;
+                const int rows = min(RAW_ROWS, active - row0);
+                if (rows > 0) {
+                    const uint32_t bytes = static_cast<uint32_t>(rows * ROW_BYTES);
+                    mbar_arrive_expect_tx(&bars->raw_full[slot], bytes);
+                    bulk_g2s(smem_raw + pad + RAW_OFF + slot * RAW_SLOT_BYTES,
+                             keys + static_cast<size_t>(row0) * ROW_BYTES, bytes, &bars->raw_full[slot]);
+                } else {
+                    mbar_arrive(&bars->raw_full[slot]);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        // ---- MMA issuer ----------------------------------------------------------
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(QGROUP, TILE_N);
+            wait_or_flag(&bars->a_ready, 0);
+            tc_fence_after_sync();
+            for (int li = 0; li < nlocal; ++li) {
+                const int st = li & 1, use = li >> 1;
+                wait_or_flag(&bars->acc_empty[st], (use & 1) ^ 1);
+                wait_or_flag(&bars->ks_full[st], use & 1);
+                tc_fence_after_sync();
+                const uint32_t d0 = tmem + ACC_COL0 + st * ACC_STAGE_COLS, d1 = d0 + TILE_N;
+                const uint32_t kbase = base + KS_OFF + st * KS_STAGE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int khalf = kk >> 2, ks = kk & 3;
+                    const uint32_t acc = kk == 0 ? 0u : 1u;
+                    // key slice s, K-half h: kbase + (2*s + h) * KS_SUB_BYTES
+                    const uint32_t kb = kbase + khalf * KS_SUB_BYTES + ks * 32;
+                    const uint64_t B0 = sw128_kmajor_desc(kb);
+                    const uint32_t A0 = tmem + kk * 8, A1 = A0 + A_COLS_PER_SLICE, A2 = A0 + 2 * A_COLS_PER_SLICE;
+                    tc_mma_bf16_ta(d0, A0, B0, idesc, acc);      // hi . hi
+                    tc_mma_bf16_ta(d1, A1, B0, idesc, acc);      // mid . hi
+                    tc_mma_bf16_ta(d1, A2, B0, idesc, 1u);       // lo . hi
+                    if constexpr (!kInt8) {
+                        const uint64_t B1 = sw128_kmajor_desc(kb + 2 * KS_SUB_BYTES);
+                        const uint64_t B2 = sw128_kmajor_desc(kb + 4 * KS_SUB_BYTES);
+                        tc_mma_bf16_ta(d1, A0, B1, idesc, 1u);   // hi . mid
+                        tc_mma_bf16_ta(d1, A1, B1, idesc, 1u);   // mid . mid
+                        tc_mma_bf16_ta(d1, A0, B2, idesc, 1u);   // hi . lo
+                    }
+                }
+                tc_commit(&bars->ks_empty[st]);
+                tc_commit(&bars->acc_full[st]);
+            }
+        }
+        __syncwarp();
+    } else if (warp < CONV_WARP0) {
+        // ---- epilogue warps: query slices into TMEM, then scores out -------------
+        const int quarter = warp & 3;                       // TMEM lanes 32*quarter .. +31
+        const int row = 32 * quarter + lane;                // query row within the group
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+        {
+            const bool live = row < qn;
+            const float4 *p = reinterpret_cast<const float4 *>(q + static_cast<size_t>(q0 + (live ? row : 0)) * (HEADS * D));
+            for (int c = 0; c < D / 8; ++c) {               // 8 d per step: 4 packed columns per slice
+                float x[8];
+                if (live) {
+                    float4 a[4][2];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        a[h][0] = __ldg(p + h * (D / 4) + 2 * c);
+                        a[h][1] = __ldg(p + h * (D / 4) + 2 * c + 1);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float v0 = e < 4 ? (&a[0][0].x)[e] : (&a[0][1].x)[e - 4];
+                        const float v1 = e < 4 ? (&a[1][0].x)[e] : (&a[1][1].x)[e - 4];
+                        const float v2 = e < 4 ? (&a[2][0].x)[e] : (&a[2][1].x)[e - 4];
+                        const float v3 = e < 4 ? (&a[3][0].x)[e] : (&a[3][1].x)[e - 4];
+                        x[e] = __fadd_rn(__fadd_rn(__fadd_rn(v0, v1), v2), v3);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = 0.f;
+                }
+                uint32_t h[8], m[8], l[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) split3(x[e], h[e], m[e], l[e]);
+                const uint32_t col = lane_addr + 4 * c;
+                tmem_st4(col, pack2(h[0], h[1]), pack2(h[2], h[3]), pack2(h[4], h[5]), pack2(h[6], h[7]));
+                tmem_st4(col + A_COLS_PER_SLICE, pack2(m[0], m[1]), pack2(m[2], m[3]), pack2(m[4], m[5]),
+                         pack2(m[6], m[7]));
+                tmem_st4(col + 2 * A_COLS_PER_SLICE, pack2(l[0], l[1]), pack2(l[2], l[3]), pack2(l[4], l[5]),
+                         pack2(l[6], l[7]));
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&bars->a_ready);
+        }
+
+        const bool bulk_ok = (active & 3) == 0;             // 16-byte aligned row segments
+        const uint32_t out_row = base + OUT_OFF + row * OUT_ROW_BYTES;
+        float *qrow = scores + static_cast<size_t>(q0 + row) * active;
+        for (int li = 0; li < nlocal; ++li) {
+            const int st = li & 1, use = li >> 1;
+            const int b0 = tile_b0(li);
+            const int nb = min(TILE_N, active - b0);
+            wait_or_flag(&bars->acc_full[st], use & 1);
+            tc_fence_after_sync();
+            const uint32_t t0 = lane_addr + ACC_COL0 + st * ACC_STAGE_COLS;
+            uint32_t x0[32], x1[32];
+            float v[TILE_N];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                tmem_ld32(t0 + 32 * half, x0);
+                tmem_ld32(t0 + TILE_N + 32 * half, x1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    v[32 * half + j] = __fadd_rn(__uint_as_float(x0[j]), __uint_as_float(x1[j]));
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&bars->acc_empty[st]);              // TMEM free for the tile after next
+            if constexpr (kInt8) {
+#pragma unroll
+                for (int j = 0; j < TILE_N; ++j)
+                    if (j < nb) v[j] = __fmul_rn(v[j], __half2float(kscale[b0 + j]));
+            }
+            if (row < qn) {
+                if (bulk_ok) {
+                    bulk_wait_read0();                        // previous row copy has left shared memory
+#pragma unroll
+                    for (int j = 0; j < TILE_N; j += 4)
+                        st_shared_v4(out_row + 4 * j, __float_as_uint(v[j]), __float_as_uint(v[j + 1]),
+                                     __float_as_uint(v[j + 2]), __float_as_uint(v[j + 3]));
+                    fence_proxy_async_smem();
+                    bulk_s2g(qrow + b0, out_row, static_cast<uint32_t>(nb) * 4u);
+                    bulk_commit();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < TILE_N; ++j)
+                        if (j < nb) qrow[b0 + j] = v[j];
+                }
+            }
+        }
+        bulk_wait0();
+    } else {
+        // ---- converters: raw rows -> swizzled bf16 key slices ------------------
+        // Per raw piece (32 rows): 32 rows x 16 chunks of 8 d = 512 chunks, 2 per
+        // thread; 16 lanes cover one row.
+        const int ct = tid - CONV_WARP0 * 32;
+        for (int li = 0; li < nlocal; ++li) {
+            const int st = li & 1, use = li >> 1;
+            const uint32_t kbase = base + KS_OFF + st * KS_STAGE_BYTES;
+            wait_or_flag(&bars->ks_empty[st], (use & 1) ^ 1);
+            for (int half = 0; half < 2; ++half) {
+                const int p = 2 * li + half;
+                const int slot = p & (RAW_SLOTS - 1);
+                wait_or_flag(&bars->raw_full[slot], (p / RAW_SLOTS) & 1);
+                const int row0 = tile_b0(li) + half * RAW_ROWS;
+                const uint32_t src = base + RAW_OFF + slot * RAW_SLOT_BYTES;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int t = ct + CONV_THREADS * i;
+                    const int r = t >> 4, c16 = t & 15;     // row in piece, 8-d chunk
+                    const int khalf = c16 >> 3, c = c16 & 7;
+                    const bool live = row0 + r < active;
+                    const uint32_t off = swz(half * RAW_ROWS + r, c);
+                    const uint32_t dst = kbase + khalf * KS_SUB_BYTES + off;
+                    if constexpr (!kInt8) {
+                        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+                        if (live) {
+                            a = ld_shared_v4(src + r * (D * 4) + c16 * 32);
+                            b = ld_shared_v4(src + r * (D * 4) + c16 * 32 + 16);
+                        }
+                        const float x[8] = {__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
+                                            __uint_as_float(a.w), __uint_as_float(b.x), __uint_as_float(b.y),
+                                            __uint_as_float(b.z), __uint_as_float(b.w)};
+                        uint32_t h[8], m[8], l[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) split3(x[e], h[e], m[e], l[e]);
+                        st_shared_v4(dst, pack2(h[0], h[1]), pack2(h[2], h[3]), pack2(h[4], h[5]), pack2(h[6], h[7]));
+                        st_shared_v4(dst + 2 * KS_SUB_BYTES, pack2(m[0], m[1]), pack2(m[2], m[3]),
+                                     pack2(m[4], m[5]), pack2(m[6], m[7]));
+                        st_shared_v4(dst + 4 * KS_SUB_BYTES, pack2(l[0], l[1]), pack2(l[2], l[3]),
+                                     pack2(l[4], l[5]), pack2(l[6], l[7]));
+                    } else {
+                        // 8 int8 keys: exact in bf16 (at most 7 significant bits).
+                        uint2 w = make_uint2(0u, 0u);
+                        if (live) w = ld_shared_v2(src + r * D + c16 * 8);
+                        uint32_t f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const uint32_t word = e < 4 ? w.x : w.y;
+                            const int val = static_cast<int>(static_cast<int8_t>((word >> (8 * (e & 3))) & 0xFFu));
+                            f[e] = __float_as_uint(static_cast<float>(val));
+                        }
+                        st_shared_v4(dst, pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+                    }
+                }
+                mbar_arrive(&bars->raw_empty[slot]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->ks_full[st]);
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale, int nq,
+                             int active, float *scores, cudaStream_t stream) {
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(scores_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(TC_SMEM));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(scores_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(TC_SMEM));
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    const int ntiles = (active + TILE_N - 1) / TILE_N;
+    const int ngroups = (nq + QGROUP - 1) / QGROUP;
+    int per = device_sm_count() / ngroups;
+    if (per < 1) per = 1;
+    if (per > ntiles) per = ntiles;
+    const long long grid = static_cast<long long>(per) * ngroups;
+    if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    if (kq8 != nullptr) {
+        scores_tc_kernel<true><<<static_cast<unsigned>(grid), TC_THREADS, TC_SMEM, stream>>>(
+            q, nullptr, kq8, reinterpret_cast<const __half *>(kscale), nq, active, ntiles, per, scores);
+    } else {
+        scores_tc_kernel<false><<<static_cast<unsigned>(grid), TC_THREADS, TC_SMEM, stream>>>(
+            q, kblk, nullptr, nullptr, nq, active, ntiles, per, scores);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t tc_error_read_clear(uint32_t *word, cudaStream_t stream) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_tc_error, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    const uint32_t zero = 0u;
+    e = cudaMemcpyToSymbolAsync(g_tc_error, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(stream);
+}
+
+}  // namespace qsa

@@ -186,4 +186,4 @@ def device_error(device: torch.device | None = None) -> int:
 
 def default_scorer_kernel() -> tuple[str, str]:
     """(kernel name, source file) of the scorer behind qsa_block_scores."""
-    return "scores_ffma_kernel", "scores_ffma.cu"
+    return "scores_tc_kernel", "scores_tc.cu"
