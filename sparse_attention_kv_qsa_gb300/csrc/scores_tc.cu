@@ -48,7 +48,7 @@ namespace {
 constexpr int TILE_N = 64;                     // key blocks per tile (MMA N)
 constexpr int QGROUP = 128;                    // queries per CTA group (MMA M)
 constexpr int RAW_ROWS = 32;                   // key rows per raw copy
-constexpr int RAW_SLOTS = 4;
+constexpr int RAW_SLOTS = 5;
 constexpr int RAW_SLOT_BYTES = RAW_ROWS * D * 4;    // 16 KiB (fp32 rows)
 constexpr int KS_SUB_BYTES = TILE_N * 128;          // one slice, one K-half: 64 rows x 128 B
 constexpr int KS_STAGE_BYTES = 6 * KS_SUB_BYTES;    // 3 slices x 2 K-halves = 48 KiB
@@ -84,6 +84,21 @@ struct TcBarriers {
 constexpr size_t TC_SMEM = BAR_OFF + sizeof(TcBarriers) + 1024;
 
 __device__ uint32_t g_tc_error;
+
+// Barrier 1 over every warp but the producer (which is already streaming).
+__device__ __forceinline__ void sync_non_producer() {
+    asm volatile("bar.sync 1, %0;" ::"r"(TC_THREADS - 32) : "memory");
+}
+
+// Query slices are staged once through the (still unused) key-slice stages:
+// slice s, row r, 16-byte chunk c at QS_OFF + s * 32 KiB + r * 256 + (c ^ (r & 15)) * 16.
+constexpr int QS_OFF = KS_OFF;
+constexpr int QS_SLICE_BYTES = QGROUP * (D / 8) * 16;   // 32 KiB
+static_assert(3 * QS_SLICE_BYTES <= 2 * KS_STAGE_BYTES, "query staging fits the key stages");
+
+__device__ __forceinline__ uint32_t qs_off(int s, int r, int c) {
+    return QS_OFF + s * QS_SLICE_BYTES + r * 256 + ((c ^ (r & 15)) << 4);
+}
 
 __device__ __forceinline__ void wait_or_flag(uint64_t *bar, uint32_t parity) {
     if (!mbar_wait(bar, parity)) atomicOr(&g_tc_error, 1u);
@@ -151,12 +166,52 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
 
+    // Head-summed query slices: every warp but the producer builds them (one
+    // 8-d chunk of one query per task, coalesced loads) into shared memory.
+    if (warp != PRODUCER_WARP) {
+        for (int t = tid - 32; t < QGROUP * (D / 8); t += TC_THREADS - 32) {
+            const int r = t >> 4, c = t & 15;
+            float x[8];
+            if (r < qn) {
+                const float4 *p =
+                    reinterpret_cast<const float4 *>(q + static_cast<size_t>(q0 + r) * (HEADS * D) + 8 * c);
+                float4 a[4][2];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    a[h][0] = __ldg(p + h * (D / 4));
+                    a[h][1] = __ldg(p + h * (D / 4) + 1);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float v0 = e < 4 ? (&a[0][0].x)[e] : (&a[0][1].x)[e - 4];
+                    const float v1 = e < 4 ? (&a[1][0].x)[e] : (&a[1][1].x)[e - 4];
+                    const float v2 = e < 4 ? (&a[2][0].x)[e] : (&a[2][1].x)[e - 4];
+                    const float v3 = e < 4 ? (&a[3][0].x)[e] : (&a[3][1].x)[e - 4];
+                    x[e] = __fadd_rn(__fadd_rn(__fadd_rn(v0, v1), v2), v3);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = 0.f;
+            }
+            uint32_t h[8], m[8], l[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) split3(x[e], h[e], m[e], l[e]);
+            st_shared_v4(base + qs_off(0, r, c), pack2(h[0], h[1]), pack2(h[2], h[3]), pack2(h[4], h[5]),
+                         pack2(h[6], h[7]));
+            st_shared_v4(base + qs_off(1, r, c), pack2(m[0], m[1]), pack2(m[2], m[3]), pack2(m[4], m[5]),
+                         pack2(m[6], m[7]));
+            st_shared_v4(base + qs_off(2, r, c), pack2(l[0], l[1]), pack2(l[2], l[3]), pack2(l[4], l[5]),
+                         pack2(l[6], l[7]));
+        }
+        sync_non_producer();
+    }
+
     if (warp == PRODUCER_WARP) {
         // ---- raw key rows -> ring (bulk async copies) --------------------------
         if (lane == 0) {
             const int npieces = 2 * nlocal;
             for (int p = 0; p < npieces; ++p) {
-                const int slot = p & (RAW_SLOTS - 1);
+                const int slot = p % RAW_SLOTS;
                 wait_or_flag(&bars->raw_empty[slot], ((p / RAW_SLOTS) & 1) ^ 1);
                 const int row0 = tile_b0(p >> 1) + (p & 1) * RAW_ROWS;
                 const int rows = min(RAW_ROWS, active - row0);
@@ -184,23 +239,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 tc_fence_after_sync();
                 const uint32_t d0 = tmem + ACC_COL0 + st * ACC_STAGE_COLS, d1 = d0 + TILE_N;
                 const uint32_t kbase = base + KS_OFF + st * KS_STAGE_BYTES;
-#pragma unroll
+                // A compact issue loop (one K-step of 16 per trip): the issuing thread
+                // shares its SM sub-partition with converter and epilogue warps, and a
+                // small loop body stays resident in the instruction cache.
+                const uint64_t kdesc = sw128_kmajor_desc(kbase);
+#pragma unroll 1
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const int khalf = kk >> 2, ks = kk & 3;
+                    // key slice s, K-half h at kbase + (2*s + h) * KS_SUB_BYTES; +32 B per K-step
+                    const uint64_t B0 = kdesc + static_cast<uint64_t>(((kk >> 2) * KS_SUB_BYTES + (kk & 3) * 32) >> 4);
+                    const uint32_t A0 = tmem + kk * 8;
                     const uint32_t acc = kk == 0 ? 0u : 1u;
-                    // key slice s, K-half h: kbase + (2*s + h) * KS_SUB_BYTES
-                    const uint32_t kb = kbase + khalf * KS_SUB_BYTES + ks * 32;
-                    const uint64_t B0 = sw128_kmajor_desc(kb);
-                    const uint32_t A0 = tmem + kk * 8, A1 = A0 + A_COLS_PER_SLICE, A2 = A0 + 2 * A_COLS_PER_SLICE;
-                    tc_mma_bf16_ta(d0, A0, B0, idesc, acc);      // hi . hi
-                    tc_mma_bf16_ta(d1, A1, B0, idesc, acc);      // mid . hi
-                    tc_mma_bf16_ta(d1, A2, B0, idesc, 1u);       // lo . hi
+                    tc_mma_bf16_ta(d0, A0, B0, idesc, acc);                                   // hi . hi
+                    tc_mma_bf16_ta(d1, A0 + A_COLS_PER_SLICE, B0, idesc, acc);               // mid . hi
+                    tc_mma_bf16_ta(d1, A0 + 2 * A_COLS_PER_SLICE, B0, idesc, 1u);            // lo . hi
                     if constexpr (!kInt8) {
-                        const uint64_t B1 = sw128_kmajor_desc(kb + 2 * KS_SUB_BYTES);
-                        const uint64_t B2 = sw128_kmajor_desc(kb + 4 * KS_SUB_BYTES);
-                        tc_mma_bf16_ta(d1, A0, B1, idesc, 1u);   // hi . mid
-                        tc_mma_bf16_ta(d1, A1, B1, idesc, 1u);   // mid . mid
-                        tc_mma_bf16_ta(d1, A0, B2, idesc, 1u);   // hi . lo
+                        const uint64_t B1 = B0 + ((2 * KS_SUB_BYTES) >> 4), B2 = B0 + ((4 * KS_SUB_BYTES) >> 4);
+                        tc_mma_bf16_ta(d1, A0, B1, idesc, 1u);                                // hi . mid
+                        tc_mma_bf16_ta(d1, A0 + A_COLS_PER_SLICE, B1, idesc, 1u);           // mid . mid
+                        tc_mma_bf16_ta(d1, A0, B2, idesc, 1u);                                // hi . lo
                     }
                 }
                 tc_commit(&bars->ks_empty[st]);
@@ -213,44 +269,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int quarter = warp & 3;                       // TMEM lanes 32*quarter .. +31
         const int row = 32 * quarter + lane;                // query row within the group
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
-        {
-            const bool live = row < qn;
-            const float4 *p = reinterpret_cast<const float4 *>(q + static_cast<size_t>(q0 + (live ? row : 0)) * (HEADS * D));
-            for (int c = 0; c < D / 8; ++c) {               // 8 d per step: 4 packed columns per slice
-                float x[8];
-                if (live) {
-                    float4 a[4][2];
+        // This warp's 32 query rows: staged slices -> TMEM (A operand).
+        for (int c = 0; c < D / 8; ++c) {
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        a[h][0] = __ldg(p + h * (D / 4) + 2 * c);
-                        a[h][1] = __ldg(p + h * (D / 4) + 2 * c + 1);
-                    }
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float v0 = e < 4 ? (&a[0][0].x)[e] : (&a[0][1].x)[e - 4];
-                        const float v1 = e < 4 ? (&a[1][0].x)[e] : (&a[1][1].x)[e - 4];
-                        const float v2 = e < 4 ? (&a[2][0].x)[e] : (&a[2][1].x)[e - 4];
-                        const float v3 = e < 4 ? (&a[3][0].x)[e] : (&a[3][1].x)[e - 4];
-                        x[e] = __fadd_rn(__fadd_rn(__fadd_rn(v0, v1), v2), v3);
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = 0.f;
-                }
-                uint32_t h[8], m[8], l[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) split3(x[e], h[e], m[e], l[e]);
-                const uint32_t col = lane_addr + 4 * c;
-                tmem_st4(col, pack2(h[0], h[1]), pack2(h[2], h[3]), pack2(h[4], h[5]), pack2(h[6], h[7]));
-                tmem_st4(col + A_COLS_PER_SLICE, pack2(m[0], m[1]), pack2(m[2], m[3]), pack2(m[4], m[5]),
-                         pack2(m[6], m[7]));
-                tmem_st4(col + 2 * A_COLS_PER_SLICE, pack2(l[0], l[1]), pack2(l[2], l[3]), pack2(l[4], l[5]),
-                         pack2(l[6], l[7]));
+            for (int sl = 0; sl < 3; ++sl) {
+                const uint4 v = ld_shared_v4(base + qs_off(sl, row, c));
+                tmem_st4(lane_addr + sl * A_COLS_PER_SLICE + 4 * c, v.x, v.y, v.z, v.w);
             }
-            tmem_st_wait();
-            tc_fence_before_sync();
-            mbar_arrive(&bars->a_ready);
         }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&bars->a_ready);   // the key stages may now be overwritten
 
         const bool bulk_ok = (active & 3) == 0;             // 16-byte aligned row segments
         const uint32_t out_row = base + OUT_OFF + row * OUT_ROW_BYTES;
@@ -300,56 +329,47 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         bulk_wait0();
     } else {
         // ---- converters: raw rows -> swizzled bf16 key slices ------------------
-        // Per raw piece (32 rows): 32 rows x 16 chunks of 8 d = 512 chunks, 2 per
-        // thread; 16 lanes cover one row.
-        const int ct = tid - CONV_WARP0 * 32;
+        // A warp converts whole rows: lane l takes d = 4l .. 4l+3 (one conflict-free
+        // 16-byte read per lane) and stores 8 bytes per slice into half of a
+        // swizzled 16-byte chunk (the two lanes of a chunk share a bank group).
+        const int cw = warp - CONV_WARP0;
+        const int khalf = lane >> 4, c = (lane >> 1) & 7, part = lane & 1;
+        wait_or_flag(&bars->a_ready, 0);   // query staging has left the key stages
         for (int li = 0; li < nlocal; ++li) {
             const int st = li & 1, use = li >> 1;
             const uint32_t kbase = base + KS_OFF + st * KS_STAGE_BYTES;
             wait_or_flag(&bars->ks_empty[st], (use & 1) ^ 1);
             for (int half = 0; half < 2; ++half) {
                 const int p = 2 * li + half;
-                const int slot = p & (RAW_SLOTS - 1);
+                const int slot = p % RAW_SLOTS;
                 wait_or_flag(&bars->raw_full[slot], (p / RAW_SLOTS) & 1);
                 const int row0 = tile_b0(li) + half * RAW_ROWS;
                 const uint32_t src = base + RAW_OFF + slot * RAW_SLOT_BYTES;
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int t = ct + CONV_THREADS * i;
-                    const int r = t >> 4, c16 = t & 15;     // row in piece, 8-d chunk
-                    const int khalf = c16 >> 3, c = c16 & 7;
+                for (int i = 0; i < RAW_ROWS / CONV_WARPS; ++i) {
+                    const int r = cw + CONV_WARPS * i;               // row in the piece
                     const bool live = row0 + r < active;
-                    const uint32_t off = swz(half * RAW_ROWS + r, c);
-                    const uint32_t dst = kbase + khalf * KS_SUB_BYTES + off;
+                    const uint32_t dst = kbase + khalf * KS_SUB_BYTES + swz(half * RAW_ROWS + r, c) + 8 * part;
                     if constexpr (!kInt8) {
-                        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-                        if (live) {
-                            a = ld_shared_v4(src + r * (D * 4) + c16 * 32);
-                            b = ld_shared_v4(src + r * (D * 4) + c16 * 32 + 16);
-                        }
-                        const float x[8] = {__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
-                                            __uint_as_float(a.w), __uint_as_float(b.x), __uint_as_float(b.y),
-                                            __uint_as_float(b.z), __uint_as_float(b.w)};
-                        uint32_t h[8], m[8], l[8];
+                        uint4 a = make_uint4(0u, 0u, 0u, 0u);
+                        if (live) a = ld_shared_v4(src + r * (D * 4) + 16 * lane);
+                        const float x[4] = {__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
+                                            __uint_as_float(a.w)};
+                        uint32_t h[4], m[4], l[4];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) split3(x[e], h[e], m[e], l[e]);
-                        st_shared_v4(dst, pack2(h[0], h[1]), pack2(h[2], h[3]), pack2(h[4], h[5]), pack2(h[6], h[7]));
-                        st_shared_v4(dst + 2 * KS_SUB_BYTES, pack2(m[0], m[1]), pack2(m[2], m[3]),
-                                     pack2(m[4], m[5]), pack2(m[6], m[7]));
-                        st_shared_v4(dst + 4 * KS_SUB_BYTES, pack2(l[0], l[1]), pack2(l[2], l[3]),
-                                     pack2(l[4], l[5]), pack2(l[6], l[7]));
+                        for (int e = 0; e < 4; ++e) split3(x[e], h[e], m[e], l[e]);
+                        st_shared_v2(dst, pack2(h[0], h[1]), pack2(h[2], h[3]));
+                        st_shared_v2(dst + 2 * KS_SUB_BYTES, pack2(m[0], m[1]), pack2(m[2], m[3]));
+                        st_shared_v2(dst + 4 * KS_SUB_BYTES, pack2(l[0], l[1]), pack2(l[2], l[3]));
                     } else {
-                        // 8 int8 keys: exact in bf16 (at most 7 significant bits).
-                        uint2 w = make_uint2(0u, 0u);
-                        if (live) w = ld_shared_v2(src + r * D + c16 * 8);
-                        uint32_t f[8];
+                        // 4 int8 keys: exact in bf16 (at most 7 significant bits).
+                        uint32_t w = 0u;
+                        if (live) w = ld_shared_u32(src + r * D + 4 * lane);
+                        uint32_t f[4];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const uint32_t word = e < 4 ? w.x : w.y;
-                            const int val = static_cast<int>(static_cast<int8_t>((word >> (8 * (e & 3))) & 0xFFu));
-                            f[e] = __float_as_uint(static_cast<float>(val));
-                        }
-                        st_shared_v4(dst, pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+                        for (int e = 0; e < 4; ++e)
+                            f[e] = __float_as_uint(static_cast<float>(static_cast<int8_t>((w >> (8 * e)) & 0xFFu)));
+                        st_shared_v2(dst, pack2(f[0], f[1]), pack2(f[2], f[3]));
                     }
                 }
                 mbar_arrive(&bars->raw_empty[slot]);
