@@ -13,19 +13,29 @@
 //     is scanned from the top bin to find the bin where the running count
 //     reaches the number still to select; that digit extends the prefix and
 //     the count above it is taken. A bin taken whole ends the search early.
-//  3. Keys above the final prefix are selected; keys equal to it are ties,
+//  3. Keys above the final prefix are selected. A bin taken whole is selected
+//     with them; otherwise keys equal to the full 32-bit prefix are ties,
 //     taken in ascending id order until k ids are selected (ties go to the
 //     lower block id). Ids leave in ascending order.
 //
-// GB300 layout. One 512-thread CTA owns one row and streams it with
-// vectorised read-only loads (16 B per thread, four in flight):
-//  Pass A reads the row from HBM and builds the 11-bit histogram in shared
-//  memory.
-//  Pass B streams the row again -- from L2, where pass A just left it -- and
-//  marks keys above the leading bin in a shared-memory selection bitmap while
-//  listing the keys inside it (~1% of a row for smooth data) as candidates.
-//  The later digits visit only that candidate list (if it would overflow its
-//  capacity, they re-stream the row and filter by prefix instead).
+// GB300 layout. One 512-thread CTA owns one row (two CTAs per SM, so every row
+// of a 256-query call is in flight at once):
+//  Rows of at least 16,384 scores first try a listing path. A strided 1/32
+//  sample of the row (loaded first, so it is not queued behind the row) fixes
+//  a threshold expected to pass about 2.5k scores, while the row itself is
+//  requested into L2 (bulk prefetch); one pass of 16-byte read-only loads then
+//  lists every score at or above the threshold, and the digits below run on
+//  that list alone. A list shorter than k or longer
+//  than its capacity sends the row to the exact passes, so the result is
+//  exact either way.
+//  Exact passes: pass A reads the row and builds the 11-bit histogram in
+//  shared memory; pass B streams the row again -- from L2, where pass A just
+//  left it -- and marks keys above the leading bin in a shared-memory
+//  selection bitmap while listing the keys inside it as candidates. The later
+//  digits visit only that candidate list (if it would overflow its capacity,
+//  they re-stream the row and filter by prefix instead).
+//  Each digit's histogram is built by all warps with shared-memory atomics and
+//  scanned by warp 0 alone (two block barriers per digit).
 // No CTA ever waits on another: no cluster, no grid-wide synchronisation, no
 // global scratch.
 #include "ptx.cuh"
@@ -37,25 +47,31 @@ namespace {
 constexpr int ROW_THREADS = 512;
 constexpr int ROW_WARPS = ROW_THREADS / 32;
 constexpr int HIST_A = 2048;             // leading digit: bits 31..21
-constexpr int GROUP = 8;                 // leading-digit bins per group
-constexpr int NGROUPS = HIST_A / GROUP;  // 256: one group per thread
+constexpr int GROUP = 8;                 // leading-digit bins per group sum
 constexpr int BINS_R = 256;              // refinement digits: 20..13, 12..5, 4..0
-constexpr int UNROLL = 4;                // 16-byte loads in flight per thread
-constexpr int CAND_MAX = 2048;           // candidate-list capacity
+constexpr int UNROLL = 4;                // 16-byte loads in flight per thread (exact passes)
+constexpr int LIST_VEC = 8;              // 16-byte loads per thread per listing step: 32 scores
+constexpr int CAND_MAX = 4096;           // candidate-list capacity
+constexpr int SAMPLE_STRIDE = 32;        // one 16-byte group of scores sampled per 512 bytes
+constexpr int FAST_MIN_ACTIVE = 16384;   // shorter rows take the exact passes directly
 constexpr int MAX_ACTIVE = 393216;
+constexpr int SAMPLE_REGS = (MAX_ACTIVE / 4 / SAMPLE_STRIDE + ROW_THREADS - 1) / ROW_THREADS;
+constexpr uint32_t PREFETCH_CHUNK = 32768;     // bytes per L2 prefetch request
+constexpr uint32_t NEG_INF_KEY = 0x007FFFFFu;  // key of -inf (and of NaN)
+constexpr uint32_t QNAN_BITS = 0x7FC00000u;
 
 __device__ uint32_t g_topk_error;
 
 struct RowShared {
     uint32_t histA[HIST_A];
-    uint32_t groupA[NGROUPS];
+    uint32_t groupA[HIST_A / GROUP];
     uint32_t histR[BINS_R];
+    uint32_t whist[ROW_WARPS * BINS_R];  // per-warp sample histograms
     uint32_t cand_key[CAND_MAX];
     uint32_t cand_idx[CAND_MAX];
-    uint32_t scan_tot[ROW_WARPS];
-    uint32_t sel_bin, sel_excl, sel_cnt;
-    uint32_t t1_bin, t1_above, t1_cnt;
-    uint32_t cand_n, n_tie;
+    alignas(16) uint32_t scan_tot[ROW_WARPS];
+    uint32_t sel_bin, sel_above, sel_cnt;
+    uint32_t cand_n;
 };
 
 constexpr size_t SHARED_BYTES = (sizeof(RowShared) + 15) / 16 * 16;
@@ -72,34 +88,93 @@ __device__ __forceinline__ uint32_t float_bits_to_key(uint32_t bits) {
     return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
 
-// Block-wide exclusive prefix sum over threads (every thread must call).
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *tot, int lane, int warp) {
-    uint32_t incl = v;
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, int lane) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(FULL_MASK, incl, o);
-        if (lane >= o) incl += t;
+        const uint32_t t = __shfl_up_sync(FULL_MASK, v, o);
+        if (lane >= o) v += t;
     }
+    return v;
+}
+
+// Block-wide exclusive prefix sum over threads (every thread must call).
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *tot, int lane, int warp) {
+    static_assert(ROW_WARPS == 16, "warp totals are read as four 16-byte words");
+    const uint32_t incl = warp_incl_scan(v, lane);
     if (lane == 31) tot[warp] = incl;
     __syncthreads();
     uint32_t before = 0u;
-    for (int w = 0; w < warp; ++w) before += tot[w];
+#pragma unroll
+    for (int q = 0; q < ROW_WARPS / 4; ++q) {
+        const uint4 t = *reinterpret_cast<const uint4 *>(tot + 4 * q);
+        before += (4 * q + 0 < warp ? t.x : 0u) + (4 * q + 1 < warp ? t.y : 0u) + (4 * q + 2 < warp ? t.z : 0u) +
+                  (4 * q + 3 < warp ? t.w : 0u);
+    }
     __syncthreads();
     return before + incl - v;
 }
 
-// Thread t holds the count of item 255 - t (items in descending order).
-// Finds the item at which the running count from the top reaches kk; leaves
-// it, the count above it and its own count in sh.sel_*.
-__device__ __forceinline__ void select_desc(uint32_t cnt, uint32_t kk, RowShared &sh, int tid, int lane,
-                                            int warp) {
-    const uint32_t excl = block_excl_scan(cnt, sh.scan_tot, lane, warp);
-    if (excl < kk && excl + cnt >= kk) {
-        sh.sel_bin = static_cast<uint32_t>(BINS_R - 1 - tid);
-        sh.sel_excl = excl;
+// Warp 0 alone. Walking the 256 bins of `hist` from the top, finds the bin
+// where the running count reaches `target` (1 <= target <= total); every lane
+// receives the bin, the count above it and its own count. Lane l owns bins
+// 255 - 8l down to 248 - 8l. Clears the histogram when `clear` is set.
+__device__ __forceinline__ void warp_find_256(uint32_t *hist, uint32_t target, bool clear, int lane,
+                                              uint32_t &bin, uint32_t &above, uint32_t &cnt) {
+    uint4 *p = reinterpret_cast<uint4 *>(hist + 8 * (31 - lane));
+    const uint4 lo = p[0], hi = p[1];
+    const uint32_t c[8] = {hi.w, hi.z, hi.y, hi.x, lo.w, lo.z, lo.y, lo.x};
+    uint32_t s = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += c[i];
+    const uint32_t incl = warp_incl_scan(s, lane);
+    const uint32_t owner = __ballot_sync(FULL_MASK, incl - s < target && incl >= target);
+    const int src = owner != 0u ? __ffs(owner) - 1 : 0;
+    uint32_t b = 0u, a = 0u, n = 0u;
+    if (lane == src) {
+        uint32_t run = incl - s;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (run < target && run + c[i] >= target) {
+                b = static_cast<uint32_t>(255 - 8 * lane - i);
+                a = run;
+                n = c[i];
+            }
+            run += c[i];
+        }
+    }
+    bin = __shfl_sync(FULL_MASK, b, src);
+    above = __shfl_sync(FULL_MASK, a, src);
+    cnt = __shfl_sync(FULL_MASK, n, src);
+    if (clear) {
+        p[0] = make_uint4(0u, 0u, 0u, 0u);
+        p[1] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Warp 0 alone: the digit of a 256-bin histogram, left in sh.sel_*; clears it.
+__device__ __forceinline__ void warp_select_256(uint32_t *hist, uint32_t target, RowShared &sh, int lane) {
+    uint32_t bin, above, cnt;
+    warp_find_256(hist, target, true, lane, bin, above, cnt);
+    if (lane == 0) {
+        sh.sel_bin = bin;
+        sh.sel_above = above;
         sh.sel_cnt = cnt;
     }
-    __syncthreads();
+}
+
+// Warp 0 alone: the leading digit, from the 256 group sums (8 bins each) in
+// sh.groupA and then the 8 bins of the group found; left in sh.sel_*.
+__device__ __forceinline__ void warp_select_2048(uint32_t target, RowShared &sh, int lane) {
+    uint32_t gb, ga, gc;
+    warp_find_256(sh.groupA, target, false, lane, gb, ga, gc);
+    const uint32_t c = lane < GROUP ? sh.histA[GROUP * gb + (GROUP - 1) - lane] : 0u;
+    const uint32_t incl = ga + warp_incl_scan(c, lane);
+    const uint32_t owner = __ballot_sync(FULL_MASK, lane < GROUP && incl - c < target && incl >= target);
+    if (owner != 0u && lane == __ffs(owner) - 1) {
+        sh.sel_bin = GROUP * gb + (GROUP - 1) - static_cast<uint32_t>(lane);
+        sh.sel_above = incl - c;
+        sh.sel_cnt = c;
+    }
 }
 
 // Calls fn(i, bits) once for every element of the row (row index i, raw
@@ -134,7 +209,7 @@ __device__ __forceinline__ void stream_row(const uint32_t *g, int n, int head, i
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(ROW_THREADS)
+__global__ void __launch_bounds__(ROW_THREADS, 2)
     topk_row_kernel(const float *__restrict__ scores, int active, int k, int32_t *__restrict__ ids) {
     const size_t row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -151,81 +226,245 @@ __global__ void __launch_bounds__(ROW_THREADS)
     int head = static_cast<int>(((16u - (addr & 15u)) & 15u) >> 2);
     if (head > n) head = n;
     const int nvec = (n - head) >> 2;
+    const uint4 *g4 = reinterpret_cast<const uint4 *>(g + head);
 
-    if (tid == 0) {
-        sh.cand_n = 0u;
-        sh.n_tie = 0u;
+    // Listing path (rows of at least FAST_MIN_ACTIVE scores). A strided sample
+    // (one 16-byte group of scores per 512 bytes) gives a threshold that about
+    // 2.5k scores of the row are expected to reach: the sample's r-th largest
+    // key with r = ceil(2.5 k * samples / n) + 8, found to 16 bits (two 8-bit
+    // sample digits). One pass then lists every score at or above it. A list of
+    // at least k entries holds the whole top-k, ties included, so when it also
+    // fits its capacity the exact selection runs on the list alone; otherwise
+    // the row takes the exact two-pass path.
+    const int nsv = nvec / SAMPLE_STRIDE;
+    const uint32_t nsamp = 4u * static_cast<uint32_t>(nsv);
+    const uint32_t r_target =
+        static_cast<uint32_t>((5ull * static_cast<uint64_t>(k) * nsamp + 2ull * n - 1) / (2ull * n)) + 8u;
+    const bool try_list = n >= FAST_MIN_ACTIVE && r_target <= nsamp / 2;
+
+    // The sample is requested before anything else, ahead of the row's prefetch.
+    uint4 sx[SAMPLE_REGS];
+#pragma unroll
+    for (int u = 0; u < SAMPLE_REGS; ++u) {
+        const int s = tid + u * ROW_THREADS;
+        sx[u] = try_list && s < nsv ? __ldg(g4 + s * SAMPLE_STRIDE + SAMPLE_STRIDE / 2) : make_uint4(0u, 0u, 0u, 0u);
     }
+
+    if (tid == 0) sh.cand_n = 0u;
     for (int i = tid; i < HIST_A; i += ROW_THREADS) sh.histA[i] = 0u;
+    for (int i = tid; i < BINS_R; i += ROW_THREADS) sh.histR[i] = 0u;
+    if (try_list) {
+        uint4 *w4 = reinterpret_cast<uint4 *>(sh.whist);
+        for (int i = tid; i < ROW_WARPS * BINS_R / 4; i += ROW_THREADS) w4[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
     for (int i = tid; i < nwords; i += ROW_THREADS) {
         selbits[i] = 0u;
         tiebits[i] = 0u;
     }
     __syncthreads();
 
-    // Pass A: the 11-bit leading-digit histogram.
-    stream_row(g, n, head, nvec, tid, [&](int, uint32_t bits) {
-        atomicAdd(&sh.histA[float_bits_to_key(bits) >> 21], 1u);
-    });
-    if (tid < NGROUPS) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(&sh.histA[tid * GROUP]);
-        const uint4 b = *reinterpret_cast<const uint4 *>(&sh.histA[tid * GROUP + 4]);
-        sh.groupA[tid] = a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w;
-    }
-    __syncthreads();
     uint32_t kk = static_cast<uint32_t>(k);
-    select_desc(tid < NGROUPS ? sh.groupA[NGROUPS - 1 - tid] : 0u, kk, sh, tid, lane, warp);
-    if (warp == 0) {
-        const uint32_t grp = sh.sel_bin, above = sh.sel_excl;
-        const uint32_t b = grp * GROUP + (GROUP - 1) - static_cast<uint32_t>(lane);
-        const uint32_t c = lane < GROUP ? sh.histA[b] : 0u;
-        uint32_t incl = c;
+    bool listed = false;
+    uint32_t tg = 0u, kmax = 0u;
+    if (try_list) {
+        if (tid == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
+            for (uint32_t off = 0; off < bytes; off += PREFETCH_CHUNK)
+                bulk_prefetch_l2(reinterpret_cast<const unsigned char *>(g4) + off, min(PREFETCH_CHUNK, bytes - off));
+        }
+        // First sample digit: the top 8 key bits. Sample keys crowd into a few
+        // of these bins, so each warp counts into its own copy; 256 threads
+        // then add the copies up.
+        uint32_t *wh = sh.whist + warp * BINS_R;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(FULL_MASK, incl, o);
-            if (lane >= o) incl += t;
-        }
-        if (lane < GROUP && above + incl - c < kk && above + incl >= kk) {
-            sh.t1_bin = b;
-            sh.t1_above = above + incl - c;
-            sh.t1_cnt = c;
-        }
-    }
-    __syncthreads();
-    const uint32_t T1 = sh.t1_bin;
-    kk -= sh.t1_above;
-    const bool doneA = sh.t1_cnt == kk;  // the whole leading bin is taken
-    const bool compact = !doneA && sh.t1_cnt <= static_cast<uint32_t>(CAND_MAX);
-
-    // Pass B: keys above the leading bin are selected; keys inside it are
-    // listed as candidates (or all selected, when the bin is taken whole).
-    stream_row(g, n, head, nvec, tid, [&](int i, uint32_t bits) {
-        const uint32_t key = float_bits_to_key(bits);
-        const uint32_t d = key >> 21;
-        if (d < T1) return;
-        if (d > T1 || doneA) {
-            atomicOr(&selbits[i >> 5], 1u << (i & 31));
-        } else if (compact) {
-            const uint32_t slot = atomicAdd(&sh.cand_n, 1u);
-            if (slot < static_cast<uint32_t>(CAND_MAX)) {
-                sh.cand_key[slot] = key;
-                sh.cand_idx[slot] = static_cast<uint32_t>(i);
+        for (int u = 0; u < SAMPLE_REGS; ++u) {
+            if (tid + u * ROW_THREADS < nsv) {
+                atomicAdd(&wh[float_bits_to_key(sx[u].x) >> 24], 1u);
+                atomicAdd(&wh[float_bits_to_key(sx[u].y) >> 24], 1u);
+                atomicAdd(&wh[float_bits_to_key(sx[u].z) >> 24], 1u);
+                atomicAdd(&wh[float_bits_to_key(sx[u].w) >> 24], 1u);
             }
         }
-    });
+        __syncthreads();
+        if (tid < BINS_R) {
+            uint32_t c = 0u;
+#pragma unroll
+            for (int w = 0; w < ROW_WARPS; ++w) c += sh.whist[w * BINS_R + tid];
+            sh.histR[tid] = c;
+        }
+        __syncthreads();
+        if (warp == 0) warp_select_256(sh.histR, r_target, sh, lane);
+        __syncthreads();
+        const uint32_t T8 = sh.sel_bin, rs = r_target - sh.sel_above;
+        // Second sample digit: key bits 23..16 inside that bin.
+#pragma unroll
+        for (int u = 0; u < SAMPLE_REGS; ++u) {
+            if (tid + u * ROW_THREADS < nsv) {
+                const uint32_t ks[4] = {float_bits_to_key(sx[u].x), float_bits_to_key(sx[u].y),
+                                        float_bits_to_key(sx[u].z), float_bits_to_key(sx[u].w)};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if ((ks[e] >> 24) == T8) atomicAdd(&sh.histR[(ks[e] >> 16) & 0xFFu], 1u);
+            }
+        }
+        __syncthreads();
+        if (warp == 0) warp_select_256(sh.histR, rs, sh, lane);
+        __syncthreads();
+        tg = (T8 << 24) | (sh.sel_bin << 16);
 
-    // Refinement digits over the candidates.
-    uint32_t prefix = T1 << 21, mask = 0xFFE00000u;
-    bool done = doneA;
-    int shift = 21;
+        // Listing pass. key(x) >= tg is tested as the fp32 comparison x >= ft,
+        // ft being the value whose key is tg: both orders agree on every x (NaN
+        // fails the comparison and has the key of -inf, which is below any tg
+        // past the -inf key). A tg at or below the -inf key would list the
+        // whole row, so such a row takes the exact path at once. Each thread
+        // gathers one hit bit per score of a 32-score step; a warp scan of the
+        // hit counts and one shared-memory atomic per warp and step give every
+        // hit its list slot, and the hit's score is read again (an L1 hit: the
+        // warp has just loaded it) for its key. The largest listed key is kept.
+        if (tg > NEG_INF_KEY) {
+            const float ft = __uint_as_float(tg >= 0x80000000u ? (tg ^ 0x80000000u) : ~tg);
+            auto list_scalar = [&](int i) {
+                const uint32_t bits = __ldg(g + i);
+                if (__uint_as_float(bits) >= ft) {
+                    const uint32_t key = float_bits_to_key(bits);
+                    kmax = max(kmax, key);
+                    const uint32_t slot = atomicAdd(&sh.cand_n, 1u);
+                    if (slot < static_cast<uint32_t>(CAND_MAX)) {
+                        sh.cand_idx[slot] = static_cast<uint32_t>(i);
+                        sh.cand_key[slot] = key;
+                    }
+                }
+            };
+            for (int i = tid; i < head; i += ROW_THREADS) list_scalar(i);
+            for (int i = head + 4 * nvec + tid; i < n; i += ROW_THREADS) list_scalar(i);
+            // The next step's loads are issued as soon as this step's hit bits
+            // are taken, ahead of the slot bookkeeping.
+            uint4 x[LIST_VEC];
+            auto load_step = [&](int v0) {
+#pragma unroll
+                for (int u = 0; u < LIST_VEC; ++u) {
+                    const int v = v0 + u * ROW_THREADS + tid;
+                    // Past the end: NaN, which no comparison lists.
+                    x[u] = v < nvec ? __ldg(g4 + v) : make_uint4(QNAN_BITS, QNAN_BITS, QNAN_BITS, QNAN_BITS);
+                }
+            };
+            load_step(0);
+#pragma unroll 1
+            for (int v0 = 0; v0 < nvec; v0 += ROW_THREADS * LIST_VEC) {
+                // A list already past its capacity is abandoned (warp-uniform test).
+                if (__shfl_sync(FULL_MASK, *reinterpret_cast<volatile uint32_t *>(&sh.cand_n), 0) >
+                    static_cast<uint32_t>(CAND_MAX))
+                    break;
+                uint32_t hits = 0u;
+#pragma unroll
+                for (int u = 0; u < LIST_VEC; ++u) {
+                    hits |= static_cast<uint32_t>(__uint_as_float(x[u].x) >= ft) << (4 * u);
+                    hits |= static_cast<uint32_t>(__uint_as_float(x[u].y) >= ft) << (4 * u + 1);
+                    hits |= static_cast<uint32_t>(__uint_as_float(x[u].z) >= ft) << (4 * u + 2);
+                    hits |= static_cast<uint32_t>(__uint_as_float(x[u].w) >= ft) << (4 * u + 3);
+                }
+                if (v0 + ROW_THREADS * LIST_VEC < nvec) load_step(v0 + ROW_THREADS * LIST_VEC);
+                const uint32_t c = __popc(hits);
+                const uint32_t incl = warp_incl_scan(c, lane);
+                const uint32_t total = __shfl_sync(FULL_MASK, incl, 31);
+                if (total != 0u) {  // warp-uniform
+                    uint32_t base = 0u;
+                    if (lane == 31) base = atomicAdd(&sh.cand_n, total);
+                    uint32_t slot = __shfl_sync(FULL_MASK, base, 31) + incl - c;
+                    const int i0 = head + 4 * (v0 + tid);
+                    while (hits != 0u) {
+                        const int j = __ffs(hits) - 1;
+                        hits &= hits - 1u;
+                        if (slot < static_cast<uint32_t>(CAND_MAX)) {
+                            const int i = i0 + 4 * ROW_THREADS * (j >> 2) + (j & 3);
+                            const uint32_t key = float_bits_to_key(__ldg(g + i));
+                            kmax = max(kmax, key);
+                            sh.cand_idx[slot] = static_cast<uint32_t>(i);
+                            sh.cand_key[slot] = key;
+                        }
+                        ++slot;
+                    }
+                }
+            }
+        } else if (tid == 0) {
+            sh.cand_n = static_cast<uint32_t>(CAND_MAX) + 1u;  // would list the whole row
+        }
+        kmax = __reduce_max_sync(FULL_MASK, kmax);
+        if (lane == 0) sh.scan_tot[warp] = kmax;
+        __syncthreads();
+        const uint32_t nc = sh.cand_n;
+#pragma unroll
+        for (int q = 0; q < ROW_WARPS / 4; ++q) {
+            const uint4 t = *reinterpret_cast<const uint4 *>(sh.scan_tot + 4 * q);
+            kmax = max(max(kmax, t.x), max(t.y, max(t.z, t.w)));
+        }
+        listed = nc >= kk && nc <= static_cast<uint32_t>(CAND_MAX);
+        __syncthreads();
+        if (!listed && tid == 0) sh.cand_n = 0u;  // the list is abandoned
+    }
+
+    // Digit search. On the list, every key lies in [tg, kmax], so the search
+    // starts below the bits those two share. On the exact path, the leading
+    // 11 bits come from pass A over the whole row.
+    uint32_t prefix, mask, T1 = 0u;
+    int shift;
+    bool done, doneA = false, compact = true;
+    if (listed) {
+        const uint32_t diff = tg ^ kmax;
+        shift = diff == 0u ? 0 : 32 - __clz(static_cast<int>(diff));
+        mask = shift == 32 ? 0u : 0xFFFFFFFFu << shift;
+        prefix = tg & mask;
+        done = sh.cand_n == kk;  // the whole list is the top-k
+    } else {
+        // Pass A: the 11-bit leading-digit histogram of the whole row.
+        stream_row(g, n, head, nvec, tid, [&](int, uint32_t bits) {
+            atomicAdd(&sh.histA[float_bits_to_key(bits) >> 21], 1u);
+        });
+        if (tid < HIST_A / GROUP) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(&sh.histA[GROUP * tid]);
+            const uint4 b = *reinterpret_cast<const uint4 *>(&sh.histA[GROUP * tid + 4]);
+            sh.groupA[tid] = a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w;
+        }
+        __syncthreads();
+        if (warp == 0) warp_select_2048(kk, sh, lane);
+        __syncthreads();
+        T1 = sh.sel_bin;
+        const uint32_t t1_cnt = sh.sel_cnt;
+        kk -= sh.sel_above;
+        // A leading bin taken whole is marked by pass B directly.
+        doneA = t1_cnt == kk;
+        done = doneA;
+        compact = !doneA && t1_cnt <= static_cast<uint32_t>(CAND_MAX);
+        prefix = T1 << 21;
+        mask = 0xFFE00000u;
+        shift = 21;
+
+        // Pass B: keys above the leading bin are selected; keys inside it are
+        // listed as candidates (or all selected, when the bin is taken whole).
+        stream_row(g, n, head, nvec, tid, [&](int i, uint32_t bits) {
+            const uint32_t key = float_bits_to_key(bits);
+            const uint32_t d = key >> 21;
+            if (d < T1) return;
+            if (d > T1 || doneA) {
+                atomicOr(&selbits[i >> 5], 1u << (i & 31));
+            } else if (compact) {
+                const uint32_t slot = atomicAdd(&sh.cand_n, 1u);
+                if (slot < static_cast<uint32_t>(CAND_MAX)) {
+                    sh.cand_key[slot] = key;
+                    sh.cand_idx[slot] = static_cast<uint32_t>(i);
+                }
+            }
+        });
+    }
+
+    // Refinement digits (at most 8 bits each) over the candidates; histR is
+    // clear here.
     const int m = min(static_cast<int>(sh.cand_n), CAND_MAX);
 #pragma unroll 1
-    for (int p = 0; p < 3 && !done; ++p) {
-        const int width = p < 2 ? 8 : 5;
+    while (!done && shift > 0) {
+        const int width = min(8, shift);
         shift -= width;
         const uint32_t dmask = (1u << width) - 1u;
-        for (int i = tid; i < BINS_R; i += ROW_THREADS) sh.histR[i] = 0u;
-        __syncthreads();
         if (compact) {
             for (int j = tid; j < m; j += ROW_THREADS) {
                 const uint32_t key = sh.cand_key[j];
@@ -238,25 +477,26 @@ __global__ void __launch_bounds__(ROW_THREADS)
                 if ((key & mask) == prefix) atomicAdd(&sh.histR[(key >> shift) & dmask], 1u);
             });
         }
-        select_desc(tid < BINS_R ? sh.histR[BINS_R - 1 - tid] : 0u, kk, sh, tid, lane, warp);
-        kk -= sh.sel_excl;
+        if (warp == 0) warp_select_256(sh.histR, kk, sh, lane);
+        __syncthreads();
+        kk -= sh.sel_above;
         prefix |= sh.sel_bin << shift;
         mask |= dmask << shift;
         done = sh.sel_cnt == kk;
     }
 
-    // Marking: keys of the leading bin above the final prefix are selected;
-    // keys equal to it are ties.
+    // Marking. Keys above the final prefix are selected. When the search ended
+    // on a bin taken whole (done), keys equal to the prefix are selected too;
+    // otherwise they are ties of the full key, of which kk are taken below.
     if (!doneA) {
         if (compact) {
             for (int j = tid; j < m; j += ROW_THREADS) {
                 const uint32_t km = sh.cand_key[j] & mask;
                 const uint32_t i = sh.cand_idx[j];
-                if (km > prefix) {
+                if (km > prefix || (done && km == prefix)) {
                     atomicOr(&selbits[i >> 5], 1u << (i & 31u));
                 } else if (km == prefix) {
                     atomicOr(&tiebits[i >> 5], 1u << (i & 31u));
-                    atomicAdd(&sh.n_tie, 1u);
                 }
             }
             __syncthreads();
@@ -265,11 +505,10 @@ __global__ void __launch_bounds__(ROW_THREADS)
                 const uint32_t key = float_bits_to_key(bits);
                 if ((key >> 21) != T1) return;
                 const uint32_t km = key & mask;
-                if (km > prefix) {
+                if (km > prefix || (done && km == prefix)) {
                     atomicOr(&selbits[i >> 5], 1u << (i & 31));
                 } else if (km == prefix) {
                     atomicOr(&tiebits[i >> 5], 1u << (i & 31));
-                    atomicAdd(&sh.n_tie, 1u);
                 }
             });
         }
@@ -278,14 +517,13 @@ __global__ void __launch_bounds__(ROW_THREADS)
     // Each thread owns a contiguous run of bitmap words, so ids stay ordered.
     const int wpt = (nwords + ROW_THREADS - 1) / ROW_THREADS;
     const int wb = min(nwords, tid * wpt), we = min(nwords, wb + wpt);
-    const uint32_t take = doneA ? 0u : min(kk, sh.n_tie);
-    if (take > 0u) {  // uniform in the CTA
+    if (!doneA && !done) {  // uniform: the first kk ties in id order join the selection
         uint32_t c = 0u;
         for (int wd = wb; wd < we; ++wd) c += __popc(tiebits[wd]);
         uint32_t run = block_excl_scan(c, sh.scan_tot, lane, warp);
-        for (int wd = wb; wd < we && run < take; ++wd) {
+        for (int wd = wb; wd < we && run < kk; ++wd) {
             uint32_t bits = tiebits[wd], add = 0u;
-            while (bits != 0u && run < take) {
+            while (bits != 0u && run < kk) {
                 add |= bits & (~bits + 1u);
                 bits &= bits - 1u;
                 ++run;
@@ -324,7 +562,6 @@ __global__ void topk_all_kernel(int active, int k, size_t total, int32_t *__rest
 cudaError_t launch_topk(const float *scores, int nq, int active, int k, int32_t *ids,
                         cudaStream_t stream) {
     if (active > MAX_ACTIVE) return cudaErrorInvalidValue;
-    static_assert(ROW_THREADS >= NGROUPS && ROW_THREADS >= BINS_R, "one scan item per thread");
     static thread_local int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);

@@ -150,10 +150,10 @@ def test_topk_exact_on_given_scores(dev, o, nq, active, k):
     parity.check_ids_valid(ids, active, k)
 
 
-@pytest.mark.parametrize("m", [2047, 2048, 2049, 6000])
+@pytest.mark.parametrize("m", [4095, 4096, 4097, 9000])
 def test_topk_candidate_list_capacity(dev, o, m):
     """The leading-digit bin holds m keys: at and below the candidate-list
-    capacity (2,048) the refinement runs on the list, above it on the row."""
+    capacity (4,096) the refinement runs on the list, above it on the row."""
     active = 10003
     S = np.full((2, active), -1.0, dtype=np.float32)
     S[:, :100] = 4.0 + np.arange(100, dtype=np.float32) * 0.01
@@ -164,6 +164,56 @@ def test_topk_candidate_list_capacity(dev, o, m):
     for k in (100 + m // 2, 100 + m - 1, 101):
         ids = qsa.block_topk(to_dev(S, dev), k).cpu().numpy()
         assert np.array_equal(ids, o.topk_f32(S, k)), (m, k)
+
+
+def _sampled_positions(active):
+    """Row indices the sampled-threshold path reads (one 16-byte group per
+    512 bytes, 16 groups in), for rows whose start is 16-byte aligned."""
+    g = np.arange(active // 4 // 32) * 32 + 16
+    return (4 * g[:, None] + np.arange(4)[None, :]).ravel()
+
+
+def test_topk_sample_sees_only_the_largest(dev, o):
+    """Every sampled score is large and every other one small: the sample's
+    threshold leaves fewer than k scores listed, so the row must take the
+    exact passes and still return the exact top-k."""
+    active, k = 65536, 512
+    S = w.normal32(41, 1, 3 * active).reshape(3, active).astype(np.float32)
+    pos = _sampled_positions(active)
+    S[:, pos] = 100.0 + np.abs(S[:, pos])
+    S[2, pos[::2]] = 50.0                              # ties among the sampled scores
+    ids = qsa.block_topk(to_dev(S, dev), k).cpu().numpy()
+    assert np.array_equal(ids, o.topk_f32(S, k))
+
+
+@pytest.mark.parametrize("nq,active,k", [(5, 70001, 64), (3, 70003, 700), (3, 100002, 5000),
+                                         (2, 16384, 1000), (2, 16383, 1000), (2, 393215, 1200),
+                                         (2, 393215, 4000)])
+def test_topk_ragged_rows_random(dev, o, nq, active, k):
+    """Rows of odd length start at every 4-byte offset, so the listing pass
+    meets ragged heads and tails; smooth data keeps the list within capacity
+    for small k and overflows it for large k."""
+    S = w.normal32(active + k, 2, nq * active).reshape(nq, active)
+    ids = qsa.block_topk(to_dev(S, dev), k).cpu().numpy()
+    assert np.array_equal(ids, o.topk_f32(S, k))
+
+
+@pytest.mark.parametrize("n_pos,n_zero,n_inf,k", [(500, 2500, 0, 1000), (1000, 2000, 0, 800),
+                                                   (0, 0, 3000, 1000), (200, 0, 3000, 2500)])
+def test_topk_threshold_at_signed_zero_and_inf(dev, o, n_pos, n_zero, n_inf, k):
+    """Counts chosen so that the sampled threshold tends to fall on the
+    zeros (both signs, equal keys) or on +inf (ties to the lower id)."""
+    active, nq = 65536, 3
+    u = w.u32(n_pos + n_zero + n_inf + k, 3, nq * active).reshape(nq, active)
+    S = -1.0 - (u % 1000).astype(np.float32)
+    for r in range(nq):
+        perm = np.argsort(u[r] >> 10, kind="stable")
+        S[r, perm[:n_pos]] = 1.0 + (u[r, perm[:n_pos]] % 4096).astype(np.float32)
+        z = perm[n_pos:n_pos + n_zero]
+        S[r, z] = np.where(u[r, z] & 1, np.float32(0.0), np.float32(-0.0))
+        S[r, perm[n_pos + n_zero:n_pos + n_zero + n_inf]] = np.inf
+    ids = qsa.block_topk(to_dev(S, dev), k).cpu().numpy()
+    assert np.array_equal(ids, o.topk_f32(S, k))
 
 
 def test_topk_nan_ranks_lowest(dev, o):
