@@ -86,6 +86,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 
 // Asks the TMA unit to bring [src, src + bytes) into L2 (no destination, no
 // completion to wait for). src 16-byte aligned; bytes % 16 == 0.
+// Programmatic dependent launch. wait: blocks until the grids this one depends
+// on have completed and their memory is visible (a no-op without such a
+// dependency). launch_dependents: lets the next grid on the stream start
+// launching; it still waits for this grid's completion before its reads.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
@@ -196,6 +205,17 @@ __device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src_smem, uint32_t 
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem),
                  "r"(bytes)
                  : "memory");
+}
+// 2-D tiled bulk store shared -> global through a tensor map (x innermost).
+__device__ __forceinline__ void tma_store_2d(const void *map, uint32_t src_smem, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src_smem), "r"(x), "r"(y)
+                 : "memory");
+}
+// Named barrier `id` over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until this thread's bulk stores no longer read shared memory.

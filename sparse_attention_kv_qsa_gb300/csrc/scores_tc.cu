@@ -27,16 +27,21 @@
 //  - B: key tiles. A producer warp streams raw key rows (contiguous, 16 KiB
 //    = 32 fp32 rows per copy) into a 4-slot shared-memory ring with bulk
 //    async copies; 8 converter warps split them into three 128-byte-swizzled
-//    K-major bf16 slices in a 2-stage ring (2 x 48 KiB).
+//    K-major bf16 slices in a 3-stage ring (3 x 48 KiB).
 //  - One thread issues tcgen05.mma into two accumulators (hi*hi;
 //    corrections) per tile, double-buffered (4 x 64 TMEM columns), and
-//    signals stages with tcgen05.commit.
+//    signals stages with tcgen05.commit. Its SM sub-partition holds no
+//    converter warp, so the 48 issues of a tile are not slowed by them.
 //  - 4 epilogue warps (thread = query row) read the accumulators, add them,
-//    write the row's 64 scores to a padded shared-memory row and send it to
-//    global memory with one 256-byte bulk async store per row.
+//    and store the scores through a per-warp shared-memory transpose as
+//    coalesced 16-byte stores (two 256-byte row segments per instruction).
 //  - Key rows at or beyond `active` are never read; the grid comes from
 //    `active` and nq alone.
 // Every mbarrier wait is bounded; a timeout sets the error word.
+#include <cstring>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include "ptx.cuh"
@@ -48,15 +53,22 @@ namespace {
 constexpr int TILE_N = 64;                     // key blocks per tile (MMA N)
 constexpr int QGROUP = 128;                    // queries per CTA group (MMA M)
 constexpr int RAW_ROWS = 32;                   // key rows per raw copy
-constexpr int RAW_SLOTS = 5;
+constexpr int RAW_SLOTS = 3;
+constexpr int KS_STAGES = 3;                   // converted key tiles in flight
 constexpr int RAW_SLOT_BYTES = RAW_ROWS * D * 4;    // 16 KiB (fp32 rows)
 constexpr int KS_SUB_BYTES = TILE_N * 128;          // one slice, one K-half: 64 rows x 128 B
 constexpr int KS_STAGE_BYTES = 6 * KS_SUB_BYTES;    // 3 slices x 2 K-halves = 48 KiB
 constexpr int OUT_ROW_BYTES = TILE_N * 4 + 16;      // padded: conflict-free 16-byte stores
+constexpr int OUT_BOX_COLS = 32;                   // tensor-store box: 32 scores (128 B) x 128 rows
+constexpr int OUT_BOX_BYTES = QGROUP * OUT_BOX_COLS * 4;   // 16 KiB, 128-byte swizzled
+constexpr int OUT_BYTES = (TILE_N / OUT_BOX_COLS) * OUT_BOX_BYTES;   // 32 KiB
+// Warp roles. Warp w runs on SM sub-partition w % 4. The MMA issuer (warp 1)
+// shares its sub-partition only with one epilogue warp (5) and two warps that
+// have no role (9, 13), so nothing competes with the issue of tcgen05.mma.
 constexpr int PRODUCER_WARP = 0, MMA_WARP = 1;
-constexpr int EPI_WARP0 = 2, EPI_WARPS = 4;
-constexpr int CONV_WARP0 = EPI_WARP0 + EPI_WARPS, CONV_WARPS = 8;
-constexpr int TC_THREADS = (CONV_WARP0 + CONV_WARPS) * 32;   // 448
+constexpr int EPI_WARP0 = 2, EPI_WARPS = 4;       // warps 2..5: TMEM lane quarters 2, 3, 0, 1
+constexpr int CONV_WARPS = 8;                     // warps 6, 7, 8, 10, 11, 12, 14, 15
+constexpr int TC_THREADS = 16 * 32;
 constexpr int CONV_THREADS = CONV_WARPS * 32;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
@@ -65,16 +77,18 @@ constexpr uint32_t ACC_COL0 = 3 * A_COLS_PER_SLICE;   // 192: accumulators after
 constexpr uint32_t ACC_STAGE_COLS = 2 * TILE_N;       // hi*hi and corrections, 64 columns each
 
 // Shared memory, from a 1,024-byte-aligned base.
-constexpr int KS_OFF = 0;                                   // 2 x 48 KiB
-constexpr int RAW_OFF = KS_OFF + 2 * KS_STAGE_BYTES;        // 4 x 16 KiB
-constexpr int OUT_OFF = RAW_OFF + RAW_SLOTS * RAW_SLOT_BYTES;
-constexpr int BAR_OFF = OUT_OFF + QGROUP * OUT_ROW_BYTES;
+constexpr int KS_OFF = 0;                                   // 3 x 48 KiB
+constexpr int RAW_OFF = KS_OFF + KS_STAGES * KS_STAGE_BYTES;  // 3 x 16 KiB
+constexpr int OUT_OFF = RAW_OFF + RAW_SLOTS * RAW_SLOT_BYTES;   // 32 KiB, 1,024-byte aligned
+constexpr int BAR_OFF = OUT_OFF + OUT_BYTES;
+static_assert(OUT_OFF % 1024 == 0, "128-byte swizzled staging needs 1,024-byte alignment");
+static_assert(EPI_WARPS * 16 * OUT_ROW_BYTES <= OUT_BYTES, "direct-store staging fits");
 
 struct TcBarriers {
     uint64_t raw_full[RAW_SLOTS];   // producer -> converters (bulk copy landed)
     uint64_t raw_empty[RAW_SLOTS];  // converters -> producer
-    uint64_t ks_full[2];            // converters -> MMA: key slices written
-    uint64_t ks_empty[2];           // MMA -> converters: key slices consumed
+    uint64_t ks_full[KS_STAGES];    // converters -> MMA: key slices written
+    uint64_t ks_empty[KS_STAGES];   // MMA -> converters: key slices consumed
     uint64_t acc_full[2];           // MMA -> epilogue
     uint64_t acc_empty[2];          // epilogue -> MMA
     uint64_t a_ready;               // query slices in TMEM
@@ -94,7 +108,13 @@ __device__ __forceinline__ void sync_non_producer() {
 // slice s, row r, 16-byte chunk c at QS_OFF + s * 32 KiB + r * 256 + (c ^ (r & 15)) * 16.
 constexpr int QS_OFF = KS_OFF;
 constexpr int QS_SLICE_BYTES = QGROUP * (D / 8) * 16;   // 32 KiB
-static_assert(3 * QS_SLICE_BYTES <= 2 * KS_STAGE_BYTES, "query staging fits the key stages");
+static_assert(3 * QS_SLICE_BYTES <= KS_STAGES * KS_STAGE_BYTES, "query staging fits the key stages");
+static_assert(TC_SMEM <= 232448, "shared memory per CTA");
+
+// Converter index of a warp (warps 9 and 13 have no role), or -1.
+__device__ __forceinline__ int converter_index(int warp) {
+    return (warp < 6 || warp == 9 || warp == 13) ? -1 : warp - 6 - (warp > 9) - (warp > 13);
+}
 
 __device__ __forceinline__ uint32_t qs_off(int s, int r, int c) {
     return QS_OFF + s * QS_SLICE_BYTES + r * 256 + ((c ^ (r & 15)) << 4);
@@ -125,7 +145,8 @@ template <bool kInt8>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     scores_tc_kernel(const float *__restrict__ q, const float *__restrict__ kblk,
                      const int8_t *__restrict__ kq8, const __half *__restrict__ kscale, int nq, int active,
-                     int ntiles, int ctas_per_group, float *__restrict__ scores) {
+                     int ntiles, int ctas_per_group, float *__restrict__ scores,
+                     const __grid_constant__ CUtensorMap out_map, int use_tma) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -147,9 +168,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(&bars->raw_full[s], 1);
             mbar_init(&bars->raw_empty[s], CONV_THREADS);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < KS_STAGES; ++s) {
             mbar_init(&bars->ks_full[s], CONV_THREADS);
             mbar_init(&bars->ks_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->acc_full[s], 1);
             mbar_init(&bars->acc_empty[s], EPI_THREADS);
         }
@@ -165,6 +188,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __syncthreads();  // barriers initialised, TMEM allocated
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
+    // Inputs may come from the previous grid on the stream; the next grid (the
+    // top-k) may launch now and waits for this one's scores itself.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     // Head-summed query slices: every warp but the producer builds them (one
     // 8-d chunk of one query per task, coalesced loads) into shared memory.
@@ -232,18 +259,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint32_t idesc = idesc_bf16_f32(QGROUP, TILE_N);
             wait_or_flag(&bars->a_ready, 0);
             tc_fence_after_sync();
+            int ks = 0, ks_use = 0;
             for (int li = 0; li < nlocal; ++li) {
                 const int st = li & 1, use = li >> 1;
                 wait_or_flag(&bars->acc_empty[st], (use & 1) ^ 1);
-                wait_or_flag(&bars->ks_full[st], use & 1);
+                wait_or_flag(&bars->ks_full[ks], ks_use & 1);
                 tc_fence_after_sync();
                 const uint32_t d0 = tmem + ACC_COL0 + st * ACC_STAGE_COLS, d1 = d0 + TILE_N;
-                const uint32_t kbase = base + KS_OFF + st * KS_STAGE_BYTES;
-                // A compact issue loop (one K-step of 16 per trip): the issuing thread
-                // shares its SM sub-partition with converter and epilogue warps, and a
-                // small loop body stays resident in the instruction cache.
+                const uint32_t kbase = base + KS_OFF + ks * KS_STAGE_BYTES;
+                // Fully unrolled: the 48 descriptors differ from the first by constants.
                 const uint64_t kdesc = sw128_kmajor_desc(kbase);
-#pragma unroll 1
+#pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     // key slice s, K-half h at kbase + (2*s + h) * KS_SUB_BYTES; +32 B per K-step
                     const uint64_t B0 = kdesc + static_cast<uint64_t>(((kk >> 2) * KS_SUB_BYTES + (kk & 3) * 32) >> 4);
@@ -259,12 +285,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         tc_mma_bf16_ta(d1, A0, B2, idesc, 1u);                                // hi . lo
                     }
                 }
-                tc_commit(&bars->ks_empty[st]);
+                tc_commit(&bars->ks_empty[ks]);
                 tc_commit(&bars->acc_full[st]);
+                if (++ks == KS_STAGES) {
+                    ks = 0;
+                    ++ks_use;
+                }
             }
         }
         __syncwarp();
-    } else if (warp < CONV_WARP0) {
+    } else if (warp < EPI_WARP0 + EPI_WARPS) {
         // ---- epilogue warps: query slices into TMEM, then scores out -------------
         const int quarter = warp & 3;                       // TMEM lanes 32*quarter .. +31
         const int row = 32 * quarter + lane;                // query row within the group
@@ -281,9 +311,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_fence_before_sync();
         mbar_arrive(&bars->a_ready);   // the key stages may now be overwritten
 
-        const bool bulk_ok = (active & 3) == 0;             // 16-byte aligned row segments
-        const uint32_t out_row = base + OUT_OFF + row * OUT_ROW_BYTES;
-        float *qrow = scores + static_cast<size_t>(q0 + row) * active;
+        // Scores leave by tensor store (use_tma: rows 16-byte aligned): the 128
+        // threads write the tile's 128 x 64 scores into two 128-byte-swizzled
+        // boxes of 32 columns, and one thread stores both asynchronously.
+        // Otherwise, through a per-warp shared-memory transpose, half a warp at
+        // a time: 16 threads write their query rows' 64 scores to padded staging
+        // rows, then the warp stores two rows per instruction.
+        const int epi_tid = tid - EPI_WARP0 * 32;
+        const bool vec_ok = (active & 3) == 0;              // 16-byte aligned row segments
+        const uint32_t stage0 = base + OUT_OFF + quarter * 16 * OUT_ROW_BYTES;
+        const uint32_t my_stage = stage0 + (lane & 15) * OUT_ROW_BYTES;
+        const int pr = lane >> 4, pc = 4 * (lane & 15);    // row of a pair, first column
         for (int li = 0; li < nlocal; ++li) {
             const int st = li & 1, use = li >> 1;
             const int b0 = tile_b0(li);
@@ -309,36 +347,67 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int j = 0; j < TILE_N; ++j)
                     if (j < nb) v[j] = __fmul_rn(v[j], __half2float(kscale[b0 + j]));
             }
-            if (row < qn) {
-                if (bulk_ok) {
-                    bulk_wait_read0();                        // previous row copy has left shared memory
+            if (use_tma) {
+                if (epi_tid == 0) bulk_wait_read0();        // the previous tile's stores have read the boxes
+                named_bar_sync(2, EPI_THREADS);
+#pragma unroll
+                for (int j = 0; j < TILE_N / 4; ++j) {
+                    const int box = j >> 3, chunk = j & 7;
+                    st_shared_v4(base + OUT_OFF + box * OUT_BOX_BYTES + row * 128 + ((chunk ^ (row & 7)) << 4),
+                                 __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                 __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(2, EPI_THREADS);
+                if (epi_tid == 0) {
+                    tma_store_2d(&out_map, base + OUT_OFF, b0, q0);
+                    if (b0 + OUT_BOX_COLS < active) tma_store_2d(&out_map, base + OUT_OFF + OUT_BOX_BYTES, b0 + OUT_BOX_COLS, q0);
+                    bulk_commit();
+                }
+                continue;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if ((lane >> 4) == h) {
 #pragma unroll
                     for (int j = 0; j < TILE_N; j += 4)
-                        st_shared_v4(out_row + 4 * j, __float_as_uint(v[j]), __float_as_uint(v[j + 1]),
+                        st_shared_v4(my_stage + 4 * j, __float_as_uint(v[j]), __float_as_uint(v[j + 1]),
                                      __float_as_uint(v[j + 2]), __float_as_uint(v[j + 3]));
-                    fence_proxy_async_smem();
-                    bulk_s2g(qrow + b0, out_row, static_cast<uint32_t>(nb) * 4u);
-                    bulk_commit();
-                } else {
-#pragma unroll
-                    for (int j = 0; j < TILE_N; ++j)
-                        if (j < nb) qrow[b0 + j] = v[j];
                 }
+                __syncwarp();
+#pragma unroll 4
+                for (int i = 0; i < 8; ++i) {
+                    const int sr = 2 * i + pr;                   // staging row
+                    const int r = 32 * quarter + 16 * h + sr;    // query row within the group
+                    if (r < qn) {
+                        const uint4 w4 = ld_shared_v4(stage0 + sr * OUT_ROW_BYTES + 4 * pc);
+                        float *dst = scores + static_cast<size_t>(q0 + r) * active + b0 + pc;
+                        if (vec_ok && pc + 4 <= nb) {
+                            *reinterpret_cast<uint4 *>(dst) = w4;
+                        } else {
+                            const uint32_t e[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                if (pc + c < nb) dst[c] = __uint_as_float(e[c]);
+                        }
+                    }
+                }
+                __syncwarp();
             }
         }
-        bulk_wait0();
-    } else {
+        if (epi_tid == 0) bulk_wait0();                     // stores complete before the CTA leaves
+    } else if (converter_index(warp) >= 0) {
         // ---- converters: raw rows -> swizzled bf16 key slices ------------------
         // A warp converts whole rows: lane l takes d = 4l .. 4l+3 (one conflict-free
         // 16-byte read per lane) and stores 8 bytes per slice into half of a
         // swizzled 16-byte chunk (the two lanes of a chunk share a bank group).
-        const int cw = warp - CONV_WARP0;
+        const int cw = converter_index(warp);
         const int khalf = lane >> 4, c = (lane >> 1) & 7, part = lane & 1;
         wait_or_flag(&bars->a_ready, 0);   // query staging has left the key stages
+        int ks = 0, ks_use = 0;
         for (int li = 0; li < nlocal; ++li) {
-            const int st = li & 1, use = li >> 1;
-            const uint32_t kbase = base + KS_OFF + st * KS_STAGE_BYTES;
-            wait_or_flag(&bars->ks_empty[st], (use & 1) ^ 1);
+            const uint32_t kbase = base + KS_OFF + ks * KS_STAGE_BYTES;
+            wait_or_flag(&bars->ks_empty[ks], (ks_use & 1) ^ 1);
             for (int half = 0; half < 2; ++half) {
                 const int p = 2 * li + half;
                 const int slot = p % RAW_SLOTS;
@@ -375,7 +444,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 mbar_arrive(&bars->raw_empty[slot]);
             }
             fence_proxy_async_smem();
-            mbar_arrive(&bars->ks_full[st]);
+            mbar_arrive(&bars->ks_full[ks]);
+            if (++ks == KS_STAGES) {
+                ks = 0;
+                ++ks_use;
+            }
         }
     }
 
@@ -385,6 +458,36 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem, TMEM_COLS);
     }
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once (no link-time
+// dependency on the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// Tensor map of the scores [nq][active] fp32 for 32 x 128 boxes, 128-byte
+// swizzle; false when rows are not 16-byte aligned (active % 4 != 0).
+bool encode_out_map(CUtensorMap *map, float *scores, int nq, int active) {
+    if ((active & 3) != 0 || (reinterpret_cast<uintptr_t>(scores) & 15u) != 0) return false;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(active), static_cast<cuuint64_t>(nq)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(active) * 4u};
+    const cuuint32_t box[2] = {OUT_BOX_COLS, QGROUP};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, scores, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -410,14 +513,26 @@ cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq
     if (per > ntiles) per = ntiles;
     const long long grid = static_cast<long long>(per) * ngroups;
     if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    if (kq8 != nullptr) {
-        scores_tc_kernel<true><<<static_cast<unsigned>(grid), TC_THREADS, TC_SMEM, stream>>>(
-            q, nullptr, kq8, reinterpret_cast<const __half *>(kscale), nq, active, ntiles, per, scores);
-    } else {
-        scores_tc_kernel<false><<<static_cast<unsigned>(grid), TC_THREADS, TC_SMEM, stream>>>(
-            q, kblk, nullptr, nullptr, nq, active, ntiles, per, scores);
-    }
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = TC_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    CUtensorMap out_map;
+    memset(&out_map, 0, sizeof(out_map));
+    const int use_tma = encode_out_map(&out_map, scores, nq, active) ? 1 : 0;
+    if (kq8 != nullptr)
+        return cudaLaunchKernelEx(&cfg, scores_tc_kernel<true>, q, static_cast<const float *>(nullptr), kq8,
+                                  reinterpret_cast<const __half *>(kscale), nq, active, ntiles, per, scores,
+                                  out_map, use_tma);
+    return cudaLaunchKernelEx(&cfg, scores_tc_kernel<false>, q, kblk, static_cast<const int8_t *>(nullptr),
+                              static_cast<const __half *>(nullptr), nq, active, ntiles, per, scores, out_map,
+                              use_tma);
 }
 
 cudaError_t tc_error_read_clear(uint32_t *word, cudaStream_t stream) {

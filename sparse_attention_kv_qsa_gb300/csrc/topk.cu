@@ -242,6 +242,10 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         static_cast<uint32_t>((5ull * static_cast<uint64_t>(k) * nsamp + 2ull * n - 1) / (2ull * n)) + 8u;
     const bool try_list = n >= FAST_MIN_ACTIVE && r_target <= nsamp / 2;
 
+    // The scores may come from the previous grid on the stream (launched as
+    // its programmatic dependent); nothing global is read before this.
+    grid_dependency_wait();
+
     // The sample is requested before anything else, ahead of the row's prefetch.
     uint4 sx[SAMPLE_REGS];
 #pragma unroll
@@ -571,9 +575,17 @@ cudaError_t launch_topk(const float *scores, int nq, int active, int k, int32_t 
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    topk_row_kernel<<<static_cast<unsigned>(nq), ROW_THREADS, row_smem_bytes(active), stream>>>(scores, active,
-                                                                                               k, ids);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nq));
+    cfg.blockDim = dim3(ROW_THREADS);
+    cfg.dynamicSmemBytes = row_smem_bytes(active);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topk_row_kernel, scores, active, k, ids);
 }
 
 cudaError_t launch_topk_all(int nq, int active, int k, int32_t *ids, cudaStream_t stream) {
