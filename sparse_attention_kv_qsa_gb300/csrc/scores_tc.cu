@@ -62,10 +62,11 @@ constexpr int OUT_ROW_BYTES = TILE_N * 4 + 16;      // padded: conflict-free 16-
 constexpr int OUT_BOX_COLS = 32;                   // tensor-store box: 32 scores (128 B) x 128 rows
 constexpr int OUT_BOX_BYTES = QGROUP * OUT_BOX_COLS * 4;   // 16 KiB, 128-byte swizzled
 constexpr int OUT_BYTES = (TILE_N / OUT_BOX_COLS) * OUT_BOX_BYTES;   // 32 KiB
-// Warp roles. Warp w runs on SM sub-partition w % 4. The MMA issuer (warp 1)
-// shares its sub-partition only with one epilogue warp (5) and two warps that
-// have no role (9, 13), so nothing competes with the issue of tcgen05.mma.
-constexpr int PRODUCER_WARP = 0, MMA_WARP = 1;
+// Warp roles. Warp w runs on SM sub-partition w % 4. The MMA issuers (warps 1
+// and 13) share their sub-partition only with one epilogue warp (5) and one
+// warp that has no role (9), so nothing competes with the issue of
+// tcgen05.mma.
+constexpr int PRODUCER_WARP = 0, MMA_WARP = 1, MMA_WARP2 = 13;
 constexpr int EPI_WARP0 = 2, EPI_WARPS = 4;       // warps 2..5: TMEM lane quarters 2, 3, 0, 1
 constexpr int CONV_WARPS = 8;                     // warps 6, 7, 8, 10, 11, 12, 14, 15
 constexpr int TC_THREADS = 16 * 32;
@@ -92,6 +93,7 @@ struct TcBarriers {
     uint64_t acc_full[2];           // MMA -> epilogue
     uint64_t acc_empty[2];          // epilogue -> MMA
     uint64_t a_ready;               // query slices in TMEM
+    uint64_t q_peer;                // CTA pairs: the peer's half of the query slices landed
     uint32_t tmem_base;
 };
 
@@ -110,6 +112,7 @@ constexpr int QS_OFF = KS_OFF;
 constexpr int QS_SLICE_BYTES = QGROUP * (D / 8) * 16;   // 32 KiB
 static_assert(3 * QS_SLICE_BYTES <= KS_STAGES * KS_STAGE_BYTES, "query staging fits the key stages");
 static_assert(TC_SMEM <= 232448, "shared memory per CTA");
+constexpr uint32_t QS_PEER_BYTES = 3u * (QGROUP / 2) * (D / 8) * 16u;   // the peer's 64 rows, 3 slices
 
 // Converter index of a warp (warps 9 and 13 have no role), or -1.
 __device__ __forceinline__ int converter_index(int warp) {
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     scores_tc_kernel(const float *__restrict__ q, const float *__restrict__ kblk,
                      const int8_t *__restrict__ kq8, const __half *__restrict__ kscale, int nq, int active,
                      int ntiles, int ctas_per_group, float *__restrict__ scores,
-                     const __grid_constant__ CUtensorMap out_map, int use_tma) {
+                     const __grid_constant__ CUtensorMap out_map, int use_tma, int pair) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -177,6 +180,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(&bars->acc_empty[s], EPI_THREADS);
         }
         mbar_init(&bars->a_ready, EPI_THREADS);
+        mbar_init(&bars->q_peer, 1);
+        if (pair) mbar_arrive_expect_tx(&bars->q_peer, QS_PEER_BYTES);
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -186,6 +191,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     tc_fence_before_sync();
     __syncthreads();  // barriers initialised, TMEM allocated
+    if (pair) cluster_sync_all();  // ... in both CTAs of the pair
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
     // Inputs may come from the previous grid on the stream; the next grid (the
@@ -195,9 +201,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     // Head-summed query slices: every warp but the producer builds them (one
     // 8-d chunk of one query per task, coalesced loads) into shared memory.
+    // CTA pairs (a cluster of two in the same query group) split the rows:
+    // each builds 64 and also writes them into its peer's staging with
+    // asynchronous cluster stores that count on the peer's q_peer barrier, so
+    // every query is read from L2 by half as many CTAs. Each CTA also starts at
+    // its own rotation of the task order, so that the CTAs of a group do not
+    // all hit the same L2 lines at once.
     if (warp != PRODUCER_WARP) {
-        for (int t = tid - 32; t < QGROUP * (D / 8); t += TC_THREADS - 32) {
-            const int r = t >> 4, c = t & 15;
+        const uint32_t rank = pair ? cluster_ctarank() : 0u;
+        const int rows0 = pair ? static_cast<int>(rank) * (QGROUP / 2) : 0;
+        const int ntask = (pair ? QGROUP / 2 : QGROUP) * (D / 8);   // a power of two
+        const uint32_t peer_bar = pair ? map_shared_rank(smem_u32(&bars->q_peer), rank ^ 1u) : 0u;
+        const uint32_t peer_base = pair ? map_shared_rank(base, rank ^ 1u) : 0u;
+        const int rot = (j0 * 37 * 16) & (ntask - 1);
+#pragma unroll 2
+        for (int t0 = tid - 32; t0 < ntask; t0 += TC_THREADS - 32) {
+            const int t = (t0 + rot) & (ntask - 1);
+            const int r = rows0 + (t >> 4), c = t & 15;
             float x[8];
             if (r < qn) {
                 const float4 *p =
@@ -223,12 +243,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t h[8], m[8], l[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) split3(x[e], h[e], m[e], l[e]);
-            st_shared_v4(base + qs_off(0, r, c), pack2(h[0], h[1]), pack2(h[2], h[3]), pack2(h[4], h[5]),
-                         pack2(h[6], h[7]));
-            st_shared_v4(base + qs_off(1, r, c), pack2(m[0], m[1]), pack2(m[2], m[3]), pack2(m[4], m[5]),
-                         pack2(m[6], m[7]));
-            st_shared_v4(base + qs_off(2, r, c), pack2(l[0], l[1]), pack2(l[2], l[3]), pack2(l[4], l[5]),
-                         pack2(l[6], l[7]));
+            const uint32_t w[3][4] = {{pack2(h[0], h[1]), pack2(h[2], h[3]), pack2(h[4], h[5]), pack2(h[6], h[7])},
+                                      {pack2(m[0], m[1]), pack2(m[2], m[3]), pack2(m[4], m[5]), pack2(m[6], m[7])},
+                                      {pack2(l[0], l[1]), pack2(l[2], l[3]), pack2(l[4], l[5]), pack2(l[6], l[7])}};
+#pragma unroll
+            for (int sl = 0; sl < 3; ++sl) {
+                st_shared_v4(base + qs_off(sl, r, c), w[sl][0], w[sl][1], w[sl][2], w[sl][3]);
+                if (pair) st_async_v4(peer_base + qs_off(sl, r, c), peer_bar, w[sl][0], w[sl][1], w[sl][2], w[sl][3]);
+            }
         }
         sync_non_producer();
     }
@@ -253,15 +275,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == MMA_WARP) {
-        // ---- MMA issuer ----------------------------------------------------------
+    } else if (warp == MMA_WARP || warp == MMA_WARP2) {
+        // ---- MMA issuers ---------------------------------------------------------
+        // Two threads take alternate tiles (each then owns one accumulator
+        // stage), so one issues while the other waits for its next tile's
+        // barriers and the tensor pipe never drains between tiles.
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(QGROUP, TILE_N);
             wait_or_flag(&bars->a_ready, 0);
             tc_fence_after_sync();
-            int ks = 0, ks_use = 0;
-            for (int li = 0; li < nlocal; ++li) {
+            for (int li = (warp == MMA_WARP ? 0 : 1); li < nlocal; li += 2) {
                 const int st = li & 1, use = li >> 1;
+                const int ks = li % KS_STAGES, ks_use = li / KS_STAGES;
                 wait_or_flag(&bars->acc_empty[st], (use & 1) ^ 1);
                 wait_or_flag(&bars->ks_full[ks], ks_use & 1);
                 tc_fence_after_sync();
@@ -287,10 +312,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 tc_commit(&bars->ks_empty[ks]);
                 tc_commit(&bars->acc_full[st]);
-                if (++ks == KS_STAGES) {
-                    ks = 0;
-                    ++ks_use;
-                }
             }
         }
         __syncwarp();
@@ -299,6 +320,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int quarter = warp & 3;                       // TMEM lanes 32*quarter .. +31
         const int row = 32 * quarter + lane;                // query row within the group
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+        if (pair) wait_or_flag(&bars->q_peer, 0);   // the peer's 64 rows have landed
         // This warp's 32 query rows: staged slices -> TMEM (A operand).
         for (int c = 0; c < D / 8; ++c) {
 #pragma unroll
@@ -454,6 +476,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    if (pair) cluster_sync_all();  // no CTA leaves while its pair may still touch it
     if (warp == MMA_WARP) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, TMEM_COLS);
@@ -521,18 +544,26 @@ cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    // CTA pairs when every group's CTA count is even (always at full size).
+    const int pair = (per % 2 == 0) ? 1 : 0;
+    cudaLaunchAttribute attrs[2];
+    attrs[0] = attr[0];
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = pair ? 2 : 1;
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 2;
     CUtensorMap out_map;
     memset(&out_map, 0, sizeof(out_map));
     const int use_tma = encode_out_map(&out_map, scores, nq, active) ? 1 : 0;
     if (kq8 != nullptr)
         return cudaLaunchKernelEx(&cfg, scores_tc_kernel<true>, q, static_cast<const float *>(nullptr), kq8,
                                   reinterpret_cast<const __half *>(kscale), nq, active, ntiles, per, scores,
-                                  out_map, use_tma);
+                                  out_map, use_tma, pair);
     return cudaLaunchKernelEx(&cfg, scores_tc_kernel<false>, q, kblk, static_cast<const int8_t *>(nullptr),
                               static_cast<const __half *>(nullptr), nq, active, ntiles, per, scores, out_map,
-                              use_tma);
+                              use_tma, pair);
 }
 
 cudaError_t tc_error_read_clear(uint32_t *word, cudaStream_t stream) {
