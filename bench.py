@@ -7,8 +7,10 @@ inputs are the seeded synthetic full-capacity workload: q and keys
 Student-t(3) at unit variance.
 
 Prints ONE JSON line (rank 0). ``value`` is query-blocks per second over all
-ranks; ``ms_per_step`` the device time of one step (CUDA events on the
-launching stream, L2 flushed before every step and the flush untimed);
+ranks; ``ms_per_step`` the device time of one step (one CUDA event pair
+around both calls on the launching stream, L2 flushed before every step and
+the flush untimed; every other step carries an extra event between the
+calls, which gives each kernel's duration);
 ``roofline`` describes the dominant kernel; ``e2e`` repeats the measurement
 through the public API with host buffers (pinned H2D of q and the active
 keys, D2H of the ids, all inside the timed region); ``cpu_baseline`` times
@@ -80,6 +82,12 @@ def load_peaks() -> dict:
 def source_sha(fname: str) -> str:
     with open(os.path.join(CSRC, fname), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def pct(xs, p):
+    """p-th percentile (nearest rank) of a list of floats."""
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, max(0, int(round(p / 100 * (len(ys) - 1)))))]
 
 
 def recorded_traffic(kernel: str, fname: str):
@@ -285,21 +293,28 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    # Even steps: one event pair around both calls (the step time; the top-k
+    # may launch under the scorer's tail). Odd steps: an extra event between
+    # the calls gives each kernel's duration (the roofline's denominator).
     for i in range(K_):
         if not args.no_flush:
             flush.fill_(float(i))
         ev[i][0].record(stream)
         score()
-        ev[i][1].record(stream)
+        if i & 1 or K_ == 1:
+            ev[i][1].record(stream)
         topk()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
-    t_score = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K_)]
-    t_topk = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K_)]
-    step_ms_local = sum(a + b for a, b in zip(t_score, t_topk)) / K_
+    split = [i for i in range(K_) if i & 1 or K_ == 1]
+    whole = [i for i in range(K_) if not i & 1]
+    t_score = [ev[i][0].elapsed_time(ev[i][1]) for i in split]
+    t_topk = [ev[i][1].elapsed_time(ev[i][2]) for i in split]
+    t_step = [ev[i][0].elapsed_time(ev[i][2]) for i in whole]
+    step_ms_local = statistics.mean(t_step)
     step_ms = max_over_ranks(step_ms_local, world, dev)
     if qsa.device_error(dev) != 0:
         raise SystemExit("a QSA kernel reported a timed-out wait; results invalid")
@@ -346,7 +361,10 @@ def main():
                          f"flushed before every step by a {2 * l2 >> 20} MiB write, flush untimed",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kernels_us": {"scores": score_us, "topk": topk_us,
-                       "scores_p50": 1e3 * statistics.median(t_score), "topk_p50": 1e3 * statistics.median(t_topk)},
+                       "scores_p50": 1e3 * statistics.median(t_score), "topk_p50": 1e3 * statistics.median(t_topk),
+                       "steps_timed_split": len(split)},
+        "step_us": {"mean": 1e3 * step_ms_local, "p10": 1e3 * pct(t_step, 10), "p50": 1e3 * pct(t_step, 50),
+                    "p90": 1e3 * pct(t_step, 90), "steps": len(t_step)},
         "roofline": roof,
         "step_roofline": {"floor_us": floor_us, "frac": floor_us / (step_ms * 1e3),
                           "note": "algorithmic step bytes at the HBM peak (the step's binding roof when "
