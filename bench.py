@@ -13,8 +13,10 @@ the flush untimed; every other step carries an extra event between the
 calls, which gives each kernel's duration);
 ``roofline`` describes the dominant kernel; ``e2e`` repeats the measurement
 through the public API with host buffers (pinned H2D of q and the active
-keys, D2H of the ids, all inside the timed region); ``cpu_baseline`` times
-the CPU oracle on this machine's cores.
+keys, D2H of the ids, all inside the timed region; consecutive steps are
+pipelined over two input buffers, the copy of one step overlapping the
+kernels of the previous one); ``cpu_baseline`` times the CPU oracle on this
+machine's cores.
 
 ``--impl reference`` times the CPU oracle itself as the reference arm.
 Under torchrun each rank runs an independent replica (no collective on the
@@ -377,38 +379,51 @@ def main():
 
     # End to end through the public API with host buffers.
     if not args.no_e2e:
+        # End to end through the public API with host buffers: every step
+        # copies its q and active keys from pinned host memory, runs both calls
+        # and reads the ids back. Steps are pipelined the way a server would
+        # run them: two device input buffers, the copy of step i+1 (copy
+        # stream) overlapping the kernels of step i (compute stream).
         q_h = torch.from_numpy(W.q).pin_memory()
         k_h = torch.from_numpy(np.ascontiguousarray(W.kblk[:W.active])).pin_memory()
-        ids_h = torch.empty((W.nq, W.k), dtype=torch.int32).pin_memory()
-        q_d = torch.empty_like(q_h, device=dev)
-        k_d = torch.empty((W.max_blocks, 128), dtype=torch.float32, device=dev)
-
-        def e2e_step():
-            q_d.copy_(q_h, non_blocking=True)
-            k_d[:W.active].copy_(k_h, non_blocking=True)
-            s = qsa.block_scores(q_d, k_d, W.active, out=scores)
-            qsa.block_topk(s, W.k, out=ids)
-            ids_h.copy_(ids, non_blocking=True)
-
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize()
+        ids_h = [torch.empty((W.nq, W.k), dtype=torch.int32).pin_memory() for _ in range(2)]
+        q_d = [torch.empty_like(q_h, device=dev) for _ in range(2)]
+        k_d = [torch.empty((W.max_blocks, 128), dtype=torch.float32, device=dev) for _ in range(2)]
+        ids_d = [torch.empty((W.nq, W.k), dtype=torch.int32, device=dev) for _ in range(2)]
+        copy_stream = torch.cuda.Stream(dev)
         n_e = min(args.e2e_steps, K_)
+
+        def run_pipeline(n):
+            copied = [torch.cuda.Event() for _ in range(n)]
+            done = [torch.cuda.Event() for _ in range(n)]
+            for i in range(n):
+                b = i & 1
+                with torch.cuda.stream(copy_stream):
+                    if i >= 2:
+                        copy_stream.wait_event(done[i - 2])      # buffer b is free again
+                    q_d[b].copy_(q_h, non_blocking=True)
+                    k_d[b][:W.active].copy_(k_h, non_blocking=True)
+                    copied[i].record(copy_stream)
+                stream.wait_event(copied[i])
+                s = qsa.block_scores(q_d[b], k_d[b], W.active, out=scores)
+                qsa.block_topk(s, W.k, out=ids_d[b])
+                ids_h[b].copy_(ids_d[b], non_blocking=True)
+                done[i].record(stream)
+
+        run_pipeline(4)
+        torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        tot = 0.0
-        for i in range(n_e):
-            if not args.no_flush:
-                flush.fill_(float(i))
-            e0.record(stream)
-            e2e_step()
-            e1.record(stream)
-            e1.synchronize()
-            tot += e0.elapsed_time(e1)
-        e_ms = max_over_ranks(tot / n_e, world, dev)
-        assert np.array_equal(ids_h.numpy(), ids.cpu().numpy())
+        e0.record(stream)
+        copy_stream.wait_event(e0)
+        run_pipeline(n_e)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e, world, dev)
+        assert np.array_equal(ids_h[(n_e - 1) & 1].numpy(), ids.cpu().numpy())
         line["e2e"] = {"value": world * units_per_step / (e_ms * 1e-3), "unit": UNIT, "ms_per_step": e_ms,
                        "steps": n_e, "h2d_bytes_per_step": q_h.numel() * 4 + k_h.numel() * 4,
-                       "d2h_bytes_per_step": ids_h.numel() * 4}
+                       "d2h_bytes_per_step": ids_h[0].numel() * 4,
+                       "pipeline": "two input buffers; the H2D copy of step i+1 overlaps the kernels of step i"}
 
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_baseline(W)
