@@ -54,6 +54,8 @@ qsa_status qsa_block_scores(const float *q, const float *kblk, int nq, int max_b
     qsa_status s = check_score_args(q, nq, max_blocks, active_blocks, scores);
     if (s != QSA_OK || nq == 0 || active_blocks == 0) return s;
     if (kblk == nullptr || !aligned16(kblk)) return QSA_ERR_INVALID;
+    if (nq <= qsa::SMALL_NQ_MAX)
+        return from_cuda(qsa::launch_scores_rows(q, kblk, nullptr, nullptr, nq, active_blocks, scores, stream));
     return from_cuda(qsa::launch_scores_tc(q, kblk, nullptr, nullptr, nq, active_blocks, scores, stream));
 }
 
@@ -63,6 +65,8 @@ qsa_status qsa_block_scores_q8(const float *q, const int8_t *kblk_q8, const uint
     if (s != QSA_OK || nq == 0 || active_blocks == 0) return s;
     if (kblk_q8 == nullptr || kscale_f16 == nullptr || !aligned16(kblk_q8)) return QSA_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(kscale_f16) & 1u) != 0) return QSA_ERR_INVALID;
+    if (nq <= qsa::SMALL_NQ_MAX)
+        return from_cuda(qsa::launch_scores_rows(q, nullptr, kblk_q8, kscale_f16, nq, active_blocks, scores, stream));
     return from_cuda(qsa::launch_scores_tc(q, nullptr, kblk_q8, kscale_f16, nq, active_blocks, scores, stream));
 }
 

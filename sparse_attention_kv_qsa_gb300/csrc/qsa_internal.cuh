@@ -22,6 +22,12 @@ cudaError_t launch_scores_ffma(const float *q, const float *kblk, const int8_t *
 cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,
                              int nq, int active, float *scores, cudaStream_t stream);
 
+// Scores for nq <= 4 (decode) on CUDA cores, the grid spanning key rows.
+// Exactly one of kblk / (kq8, kscale) is non-null.
+constexpr int SMALL_NQ_MAX = 4;
+cudaError_t launch_scores_rows(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,
+                               int nq, int active, float *scores, cudaStream_t stream);
+
 // Exact top-k (k < active); one CTA per row.
 cudaError_t launch_topk(const float *scores, int nq, int active, int k, int32_t *ids,
                         cudaStream_t stream);

@@ -128,6 +128,19 @@ def test_int8_ragged(dev, o, scorer, nq, active, k):
     check_select(o, W, gpu_scores(W, dev, scorer))
 
 
+@pytest.mark.parametrize("nq,active", [(1, 1), (2, 63), (3, 4099), (4, 65536), (1, 70001)])
+def test_small_nq_fp32_keys(dev, o, nq, active):
+    """nq <= 4 takes the CUDA-core row scorer (grid over key rows)."""
+    W = w.normal_case(nq=nq, active=active, k=min(64, active))
+    check_select(o, W, gpu_scores(W, dev))
+
+
+@pytest.mark.parametrize("nq,active", [(2, 517), (3, 65535), (4, 1)])
+def test_small_nq_int8_keys(dev, o, nq, active):
+    W = w.int8_case(nq, active, min(50, active), max_blocks=active + 1)
+    check_select(o, W, gpu_scores(W, dev))
+
+
 def _tie_heavy(nq, active, seed):
     u = w.u32(seed, 11, nq * active).reshape(nq, active)
     s = ((u % 7).astype(np.float32) - 3.0) * 0.5          # 7 values: heavy ties
@@ -233,10 +246,11 @@ def test_topk_k_at_least_active(dev, o, active, k):
     assert np.array_equal(ids, o.topk_f32(S, k))
 
 
-def test_outputs_stay_in_bounds(dev, o):
+@pytest.mark.parametrize("nq", [37, 3])
+def test_outputs_stay_in_bounds(dev, o, nq):
     """Canary words after the scores and ids must survive; capacity rows
     (NaN) must not be read."""
-    W = w.normal_case(nq=37, active=2051, k=100, max_blocks=2300)
+    W = w.normal_case(nq=nq, active=2051, k=100, max_blocks=2300)
     q, kb = to_dev(W.q, dev), to_dev(W.kblk, dev)
     n_s, n_i = W.nq * W.active, W.nq * W.k
     buf_s = torch.full((n_s + 64,), 12345.0, dtype=torch.float32, device=dev)
