@@ -67,6 +67,9 @@ typedef enum {
  * Accuracy: |scores - exact| <= 1e-6 * max_b |exact[i][b]| per row for
  * finite inputs; scores are exact when every product and partial sum is an
  * integer below 2^24 in magnitude.
+ * Kernels: nq >= 5 runs on the tensor cores (3-way exact bf16 split, hi*hi in
+ * its own accumulator); nq <= 4 (decode) on CUDA cores with one fp32 FMA
+ * chain per query and key row. Both meet the accuracy bound above.
  * ("#3108 ...", Summary item 4; "#337 ...", What items 1-2.)
  */
 qsa_status qsa_block_scores(const float *q, const float *kblk, int nq, int max_blocks,
