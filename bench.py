@@ -86,6 +86,61 @@ def source_sha(fname: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
+def decode_side_measurement(dev, stream):
+    """Decode-shaped calls (int8 keys, k=128, 262,144 cells = 65,536 blocks;
+    nq = 1 and 4): launch- and latency-bound, so reported in microseconds per
+    score + top-k step, once with a CUDA-event pair per step (L2 flushed
+    first) and once per step of a CUDA graph of 20 back-to-back steps."""
+    import torch
+    import sparse_attention_kv_qsa_gb300 as qsa
+    from sparse_attention_kv_qsa_gb300 import workloads as w
+    out = {"workload": "decode: int8 keys + binary16 scales, 262,144 cells (65,536 blocks), k=128", "unit": "us"}
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    for nq in (1, 4):
+        W = w.decode(nq, 262144)
+        q = torch.from_numpy(W.q).to(dev)
+        kq = torch.from_numpy(W.kq8).to(dev)
+        ks = torch.from_numpy(W.kscale.view(np.int16)).to(dev)
+        s = torch.empty((nq, W.active), dtype=torch.float32, device=dev)
+        ids = torch.empty((nq, W.k), dtype=torch.int32, device=dev)
+
+        def step():
+            qsa.block_scores_q8(q, kq, ks, W.active, out=s)
+            qsa.block_topk(s, W.k, out=ids)
+
+        for _ in range(5):
+            step()
+        torch.cuda.synchronize()
+        ts = []
+        for i in range(50):
+            flush.fill_(float(i))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(1e3 * e0.elapsed_time(e1))
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            step()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(20):
+                    step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[f"nq{nq}"] = {"step_p50": pct(ts, 50), "step_p10": pct(ts, 10), "step_p90": pct(ts, 90),
+                          "graph_step": 1e3 * e0.elapsed_time(e1) / 20}
+    return out
+
+
 def pct(xs, p):
     """p-th percentile (nearest rank) of a list of floats."""
     ys = sorted(xs)
@@ -239,6 +294,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="warm L2 (back-to-back steps)")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped side measurement")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -424,6 +480,9 @@ def main():
                        "steps": n_e, "h2d_bytes_per_step": q_h.numel() * 4 + k_h.numel() * 4,
                        "d2h_bytes_per_step": ids_h[0].numel() * 4,
                        "pipeline": "two input buffers; the H2D copy of step i+1 overlaps the kernels of step i"}
+
+    if rank == 0 and not args.no_decode:
+        line["decode"] = decode_side_measurement(dev, stream)
 
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_baseline(W)
