@@ -22,7 +22,7 @@
 // of a 256-query call is in flight at once):
 //  Rows of at least 16,384 scores first try a listing path. A strided 1/32
 //  sample of the row (loaded first, so it is not queued behind the row) fixes
-//  a threshold expected to pass about 2.5k scores, while the row itself is
+//  a threshold expected to pass about 1.8k scores, while the row itself is
 //  requested into L2 (bulk prefetch); one pass of 16-byte read-only loads then
 //  lists every score at or above the threshold, and the digits below run on
 //  that list alone. A list shorter than k or longer
@@ -230,16 +230,19 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
 
     // Listing path (rows of at least FAST_MIN_ACTIVE scores). A strided sample
     // (one 16-byte group of scores per 512 bytes) gives a threshold that about
-    // 2.5k scores of the row are expected to reach: the sample's r-th largest
-    // key with r = ceil(2.5 k * samples / n) + 8, found to 16 bits (two 8-bit
-    // sample digits). One pass then lists every score at or above it. A list of
+    // 1.8k + 8 n / samples scores of the row are expected to reach: the
+    // sample's r-th largest key with r = ceil(1.8 k * samples / n) + 8, found to
+    // 16 bits (two 8-bit sample digits). The sample keys above the true k-th
+    // key number Binomial(samples, k / n) (mean 16 at k = 512 of 65,536), so
+    // a list shorter than k needs that count to reach r (37 there): about
+    // 5 standard deviations. One pass then lists every score at or above it. A list of
     // at least k entries holds the whole top-k, ties included, so when it also
     // fits its capacity the exact selection runs on the list alone; otherwise
     // the row takes the exact two-pass path.
     const int nsv = nvec / SAMPLE_STRIDE;
     const uint32_t nsamp = 4u * static_cast<uint32_t>(nsv);
     const uint32_t r_target =
-        static_cast<uint32_t>((5ull * static_cast<uint64_t>(k) * nsamp + 2ull * n - 1) / (2ull * n)) + 8u;
+        static_cast<uint32_t>((9ull * static_cast<uint64_t>(k) * nsamp + 5ull * n - 1) / (5ull * n)) + 8u;
     const bool try_list = n >= FAST_MIN_ACTIVE && r_target <= nsamp / 2;
 
     // The scores may come from the previous grid on the stream (launched as
