@@ -20,7 +20,7 @@
 //
 // GB300 layout. One 512-thread CTA owns one row (two CTAs per SM, so every row
 // of a 256-query call is in flight at once):
-//  Rows of at least 16,384 scores first try a listing path. A strided 1/32
+//  Rows of at least 8,192 scores first try a listing path. A strided 1/32
 //  sample of the row (loaded first, so it is not queued behind the row) fixes
 //  a threshold expected to pass about 1.8k scores, while the row itself is
 //  requested into L2 (bulk prefetch); one pass of 16-byte read-only loads then
@@ -53,7 +53,7 @@ constexpr int UNROLL = 4;                // 16-byte loads in flight per thread (
 constexpr int LIST_VEC = 8;              // 16-byte loads per thread per listing step: 32 scores
 constexpr int CAND_MAX = 4096;           // candidate-list capacity
 constexpr int SAMPLE_STRIDE = 32;        // one 16-byte group of scores sampled per 512 bytes
-constexpr int FAST_MIN_ACTIVE = 16384;   // shorter rows take the exact passes directly
+constexpr int FAST_MIN_ACTIVE = 8192;    // shorter rows take the exact passes directly
 constexpr int MAX_ACTIVE = 393216;
 constexpr int SAMPLE_REGS = (MAX_ACTIVE / 4 / SAMPLE_STRIDE + ROW_THREADS - 1) / ROW_THREADS;
 constexpr uint32_t PREFETCH_CHUNK = 32768;     // bytes per L2 prefetch request

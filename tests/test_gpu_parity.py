@@ -163,11 +163,12 @@ def test_topk_exact_on_given_scores(dev, o, nq, active, k):
     parity.check_ids_valid(ids, active, k)
 
 
-@pytest.mark.parametrize("m", [4095, 4096, 4097, 9000])
+@pytest.mark.parametrize("m", [4095, 4096, 4097, 8000])
 def test_topk_candidate_list_capacity(dev, o, m):
-    """The leading-digit bin holds m keys: at and below the candidate-list
-    capacity (4,096) the refinement runs on the list, above it on the row."""
-    active = 10003
+    """Exact path (rows under 8,192 scores): the leading-digit bin holds m
+    keys; at and below the candidate-list capacity (4,096) the refinement
+    runs on the list, above it on the row."""
+    active = 8191
     S = np.full((2, active), -1.0, dtype=np.float32)
     S[:, :100] = 4.0 + np.arange(100, dtype=np.float32) * 0.01
     vals = (1.0 + np.arange(m, dtype=np.float64) * 2.0 ** -20).astype(np.float32)
@@ -200,7 +201,8 @@ def test_topk_sample_sees_only_the_largest(dev, o):
 
 
 @pytest.mark.parametrize("nq,active,k", [(5, 70001, 64), (3, 70003, 700), (3, 100002, 5000),
-                                         (2, 16384, 1000), (2, 16383, 1000), (2, 393215, 1200),
+                                         (2, 16384, 1000), (2, 16383, 1000), (3, 8192, 700), (3, 8191, 700),
+                                         (2, 393215, 1200),
                                          (2, 393215, 4000)])
 def test_topk_ragged_rows_random(dev, o, nq, active, k):
     """Rows of odd length start at every 4-byte offset, so the listing pass
