@@ -21,11 +21,9 @@
 // GB300 layout. One 512-thread CTA owns one row (two CTAs per SM, so every row
 // of a 256-query call is in flight at once):
 //  Rows of at least 8,192 scores first try a listing path. A strided 1/32
-//  sample of the row (loaded first, so it is not queued behind the row) fixes
-//  a threshold expected to pass about 1.8k scores, while the row itself is
-//  requested into L2 (bulk prefetch); one pass of 16-byte read-only loads then
-//  lists every score at or above the threshold, and the digits below run on
-//  that list alone. A list shorter than k or longer
+//  sample of the row fixes a threshold expected to pass about 1.8k scores;
+//  one pass of 16-byte read-only loads then lists every score at or above
+//  the threshold, and the digits below run on that list alone. A list shorter than k or longer
 //  than its capacity sends the row to the exact passes, so the result is
 //  exact either way.
 //  Exact passes: pass A reads the row and builds the 11-bit histogram in
@@ -56,7 +54,6 @@ constexpr int SAMPLE_STRIDE = 32;        // one 16-byte group of scores sampled 
 constexpr int FAST_MIN_ACTIVE = 8192;    // shorter rows take the exact passes directly
 constexpr int MAX_ACTIVE = 393216;
 constexpr int SAMPLE_REGS = (MAX_ACTIVE / 4 / SAMPLE_STRIDE + ROW_THREADS - 1) / ROW_THREADS;
-constexpr uint32_t PREFETCH_CHUNK = 32768;     // bytes per L2 prefetch request
 constexpr uint32_t NEG_INF_KEY = 0x007FFFFFu;  // key of -inf (and of NaN)
 constexpr uint32_t QNAN_BITS = 0x7FC00000u;
 
@@ -249,7 +246,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
     // its programmatic dependent); nothing global is read before this.
     grid_dependency_wait();
 
-    // The sample is requested before anything else, ahead of the row's prefetch.
+    // The sample is requested before anything else.
     uint4 sx[SAMPLE_REGS];
 #pragma unroll
     for (int u = 0; u < SAMPLE_REGS; ++u) {
@@ -274,13 +271,6 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
     bool listed = false;
     uint32_t tg = 0u, kmax = 0u;
     if (try_list) {
-        if (warp == ROW_WARPS - 1) {
-            // One chunk per lane: a warp issues the whole row's prefetch at once
-            // (a single thread issuing them one by one held its warp ~0.7 us).
-            const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
-            for (uint32_t off = static_cast<uint32_t>(lane) * PREFETCH_CHUNK; off < bytes; off += 32u * PREFETCH_CHUNK)
-                bulk_prefetch_l2(reinterpret_cast<const unsigned char *>(g4) + off, min(PREFETCH_CHUNK, bytes - off));
-        }
         // First sample digit: the top 8 key bits. Sample keys crowd into a few
         // of these bins, so each warp counts into its own copy; 256 threads
         // then add the copies up.
