@@ -255,7 +255,8 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
     }
 
     if (tid == 0) sh.cand_n = 0u;
-    for (int i = tid; i < HIST_A; i += ROW_THREADS) sh.histA[i] = 0u;
+    if (!try_list)
+        for (int i = tid; i < HIST_A; i += ROW_THREADS) sh.histA[i] = 0u;   // the exact path's histogram
     for (int i = tid; i < BINS_R; i += ROW_THREADS) sh.histR[i] = 0u;
     if (try_list) {
         uint4 *w4 = reinterpret_cast<uint4 *>(sh.whist);
@@ -398,8 +399,12 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
             kmax = max(max(kmax, t.x), max(t.y, max(t.z, t.w)));
         }
         listed = nc >= kk && nc <= static_cast<uint32_t>(CAND_MAX);
-        __syncthreads();
-        if (!listed && tid == 0) sh.cand_n = 0u;  // the list is abandoned
+        if (!listed) {  // uniform: the list is abandoned; the exact path follows
+            __syncthreads();
+            if (tid == 0) sh.cand_n = 0u;
+            for (int i = tid; i < HIST_A; i += ROW_THREADS) sh.histA[i] = 0u;
+            __syncthreads();
+        }
     }
 
     // Digit search. On the list, every key lies in [tg, kmax], so the search
