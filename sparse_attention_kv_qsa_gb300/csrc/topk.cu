@@ -536,11 +536,32 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         }
         __syncthreads();
     }
-    {
+    int32_t *out = ids + row * static_cast<size_t>(k);
+    if (wpt == 4) {
+        // Up to 65,536 scores (nwords <= 2,048): a thread's four words as one
+        // conflict-free 16-byte load, kept in registers for both passes.
+        uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
+        if (wb < nwords) w4 = *reinterpret_cast<const uint4 *>(selbits + wb);
+        // Words past nwords (the last thread, when nwords % 4 != 0) belong to
+        // the tie bitmap that follows: drop them.
+        const uint32_t wv[4] = {w4.x, wb + 1 < nwords ? w4.y : 0u, wb + 2 < nwords ? w4.z : 0u,
+                                wb + 3 < nwords ? w4.w : 0u};
+        uint32_t pos = block_excl_scan(__popc(wv[0]) + __popc(wv[1]) + __popc(wv[2]) + __popc(wv[3]), sh.scan_tot,
+                                       lane, warp);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            uint32_t bits = wv[e];
+            while (bits != 0u) {
+                const int b = __ffs(bits) - 1;
+                bits &= bits - 1u;
+                if (pos < static_cast<uint32_t>(k)) out[pos] = (wb + e) * 32 + b;  // always, for consistent counts
+                ++pos;
+            }
+        }
+    } else {
         uint32_t c = 0u;
         for (int wd = wb; wd < we; ++wd) c += __popc(selbits[wd]);
         uint32_t pos = block_excl_scan(c, sh.scan_tot, lane, warp);
-        int32_t *out = ids + row * static_cast<size_t>(k);
         for (int wd = wb; wd < we; ++wd) {
             uint32_t bits = selbits[wd];
             while (bits != 0u) {

@@ -202,6 +202,7 @@ def test_topk_sample_sees_only_the_largest(dev, o):
 
 @pytest.mark.parametrize("nq,active,k", [(5, 70001, 64), (3, 70003, 700), (3, 100002, 5000),
                                          (2, 16384, 1000), (2, 16383, 1000), (3, 8192, 700), (3, 8191, 700),
+                                         (3, 50001, 600), (2, 49153, 3000),
                                          (2, 393215, 1200),
                                          (2, 393215, 4000)])
 def test_topk_ragged_rows_random(dev, o, nq, active, k):
