@@ -319,20 +319,13 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         // whole row, so such a row takes the exact path at once. Each thread
         // gathers one hit bit per score of a 32-score step; a warp scan of the
         // hit counts and one shared-memory atomic per warp and step give every
-        // hit its list slot, and the hit's score is read again (an L1 hit: the
-        // warp has just loaded it) for its key. The largest listed key is kept.
+        // hit its list slot, which records the score's index.
         if (tg > NEG_INF_KEY) {
             const float ft = __uint_as_float(tg >= 0x80000000u ? (tg ^ 0x80000000u) : ~tg);
             auto list_scalar = [&](int i) {
-                const uint32_t bits = __ldg(g + i);
-                if (__uint_as_float(bits) >= ft) {
-                    const uint32_t key = float_bits_to_key(bits);
-                    kmax = max(kmax, key);
+                if (__uint_as_float(__ldg(g + i)) >= ft) {
                     const uint32_t slot = atomicAdd(&sh.cand_n, 1u);
-                    if (slot < static_cast<uint32_t>(CAND_MAX)) {
-                        sh.cand_idx[slot] = static_cast<uint32_t>(i);
-                        sh.cand_key[slot] = key;
-                    }
+                    if (slot < static_cast<uint32_t>(CAND_MAX)) sh.cand_idx[slot] = static_cast<uint32_t>(i);
                 }
             };
             for (int i = tid; i < head; i += ROW_THREADS) list_scalar(i);
@@ -377,10 +370,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
                         hits &= hits - 1u;
                         if (slot < static_cast<uint32_t>(CAND_MAX)) {
                             const int i = i0 + 4 * ROW_THREADS * (j >> 2) + (j & 3);
-                            const uint32_t key = float_bits_to_key(__ldg(g + i));
-                            kmax = max(kmax, key);
                             sh.cand_idx[slot] = static_cast<uint32_t>(i);
-                            sh.cand_key[slot] = key;
                         }
                         ++slot;
                     }
@@ -389,17 +379,29 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         } else if (tid == 0) {
             sh.cand_n = static_cast<uint32_t>(CAND_MAX) + 1u;  // would list the whole row
         }
-        kmax = __reduce_max_sync(FULL_MASK, kmax);
-        if (lane == 0) sh.scan_tot[warp] = kmax;
         __syncthreads();
         const uint32_t nc = sh.cand_n;
-#pragma unroll
-        for (int q = 0; q < ROW_WARPS / 4; ++q) {
-            const uint4 t = *reinterpret_cast<const uint4 *>(sh.scan_tot + 4 * q);
-            kmax = max(max(kmax, t.x), max(t.y, max(t.z, t.w)));
-        }
         listed = nc >= kk && nc <= static_cast<uint32_t>(CAND_MAX);
-        if (!listed) {  // uniform: the list is abandoned; the exact path follows
+        if (listed) {
+            // Keys of the listed scores, read again as one batch (the loads
+            // are independent, so this costs about one L2 round trip; reading
+            // each hit's score inside the listing loop stalled it), and the
+            // largest of them.
+#pragma unroll 4
+            for (int j = tid; j < static_cast<int>(nc); j += ROW_THREADS) {
+                const uint32_t key = float_bits_to_key(__ldg(g + sh.cand_idx[j]));
+                sh.cand_key[j] = key;
+                kmax = max(kmax, key);
+            }
+            kmax = __reduce_max_sync(FULL_MASK, kmax);
+            if (lane == 0) sh.scan_tot[warp] = kmax;
+            __syncthreads();
+#pragma unroll
+            for (int q = 0; q < ROW_WARPS / 4; ++q) {
+                const uint4 t = *reinterpret_cast<const uint4 *>(sh.scan_tot + 4 * q);
+                kmax = max(max(kmax, t.x), max(t.y, max(t.z, t.w)));
+            }
+        } else {  // uniform: the list is abandoned; the exact path follows
             __syncthreads();
             if (tid == 0) sh.cand_n = 0u;
             for (int i = tid; i < HIST_A; i += ROW_THREADS) sh.histA[i] = 0u;
