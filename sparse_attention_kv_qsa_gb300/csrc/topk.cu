@@ -319,13 +319,20 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         // whole row, so such a row takes the exact path at once. Each thread
         // gathers one hit bit per score of a 32-score step; a warp scan of the
         // hit counts and one shared-memory atomic per warp and step give every
-        // hit its list slot, which records the score's index.
+        // hit its list slot, which records the score's index; the score itself
+        // is copied into the slot by an asynchronous 4-byte copy (re-reading it
+        // into a register, or gathering the listed scores after the pass,
+        // each stalled on an L2 round trip).
         if (tg > NEG_INF_KEY) {
             const float ft = __uint_as_float(tg >= 0x80000000u ? (tg ^ 0x80000000u) : ~tg);
+            const uint32_t key_base = smem_u32(sh.cand_key);
             auto list_scalar = [&](int i) {
                 if (__uint_as_float(__ldg(g + i)) >= ft) {
                     const uint32_t slot = atomicAdd(&sh.cand_n, 1u);
-                    if (slot < static_cast<uint32_t>(CAND_MAX)) sh.cand_idx[slot] = static_cast<uint32_t>(i);
+                    if (slot < static_cast<uint32_t>(CAND_MAX)) {
+                        sh.cand_idx[slot] = static_cast<uint32_t>(i);
+                        cp_async_4(key_base + 4u * slot, g + i);
+                    }
                 }
             };
             for (int i = tid; i < head; i += ROW_THREADS) list_scalar(i);
@@ -371,6 +378,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
                         if (slot < static_cast<uint32_t>(CAND_MAX)) {
                             const int i = i0 + 4 * ROW_THREADS * (j >> 2) + (j & 3);
                             sh.cand_idx[slot] = static_cast<uint32_t>(i);
+                            cp_async_4(key_base + 4u * slot, g + i);
                         }
                         ++slot;
                     }
@@ -379,17 +387,15 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         } else if (tid == 0) {
             sh.cand_n = static_cast<uint32_t>(CAND_MAX) + 1u;  // would list the whole row
         }
+        cp_async_wait_all();  // this thread's copies of listed scores have landed
         __syncthreads();
         const uint32_t nc = sh.cand_n;
         listed = nc >= kk && nc <= static_cast<uint32_t>(CAND_MAX);
         if (listed) {
-            // Keys of the listed scores, read again as one batch (the loads
-            // are independent, so this costs about one L2 round trip; reading
-            // each hit's score inside the listing loop stalled it), and the
-            // largest of them.
+            // The listed scores become keys in place; the largest is kept.
 #pragma unroll 4
             for (int j = tid; j < static_cast<int>(nc); j += ROW_THREADS) {
-                const uint32_t key = float_bits_to_key(__ldg(g + sh.cand_idx[j]));
+                const uint32_t key = float_bits_to_key(sh.cand_key[j]);
                 sh.cand_key[j] = key;
                 kmax = max(kmax, key);
             }
