@@ -51,6 +51,7 @@ constexpr int UNROLL = 4;                // 16-byte loads in flight per thread (
 constexpr int LIST_VEC = 8;              // 16-byte loads per thread per listing step: 32 scores
 constexpr int CAND_MAX = 4096;           // candidate-list capacity
 constexpr int SAMPLE_STRIDE = 32;        // one 16-byte group of scores sampled per 512 bytes
+constexpr int SAMPLE_SHIFT = 18;         // sample bins: 2^18 keys = 1/32 octave; 256 bins span 8
 constexpr int FAST_MIN_ACTIVE = 8192;    // shorter rows take the exact passes directly
 constexpr int MAX_ACTIVE = 393216;
 constexpr int SAMPLE_REGS = (MAX_ACTIVE / 4 / SAMPLE_STRIDE + ROW_THREADS - 1) / ROW_THREADS;
@@ -63,7 +64,6 @@ struct RowShared {
     uint32_t histA[HIST_A];
     uint32_t groupA[HIST_A / GROUP];
     uint32_t histR[BINS_R];
-    uint32_t whist[ROW_WARPS * BINS_R];  // per-warp sample histograms
     uint32_t cand_key[CAND_MAX];
     uint32_t cand_idx[CAND_MAX];
     alignas(16) uint32_t scan_tot[ROW_WARPS];
@@ -229,10 +229,10 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
     // (one 16-byte group of scores per 512 bytes) gives a threshold that about
     // 1.8k + 8 n / samples scores of the row are expected to reach: the
     // sample's r-th largest key with r = ceil(1.8 k * samples / n) + 8, found to
-    // 16 bits (two 8-bit sample digits). The sample keys above the true k-th
-    // key number Binomial(samples, k / n) (mean 16 at k = 512 of 65,536), so
-    // a list shorter than k needs that count to reach r (37 there): about
-    // 5 standard deviations. One pass then lists every score at or above it. A list of
+    // 1/32 of an octave. The sample keys above the true k-th key number
+    // Binomial(samples, k / n) (mean 16 at k = 512 of 65,536), so a list
+    // shorter than k needs that count to reach r (37 there): about 5 standard
+    // deviations. One pass then lists every score at or above it. A list of
     // at least k entries holds the whole top-k, ties included, so when it also
     // fits its capacity the exact selection runs on the list alone; otherwise
     // the row takes the exact two-pass path.
@@ -258,10 +258,6 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
     if (!try_list)
         for (int i = tid; i < HIST_A; i += ROW_THREADS) sh.histA[i] = 0u;   // the exact path's histogram
     for (int i = tid; i < BINS_R; i += ROW_THREADS) sh.histR[i] = 0u;
-    if (try_list) {
-        uint4 *w4 = reinterpret_cast<uint4 *>(sh.whist);
-        for (int i = tid; i < ROW_WARPS * BINS_R / 4; i += ROW_THREADS) w4[i] = make_uint4(0u, 0u, 0u, 0u);
-    }
     for (int i = tid; i < nwords; i += ROW_THREADS) {
         selbits[i] = 0u;
         tiebits[i] = 0u;
@@ -272,45 +268,50 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
     bool listed = false;
     uint32_t tg = 0u, kmax = 0u;
     if (try_list) {
-        // First sample digit: the top 8 key bits. Sample keys crowd into a few
-        // of these bins, so each warp counts into its own copy; 256 threads
-        // then add the copies up.
-        uint32_t *wh = sh.whist + warp * BINS_R;
+        // Sample threshold. The largest sample key smax tops a window of 256
+        // bins, each 2^18 keys wide (1/32 of an octave for normal floats),
+        // reaching 8 octaves below it. Counting the sample keys by their
+        // distance below smax spreads them over the bins (bins of fixed key
+        // digits crowd them into a few, which serialises the shared-memory
+        // atomics). tg is the lowest key of the bin where the count from the
+        // top reaches r, so at least r sample keys are >= tg. A sample whose
+        // r-th key lies below the window leaves tg = 0: the exact path.
+        uint32_t ks[SAMPLE_REGS][4];
+        uint32_t m = 0u;
+#pragma unroll
+        for (int u = 0; u < SAMPLE_REGS; ++u) {
+            ks[u][0] = float_bits_to_key(sx[u].x);
+            ks[u][1] = float_bits_to_key(sx[u].y);
+            ks[u][2] = float_bits_to_key(sx[u].z);
+            ks[u][3] = float_bits_to_key(sx[u].w);
+            if (tid + u * ROW_THREADS < nsv) m = max(m, max(max(ks[u][0], ks[u][1]), max(ks[u][2], ks[u][3])));
+        }
+        m = __reduce_max_sync(FULL_MASK, m);
+        if (lane == 0) sh.scan_tot[warp] = m;
+        __syncthreads();
+        uint32_t smax = 0u;
+#pragma unroll
+        for (int q = 0; q < ROW_WARPS / 4; ++q) {
+            const uint4 t = *reinterpret_cast<const uint4 *>(sh.scan_tot + 4 * q);
+            smax = max(max(smax, t.x), max(t.y, max(t.z, t.w)));
+        }
 #pragma unroll
         for (int u = 0; u < SAMPLE_REGS; ++u) {
             if (tid + u * ROW_THREADS < nsv) {
-                atomicAdd(&wh[float_bits_to_key(sx[u].x) >> 24], 1u);
-                atomicAdd(&wh[float_bits_to_key(sx[u].y) >> 24], 1u);
-                atomicAdd(&wh[float_bits_to_key(sx[u].z) >> 24], 1u);
-                atomicAdd(&wh[float_bits_to_key(sx[u].w) >> 24], 1u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t d = smax - ks[u][e];
+                    if (d < (static_cast<uint32_t>(BINS_R) << SAMPLE_SHIFT))
+                        atomicAdd(&sh.histR[BINS_R - 1 - (d >> SAMPLE_SHIFT)], 1u);
+                }
             }
         }
         __syncthreads();
-        if (tid < BINS_R) {
-            uint32_t c = 0u;
-#pragma unroll
-            for (int w = 0; w < ROW_WARPS; ++w) c += sh.whist[w * BINS_R + tid];
-            sh.histR[tid] = c;
-        }
-        __syncthreads();
+        // A target past the window's count finds no bin (count 0).
         if (warp == 0) warp_select_256(sh.histR, r_target, sh, lane);
         __syncthreads();
-        const uint32_t T8 = sh.sel_bin, rs = r_target - sh.sel_above;
-        // Second sample digit: key bits 23..16 inside that bin.
-#pragma unroll
-        for (int u = 0; u < SAMPLE_REGS; ++u) {
-            if (tid + u * ROW_THREADS < nsv) {
-                const uint32_t ks[4] = {float_bits_to_key(sx[u].x), float_bits_to_key(sx[u].y),
-                                        float_bits_to_key(sx[u].z), float_bits_to_key(sx[u].w)};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if ((ks[e] >> 24) == T8) atomicAdd(&sh.histR[(ks[e] >> 16) & 0xFFu], 1u);
-            }
-        }
-        __syncthreads();
-        if (warp == 0) warp_select_256(sh.histR, rs, sh, lane);
-        __syncthreads();
-        tg = (T8 << 24) | (sh.sel_bin << 16);
+        const uint32_t below = (static_cast<uint32_t>(BINS_R) - sh.sel_bin) << SAMPLE_SHIFT;  // (b + 1) bins
+        tg = sh.sel_cnt != 0u && smax >= below ? smax - below + 1u : 0u;
 
         // Listing pass. key(x) >= tg is tested as the fp32 comparison x >= ft,
         // ft being the value whose key is tg: both orders agree on every x (NaN

@@ -200,6 +200,27 @@ def test_topk_sample_sees_only_the_largest(dev, o):
     assert np.array_equal(ids, o.topk_f32(S, k))
 
 
+@pytest.mark.parametrize("outlier", [1e30, np.inf, 1e10, 100.0, -1e-30])
+def test_topk_sample_maximum_far_above_the_rest(dev, o, outlier):
+    """A few sampled scores (fewer than the sample rank the threshold uses)
+    far above the rest put the threshold's rank many octaves below the
+    sample maximum (1e30, inf, 1e10: past the sampled window, so the exact
+    passes run), a few octaves below it (100), or make every sampled score
+    but some tiny negatives negative and large (-1e-30 on an all-negative
+    row): the top-k stays exact."""
+    active, k = 65536, 512
+    S = w.normal32(43, 1, 3 * active).reshape(3, active).astype(np.float32)
+    if outlier < 0:
+        S = -np.abs(S) - 1.0
+    pos = _sampled_positions(active)
+    S[0, pos[:3]] = outlier
+    S[1, pos[5:25:4]] = outlier
+    S[2, pos[-2:]] = outlier
+    S[2, 7] = outlier                                  # and one unsampled
+    ids = qsa.block_topk(to_dev(S, dev), k).cpu().numpy()
+    assert np.array_equal(ids, o.topk_f32(S, k))
+
+
 @pytest.mark.parametrize("nq,active,k", [(5, 70001, 64), (3, 70003, 700), (3, 100002, 5000),
                                          (2, 16384, 1000), (2, 16383, 1000), (3, 8192, 700), (3, 8191, 700),
                                          (3, 50001, 600), (2, 49153, 3000),
