@@ -247,6 +247,16 @@ __device__ __forceinline__ void tma_store_2d(const void *map, uint32_t src_smem,
                  "r"(src_smem), "r"(x), "r"(y)
                  : "memory");
 }
+// 2-D tiled bulk load global -> this CTA's shared memory through a tensor map
+// (x innermost; x times the element size a multiple of 16 bytes), completing
+// the box's bytes on `bar`. Rows past the tensor's extent arrive as zeros.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const void *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst_smem),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
 // Named barrier `id` over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -21,20 +21,22 @@
 //
 // GB300 mapping, one persistent CTA per SM, CTAs grouped by 128 queries:
 //  - MMA D[query][block] = A[query][d] . B[block][d], M = 128 queries,
-//    N = 64 blocks per tile, K = 16 per instruction.
+//    N = 128 blocks per tile, K = 16 per instruction (an N = 128 MMA does
+//    twice the work of an N = 64 one in about 1.45 times the cycles).
 //  - A: the group's head-summed queries, three slices resident in TMEM
 //    (192 of the 512 columns), written once by the epilogue warps.
-//  - B: key tiles. A producer warp streams raw key rows (contiguous, 16 KiB
-//    = 32 fp32 rows per copy) into a 4-slot shared-memory ring with bulk
-//    async copies; 8 converter warps split them into three 128-byte-swizzled
-//    K-major bf16 slices in a 3-stage ring (3 x 48 KiB).
+//  - B: key tiles in K-halves. A producer warp loads raw key pieces of
+//    64 rows x 64 d with 2-D tensor copies (16 KiB fp32) into a 6-slot
+//    ring; 5 converter warps split them into three 128-byte-swizzled
+//    K-major bf16 slices of a K-half stage (3 x 16 KiB), 2 stages in flight.
 //  - One thread issues tcgen05.mma into two accumulators (hi*hi;
-//    corrections) per tile, double-buffered (4 x 64 TMEM columns), and
-//    signals stages with tcgen05.commit. Its SM sub-partition holds no
-//    converter warp, so the 48 issues of a tile are not slowed by them.
-//  - 4 epilogue warps (thread = query row) read the accumulators, add them,
-//    and store the scores through a per-warp shared-memory transpose as
-//    coalesced 16-byte stores (two 256-byte row segments per instruction).
+//    corrections), 128 columns each, and frees each K-half stage and hands
+//    the finished tile to the epilogue with tcgen05.commit. Its SM
+//    sub-partition holds no converter warp.
+//  - 8 epilogue warps (two per TMEM lane quarter, one per column half;
+//    thread = query row) read both accumulators out at once, so the next
+//    tile's MMAs can start, add them, and store the scores by 2-D tensor
+//    stores (or coalesced direct stores when rows are not 16-byte aligned).
 //  - Key rows at or beyond `active` are never read; the grid comes from
 //    `active` and nq alone.
 // Every mbarrier wait is bounded; a timeout sets the error word.
@@ -50,48 +52,51 @@
 namespace qsa {
 namespace {
 
-constexpr int TILE_N = 64;                     // key blocks per tile (MMA N)
+constexpr int TILE_N = 128;                    // key blocks per tile (MMA N)
 constexpr int QGROUP = 128;                    // queries per CTA group (MMA M)
-constexpr int RAW_ROWS = 32;                   // key rows per raw copy
-constexpr int RAW_SLOTS = 3;
-constexpr int KS_STAGES = 3;                   // converted key tiles in flight
-constexpr int RAW_SLOT_BYTES = RAW_ROWS * D * 4;    // 16 KiB (fp32 rows)
-constexpr int KS_SUB_BYTES = TILE_N * 128;          // one slice, one K-half: 64 rows x 128 B
-constexpr int KS_STAGE_BYTES = 6 * KS_SUB_BYTES;    // 3 slices x 2 K-halves = 48 KiB
-constexpr int OUT_ROW_BYTES = TILE_N * 4 + 16;      // padded: conflict-free 16-byte stores
+constexpr int KHALF = D / 2;                   // d per K-half: one 128-byte row of bf16
+constexpr int PIECE_ROWS = 64;                 // key rows per raw piece (one K-half)
+constexpr int RAW_SLOTS = 6;
+constexpr int RAW_SLOT_BYTES = PIECE_ROWS * KHALF * 4;   // 16 KiB (fp32)
+constexpr int KS_STAGES = 2;                   // K-half key stages in flight
+constexpr int KS_SUB_BYTES = TILE_N * 128;     // one slice of one K-half: 128 rows x 128 B
+constexpr int KS_STAGE_BYTES = 3 * KS_SUB_BYTES;    // 48 KiB
 constexpr int OUT_BOX_COLS = 32;                   // tensor-store box: 32 scores (128 B) x 128 rows
 constexpr int OUT_BOX_BYTES = QGROUP * OUT_BOX_COLS * 4;   // 16 KiB, 128-byte swizzled
-constexpr int OUT_BYTES = (TILE_N / OUT_BOX_COLS) * OUT_BOX_BYTES;   // 32 KiB
-// Warp roles. Warp w runs on SM sub-partition w % 4. The MMA issuers (warps 1
-// and 13) share their sub-partition only with one epilogue warp (5) and one
-// warp that has no role (9), so nothing competes with the issue of
-// tcgen05.mma.
-constexpr int PRODUCER_WARP = 0, MMA_WARP = 1, MMA_WARP2 = 13;
-constexpr int EPI_WARP0 = 2, EPI_WARPS = 4;       // warps 2..5: TMEM lane quarters 2, 3, 0, 1
-constexpr int CONV_WARPS = 8;                     // warps 6, 7, 8, 10, 11, 12, 14, 15
+constexpr int OUT_BYTES = 2 * OUT_BOX_BYTES;               // one column half of a tile: 32 KiB
+constexpr int OUT_ROWS = 8;                                // direct stores: rows per warp transpose
+constexpr int OUT_ROW_BYTES = (TILE_N / 2) * 4 + 16;       // padded: conflict-free 16-byte stores
+// Warp roles. Warp w runs on SM sub-partition w % 4 and reads TMEM lanes
+// 32 (w % 4) .. +31. The MMA issuer (warp 1) shares its sub-partition with two
+// epilogue warps (5, 9) and one warp with no role (13), so no converter
+// competes with the issue of tcgen05.mma.
+constexpr int PRODUCER_WARP = 0, MMA_WARP = 1;
+constexpr int EPI_WARP0 = 2, EPI_WARPS = 8;       // warps 2..9: lane quarters 2, 3, 0, 1 twice
+constexpr int CONV_WARPS = 5;                     // warps 10, 11, 12, 14, 15
 constexpr int TC_THREADS = 16 * 32;
 constexpr int CONV_THREADS = CONV_WARPS * 32;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_COLS_PER_SLICE = D / 2;   // 64 columns: 128 bf16 packed in pairs
-constexpr uint32_t ACC_COL0 = 3 * A_COLS_PER_SLICE;   // 192: accumulators after the query slices
-constexpr uint32_t ACC_STAGE_COLS = 2 * TILE_N;       // hi*hi and corrections, 64 columns each
+constexpr uint32_t ACC0_COL = 3 * A_COLS_PER_SLICE;   // 192: hi*hi, 128 columns
+constexpr uint32_t ACC1_COL = ACC0_COL + TILE_N;      // 320: corrections, 128 columns
+static_assert(ACC1_COL + TILE_N <= TMEM_COLS, "accumulators fit TMEM");
 
 // Shared memory, from a 1,024-byte-aligned base.
-constexpr int KS_OFF = 0;                                   // 3 x 48 KiB
-constexpr int RAW_OFF = KS_OFF + KS_STAGES * KS_STAGE_BYTES;  // 3 x 16 KiB
+constexpr int KS_OFF = 0;                                   // 2 x 48 KiB
+constexpr int RAW_OFF = KS_OFF + KS_STAGES * KS_STAGE_BYTES;  // 6 x 16 KiB
 constexpr int OUT_OFF = RAW_OFF + RAW_SLOTS * RAW_SLOT_BYTES;   // 32 KiB, 1,024-byte aligned
 constexpr int BAR_OFF = OUT_OFF + OUT_BYTES;
 static_assert(OUT_OFF % 1024 == 0, "128-byte swizzled staging needs 1,024-byte alignment");
-static_assert(EPI_WARPS * 16 * OUT_ROW_BYTES <= OUT_BYTES, "direct-store staging fits");
+static_assert(EPI_WARPS * OUT_ROWS * OUT_ROW_BYTES <= OUT_BYTES, "direct-store staging fits");
 
 struct TcBarriers {
-    uint64_t raw_full[RAW_SLOTS];   // producer -> converters (bulk copy landed)
+    uint64_t raw_full[RAW_SLOTS];   // producer -> converters (tensor copy landed)
     uint64_t raw_empty[RAW_SLOTS];  // converters -> producer
     uint64_t ks_full[KS_STAGES];    // converters -> MMA: key slices written
     uint64_t ks_empty[KS_STAGES];   // MMA -> converters: key slices consumed
-    uint64_t acc_full[2];           // MMA -> epilogue
-    uint64_t acc_empty[2];          // epilogue -> MMA
+    uint64_t acc_full;              // MMA -> epilogue: the tile's accumulators are final
+    uint64_t acc_empty;             // epilogue -> MMA: accumulators read out
     uint64_t a_ready;               // query slices in TMEM
     uint64_t q_peer;                // CTA pairs: the peer's half of the query slices landed
     uint32_t tmem_base;
@@ -114,9 +119,9 @@ static_assert(3 * QS_SLICE_BYTES <= KS_STAGES * KS_STAGE_BYTES, "query staging f
 static_assert(TC_SMEM <= 232448, "shared memory per CTA");
 constexpr uint32_t QS_PEER_BYTES = 3u * (QGROUP / 2) * (D / 8) * 16u;   // the peer's 64 rows, 3 slices
 
-// Converter index of a warp (warps 9 and 13 have no role), or -1.
+// Converter index of a warp (warp 13 has no role), or -1.
 __device__ __forceinline__ int converter_index(int warp) {
-    return (warp < 6 || warp == 9 || warp == 13) ? -1 : warp - 6 - (warp > 9) - (warp > 13);
+    return (warp < 10 || warp == 13) ? -1 : warp - 10 - (warp > 13);
 }
 
 __device__ __forceinline__ uint32_t qs_off(int s, int r, int c) {
@@ -146,10 +151,10 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 
 template <bool kInt8>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    scores_tc_kernel(const float *__restrict__ q, const float *__restrict__ kblk,
-                     const int8_t *__restrict__ kq8, const __half *__restrict__ kscale, int nq, int active,
+    scores_tc_kernel(const float *__restrict__ q, const __half *__restrict__ kscale, int nq, int active,
                      int ntiles, int ctas_per_group, float *__restrict__ scores,
-                     const __grid_constant__ CUtensorMap out_map, int use_tma, int pair) {
+                     const __grid_constant__ CUtensorMap key_map, const __grid_constant__ CUtensorMap out_map,
+                     int use_tma, int pair) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -162,8 +167,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int q0 = group * QGROUP;
     const int qn = min(QGROUP, nq - q0);
     const int nlocal = j0 < ntiles ? (ntiles - 1 - j0) / ctas_per_group + 1 : 0;
-    constexpr int ROW_BYTES = kInt8 ? D : D * 4;
-    const char *keys = kInt8 ? reinterpret_cast<const char *>(kq8) : reinterpret_cast<const char *>(kblk);
+    constexpr uint32_t PIECE_BYTES = PIECE_ROWS * KHALF * (kInt8 ? 1 : 4);
     auto tile_b0 = [&](int li) { return (j0 + li * ctas_per_group) * TILE_N; };
 
     if (tid == 0) {
@@ -175,10 +179,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(&bars->ks_full[s], CONV_THREADS);
             mbar_init(&bars->ks_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars->acc_full[s], 1);
-            mbar_init(&bars->acc_empty[s], EPI_THREADS);
-        }
+        mbar_init(&bars->acc_full, 1);
+        mbar_init(&bars->acc_empty, EPI_THREADS);
         mbar_init(&bars->a_ready, EPI_THREADS);
         mbar_init(&bars->q_peer, 1);
         if (pair) mbar_arrive_expect_tx(&bars->q_peer, QS_PEER_BYTES);
@@ -256,73 +258,69 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
 
     if (warp == PRODUCER_WARP) {
-        // ---- raw key rows -> ring (bulk async copies) --------------------------
+        // ---- raw key pieces -> ring (2-D tensor copies) ------------------------
+        // Piece p: tile p / 4, K-half (p / 2) % 2, rows 64 * (p % 2) .. +63.
         if (lane == 0) {
-            const int npieces = 2 * nlocal;
+            const int npieces = 4 * nlocal;
             for (int p = 0; p < npieces; ++p) {
                 const int slot = p % RAW_SLOTS;
                 wait_or_flag(&bars->raw_empty[slot], ((p / RAW_SLOTS) & 1) ^ 1);
-                const int row0 = tile_b0(p >> 1) + (p & 1) * RAW_ROWS;
-                const int rows = min(RAW_ROWS, active - row0);
-                if (rows > 0) {
-                    const uint32_t bytes = static_cast<uint32_t>(rows * ROW_BYTES);
-                    mbar_arrive_expect_tx(&bars->raw_full[slot], bytes);
-                    bulk_g2s(smem_raw + pad + RAW_OFF + slot * RAW_SLOT_BYTES,
-                             keys + static_cast<size_t>(row0) * ROW_BYTES, bytes, &bars->raw_full[slot]);
+                const int row0 = tile_b0(p >> 2) + (p & 1) * PIECE_ROWS;
+                if (row0 < active) {
+                    mbar_arrive_expect_tx(&bars->raw_full[slot], PIECE_BYTES);
+                    tma_load_2d(base + RAW_OFF + slot * RAW_SLOT_BYTES, &key_map, ((p >> 1) & 1) * KHALF, row0,
+                                &bars->raw_full[slot]);
                 } else {
                     mbar_arrive(&bars->raw_full[slot]);
                 }
             }
         }
         __syncwarp();
-    } else if (warp == MMA_WARP || warp == MMA_WARP2) {
-        // ---- MMA issuers ---------------------------------------------------------
-        // Two threads take alternate tiles (each then owns one accumulator
-        // stage), so one issues while the other waits for its next tile's
-        // barriers and the tensor pipe never drains between tiles.
+    } else if (warp == MMA_WARP) {
+        // ---- MMA issuer ------------------------------------------------------------
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(QGROUP, TILE_N);
+            const uint32_t d0 = tmem + ACC0_COL, d1 = tmem + ACC1_COL;
             wait_or_flag(&bars->a_ready, 0);
             tc_fence_after_sync();
-            for (int li = (warp == MMA_WARP ? 0 : 1); li < nlocal; li += 2) {
-                const int st = li & 1, use = li >> 1;
-                const int ks = li % KS_STAGES, ks_use = li / KS_STAGES;
-                wait_or_flag(&bars->acc_empty[st], (use & 1) ^ 1);
-                wait_or_flag(&bars->ks_full[ks], ks_use & 1);
-                tc_fence_after_sync();
-                const uint32_t d0 = tmem + ACC_COL0 + st * ACC_STAGE_COLS, d1 = d0 + TILE_N;
-                const uint32_t kbase = base + KS_OFF + ks * KS_STAGE_BYTES;
-                // Fully unrolled: the 48 descriptors differ from the first by constants.
-                const uint64_t kdesc = sw128_kmajor_desc(kbase);
+            for (int li = 0; li < nlocal; ++li) {
+                wait_or_flag(&bars->acc_empty, (li & 1) ^ 1);
+                for (int kh = 0; kh < 2; ++kh) {
+                    const int t = 2 * li + kh, ks = t % KS_STAGES;
+                    wait_or_flag(&bars->ks_full[ks], (t / KS_STAGES) & 1);
+                    tc_fence_after_sync();
+                    // Slice s of this K-half at stage + s * KS_SUB_BYTES; +32 B per K-step.
+                    const uint64_t kdesc = sw128_kmajor_desc(base + KS_OFF + ks * KS_STAGE_BYTES);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    // key slice s, K-half h at kbase + (2*s + h) * KS_SUB_BYTES; +32 B per K-step
-                    const uint64_t B0 = kdesc + static_cast<uint64_t>(((kk >> 2) * KS_SUB_BYTES + (kk & 3) * 32) >> 4);
-                    const uint32_t A0 = tmem + kk * 8;
-                    const uint32_t acc = kk == 0 ? 0u : 1u;
-                    tc_mma_bf16_ta(d0, A0, B0, idesc, acc);                                   // hi . hi
-                    tc_mma_bf16_ta(d1, A0 + A_COLS_PER_SLICE, B0, idesc, acc);               // mid . hi
-                    tc_mma_bf16_ta(d1, A0 + 2 * A_COLS_PER_SLICE, B0, idesc, 1u);            // lo . hi
-                    if constexpr (!kInt8) {
-                        const uint64_t B1 = B0 + ((2 * KS_SUB_BYTES) >> 4), B2 = B0 + ((4 * KS_SUB_BYTES) >> 4);
-                        tc_mma_bf16_ta(d1, A0, B1, idesc, 1u);                                // hi . mid
-                        tc_mma_bf16_ta(d1, A0 + A_COLS_PER_SLICE, B1, idesc, 1u);           // mid . mid
-                        tc_mma_bf16_ta(d1, A0, B2, idesc, 1u);                                // hi . lo
+                    for (int kk = 0; kk < KHALF / 16; ++kk) {
+                        const uint64_t B0 = kdesc + static_cast<uint64_t>((kk * 32) >> 4);
+                        const uint32_t A0 = tmem + (4 * kh + kk) * 8;
+                        const uint32_t acc = (kh | kk) != 0 ? 1u : 0u;
+                        tc_mma_bf16_ta(d0, A0, B0, idesc, acc);                                   // hi . hi
+                        tc_mma_bf16_ta(d1, A0 + A_COLS_PER_SLICE, B0, idesc, acc);               // mid . hi
+                        tc_mma_bf16_ta(d1, A0 + 2 * A_COLS_PER_SLICE, B0, idesc, 1u);            // lo . hi
+                        if constexpr (!kInt8) {
+                            const uint64_t B1 = B0 + (KS_SUB_BYTES >> 4), B2 = B0 + ((2 * KS_SUB_BYTES) >> 4);
+                            tc_mma_bf16_ta(d1, A0, B1, idesc, 1u);                                // hi . mid
+                            tc_mma_bf16_ta(d1, A0 + A_COLS_PER_SLICE, B1, idesc, 1u);           // mid . mid
+                            tc_mma_bf16_ta(d1, A0, B2, idesc, 1u);                                // hi . lo
+                        }
                     }
+                    tc_commit(&bars->ks_empty[ks]);
                 }
-                tc_commit(&bars->ks_empty[ks]);
-                tc_commit(&bars->acc_full[st]);
+                tc_commit(&bars->acc_full);
             }
         }
         __syncwarp();
     } else if (warp < EPI_WARP0 + EPI_WARPS) {
         // ---- epilogue warps: query slices into TMEM, then scores out -------------
         const int quarter = warp & 3;                       // TMEM lanes 32*quarter .. +31
+        const int team = (warp - EPI_WARP0) >> 2;           // column half of a tile: 0 or 1
         const int row = 32 * quarter + lane;                // query row within the group
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
         if (pair) wait_or_flag(&bars->q_peer, 0);   // the peer's 64 rows have landed
-        // This warp's 32 query rows: staged slices -> TMEM (A operand).
-        for (int c = 0; c < D / 8; ++c) {
+        // This warp's 32 query rows, half of the 16-byte chunks: staged slices -> TMEM.
+        for (int c = 8 * team; c < 8 * team + 8; ++c) {
 #pragma unroll
             for (int sl = 0; sl < 3; ++sl) {
                 const uint4 v = ld_shared_v4(base + qs_off(sl, row, c));
@@ -333,84 +331,89 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_fence_before_sync();
         mbar_arrive(&bars->a_ready);   // the key stages may now be overwritten
 
-        // Scores leave by tensor store (use_tma: rows 16-byte aligned): the 128
-        // threads write the tile's 128 x 64 scores into two 128-byte-swizzled
-        // boxes of 32 columns, and one thread stores both asynchronously.
-        // Otherwise, through a per-warp shared-memory transpose, half a warp at
-        // a time: 16 threads write their query rows' 64 scores to padded staging
-        // rows, then the warp stores two rows per instruction.
+        // Scores leave by tensor store (use_tma: rows 16-byte aligned): each
+        // team writes its 128 x 64 half of the tile into two 128-byte-swizzled
+        // boxes of 32 columns, one team after the other through the same
+        // staging, and one thread stores the boxes asynchronously. Otherwise,
+        // through a per-warp shared-memory transpose, 8 rows at a time.
         const int epi_tid = tid - EPI_WARP0 * 32;
+        const int col0 = 64 * team;                         // first column of this thread's half
         const bool vec_ok = (active & 3) == 0;              // 16-byte aligned row segments
-        const uint32_t stage0 = base + OUT_OFF + quarter * 16 * OUT_ROW_BYTES;
-        const uint32_t my_stage = stage0 + (lane & 15) * OUT_ROW_BYTES;
-        const int pr = lane >> 4, pc = 4 * (lane & 15);    // row of a pair, first column
+        const uint32_t stage0 = base + OUT_OFF + (warp - EPI_WARP0) * OUT_ROWS * OUT_ROW_BYTES;
         for (int li = 0; li < nlocal; ++li) {
-            const int st = li & 1, use = li >> 1;
             const int b0 = tile_b0(li);
             const int nb = min(TILE_N, active - b0);
-            wait_or_flag(&bars->acc_full[st], use & 1);
+            wait_or_flag(&bars->acc_full, li & 1);
             tc_fence_after_sync();
-            const uint32_t t0 = lane_addr + ACC_COL0 + st * ACC_STAGE_COLS;
-            uint32_t x0[32], x1[32];
-            float v[TILE_N];
+            float v[TILE_N / 2];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                tmem_ld32(t0 + 32 * half, x0);
-                tmem_ld32(t0 + TILE_N + 32 * half, x1);
+                uint32_t x0[32], x1[32];
+                tmem_ld32(lane_addr + ACC0_COL + col0 + 32 * half, x0);
+                tmem_ld32(lane_addr + ACC1_COL + col0 + 32 * half, x1);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     v[32 * half + j] = __fadd_rn(__uint_as_float(x0[j]), __uint_as_float(x1[j]));
             }
             tc_fence_before_sync();
-            mbar_arrive(&bars->acc_empty[st]);              // TMEM free for the tile after next
+            mbar_arrive(&bars->acc_empty);                  // TMEM free for the next tile
             if constexpr (kInt8) {
 #pragma unroll
-                for (int j = 0; j < TILE_N; ++j)
-                    if (j < nb) v[j] = __fmul_rn(v[j], __half2float(kscale[b0 + j]));
+                for (int j = 0; j < TILE_N / 2; ++j)
+                    if (col0 + j < nb) v[j] = __fmul_rn(v[j], __half2float(kscale[b0 + col0 + j]));
             }
             if (use_tma) {
-                if (epi_tid == 0) bulk_wait_read0();        // the previous tile's stores have read the boxes
-                named_bar_sync(2, EPI_THREADS);
+#pragma unroll 1
+                for (int tm = 0; tm < 2; ++tm) {
+                    if (epi_tid == 0) bulk_wait_read0();    // earlier stores have read the staging
+                    named_bar_sync(2, EPI_THREADS);
+                    if (team == tm) {
 #pragma unroll
-                for (int j = 0; j < TILE_N / 4; ++j) {
-                    const int box = j >> 3, chunk = j & 7;
-                    st_shared_v4(base + OUT_OFF + box * OUT_BOX_BYTES + row * 128 + ((chunk ^ (row & 7)) << 4),
-                                 __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
-                                 __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
-                }
-                fence_proxy_async_smem();
-                named_bar_sync(2, EPI_THREADS);
-                if (epi_tid == 0) {
-                    tma_store_2d(&out_map, base + OUT_OFF, b0, q0);
-                    if (b0 + OUT_BOX_COLS < active) tma_store_2d(&out_map, base + OUT_OFF + OUT_BOX_BYTES, b0 + OUT_BOX_COLS, q0);
-                    bulk_commit();
+                        for (int j = 0; j < TILE_N / 8; ++j) {
+                            const int box = j >> 3, chunk = j & 7;
+                            st_shared_v4(base + OUT_OFF + box * OUT_BOX_BYTES + row * 128 + ((chunk ^ (row & 7)) << 4),
+                                         __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                         __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    named_bar_sync(2, EPI_THREADS);
+                    if (epi_tid == 0) {
+                        const int x0 = b0 + 64 * tm;
+                        if (x0 < active) tma_store_2d(&out_map, base + OUT_OFF, x0, q0);
+                        if (x0 + OUT_BOX_COLS < active)
+                            tma_store_2d(&out_map, base + OUT_OFF + OUT_BOX_BYTES, x0 + OUT_BOX_COLS, q0);
+                        bulk_commit();
+                    }
                 }
                 continue;
             }
+#pragma unroll 1
+            for (int h = 0; h < 4; ++h) {
+                if ((lane >> 3) == h) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if ((lane >> 4) == h) {
-#pragma unroll
-                    for (int j = 0; j < TILE_N; j += 4)
-                        st_shared_v4(my_stage + 4 * j, __float_as_uint(v[j]), __float_as_uint(v[j + 1]),
-                                     __float_as_uint(v[j + 2]), __float_as_uint(v[j + 3]));
+                    for (int j = 0; j < TILE_N / 2; j += 4)
+                        st_shared_v4(stage0 + (lane & 7) * OUT_ROW_BYTES + 4 * j, __float_as_uint(v[j]),
+                                     __float_as_uint(v[j + 1]), __float_as_uint(v[j + 2]), __float_as_uint(v[j + 3]));
                 }
                 __syncwarp();
-#pragma unroll 4
-                for (int i = 0; i < 8; ++i) {
-                    const int sr = 2 * i + pr;                   // staging row
-                    const int r = 32 * quarter + 16 * h + sr;    // query row within the group
-                    if (r < qn) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int id = 32 * i + lane;
+                    const int sr = id >> 4, pc = 4 * (id & 15);   // staging row, first column
+                    const int r = 32 * quarter + 8 * h + sr;      // query row within the group
+                    const int col = col0 + pc;
+                    if (r < qn && col < nb) {
                         const uint4 w4 = ld_shared_v4(stage0 + sr * OUT_ROW_BYTES + 4 * pc);
-                        float *dst = scores + static_cast<size_t>(q0 + r) * active + b0 + pc;
-                        if (vec_ok && pc + 4 <= nb) {
+                        float *dst = scores + static_cast<size_t>(q0 + r) * active + b0 + col;
+                        if (vec_ok && col + 4 <= nb) {
                             *reinterpret_cast<uint4 *>(dst) = w4;
                         } else {
                             const uint32_t e[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
-                                if (pc + c < nb) dst[c] = __uint_as_float(e[c]);
+                                if (col + c < nb) dst[c] = __uint_as_float(e[c]);
                         }
                     }
                 }
@@ -419,58 +422,77 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         if (epi_tid == 0) bulk_wait0();                     // stores complete before the CTA leaves
     } else if (converter_index(warp) >= 0) {
-        // ---- converters: raw rows -> swizzled bf16 key slices ------------------
-        // A warp converts whole rows: lane l takes d = 4l .. 4l+3 (one conflict-free
-        // 16-byte read per lane) and stores 8 bytes per slice into half of a
-        // swizzled 16-byte chunk (the two lanes of a chunk share a bank group).
+        // ---- converters: raw pieces -> swizzled bf16 key slices ----------------
+        // Half a warp converts one row of a piece (64 d of one key): lane l
+        // takes d = 4 (l % 16) .. +3 (one conflict-free 16-byte read) and
+        // stores 8 bytes per slice into half of a swizzled 16-byte chunk.
         const int cw = converter_index(warp);
-        const int khalf = lane >> 4, c = (lane >> 1) & 7, part = lane & 1;
+        const int sub = lane & 15, rsel = lane >> 4;
+        const int c = sub >> 1, part = sub & 1;
         wait_or_flag(&bars->a_ready, 0);   // query staging has left the key stages
-        int ks = 0, ks_use = 0;
-        for (int li = 0; li < nlocal; ++li) {
+        for (int t = 0; t < 2 * nlocal; ++t) {             // K-half stage t: tile t / 2, K-half t % 2
+            const int ks = t % KS_STAGES;
             const uint32_t kbase = base + KS_OFF + ks * KS_STAGE_BYTES;
-            wait_or_flag(&bars->ks_empty[ks], (ks_use & 1) ^ 1);
-            for (int half = 0; half < 2; ++half) {
-                const int p = 2 * li + half;
+            wait_or_flag(&bars->ks_empty[ks], ((t / KS_STAGES) & 1) ^ 1);
+            for (int rh = 0; rh < 2; ++rh) {
+                const int p = 2 * t + rh;
                 const int slot = p % RAW_SLOTS;
                 wait_or_flag(&bars->raw_full[slot], (p / RAW_SLOTS) & 1);
-                const int row0 = tile_b0(li) + half * RAW_ROWS;
+                const int row0 = tile_b0(t >> 1) + rh * PIECE_ROWS;
                 const uint32_t src = base + RAW_OFF + slot * RAW_SLOT_BYTES;
+                // A warp's row pairs are i = cw + CONV_WARPS j; all of its reads
+                // are issued before any conversion.
+                constexpr int NPAIR = PIECE_ROWS / 2;
+                constexpr int PER_WARP = (NPAIR + CONV_WARPS - 1) / CONV_WARPS;
+                if constexpr (!kInt8) {
+                    uint4 a[PER_WARP];
 #pragma unroll
-                for (int i = 0; i < RAW_ROWS / CONV_WARPS; ++i) {
-                    const int r = cw + CONV_WARPS * i;               // row in the piece
-                    const bool live = row0 + r < active;
-                    const uint32_t dst = kbase + khalf * KS_SUB_BYTES + swz(half * RAW_ROWS + r, c) + 8 * part;
-                    if constexpr (!kInt8) {
-                        uint4 a = make_uint4(0u, 0u, 0u, 0u);
-                        if (live) a = ld_shared_v4(src + r * (D * 4) + 16 * lane);
-                        const float x[4] = {__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
-                                            __uint_as_float(a.w)};
-                        uint32_t h[4], m[4], l[4];
+                    for (int j = 0; j < PER_WARP; ++j) {
+                        const int r = 2 * (cw + CONV_WARPS * j) + rsel;     // row in the piece
+                        a[j] = make_uint4(0u, 0u, 0u, 0u);
+                        if (r < PIECE_ROWS && row0 + r < active) a[j] = ld_shared_v4(src + r * (KHALF * 4) + 16 * sub);
+                    }
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) split3(x[e], h[e], m[e], l[e]);
-                        st_shared_v2(dst, pack2(h[0], h[1]), pack2(h[2], h[3]));
-                        st_shared_v2(dst + 2 * KS_SUB_BYTES, pack2(m[0], m[1]), pack2(m[2], m[3]));
-                        st_shared_v2(dst + 4 * KS_SUB_BYTES, pack2(l[0], l[1]), pack2(l[2], l[3]));
-                    } else {
-                        // 4 int8 keys: exact in bf16 (at most 7 significant bits).
-                        uint32_t w = 0u;
-                        if (live) w = ld_shared_u32(src + r * D + 4 * lane);
-                        uint32_t f[4];
+                    for (int j = 0; j < PER_WARP; ++j) {
+                        const int r = 2 * (cw + CONV_WARPS * j) + rsel;
+                        if (r < PIECE_ROWS) {
+                            const uint32_t dst = kbase + swz(rh * PIECE_ROWS + r, c) + 8 * part;
+                            const float x[4] = {__uint_as_float(a[j].x), __uint_as_float(a[j].y),
+                                                __uint_as_float(a[j].z), __uint_as_float(a[j].w)};
+                            uint32_t h[4], m[4], l[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            f[e] = __float_as_uint(static_cast<float>(static_cast<int8_t>((w >> (8 * e)) & 0xFFu)));
-                        st_shared_v2(dst, pack2(f[0], f[1]), pack2(f[2], f[3]));
+                            for (int e = 0; e < 4; ++e) split3(x[e], h[e], m[e], l[e]);
+                            st_shared_v2(dst, pack2(h[0], h[1]), pack2(h[2], h[3]));
+                            st_shared_v2(dst + KS_SUB_BYTES, pack2(m[0], m[1]), pack2(m[2], m[3]));
+                            st_shared_v2(dst + 2 * KS_SUB_BYTES, pack2(l[0], l[1]), pack2(l[2], l[3]));
+                        }
+                    }
+                } else {
+                    // 4 int8 keys per lane: exact in bf16 (at most 7 significant bits).
+                    uint32_t a[PER_WARP];
+#pragma unroll
+                    for (int j = 0; j < PER_WARP; ++j) {
+                        const int r = 2 * (cw + CONV_WARPS * j) + rsel;
+                        a[j] = 0u;
+                        if (r < PIECE_ROWS && row0 + r < active) a[j] = ld_shared_u32(src + r * KHALF + 4 * sub);
+                    }
+#pragma unroll
+                    for (int j = 0; j < PER_WARP; ++j) {
+                        const int r = 2 * (cw + CONV_WARPS * j) + rsel;
+                        if (r < PIECE_ROWS) {
+                            const uint32_t dst = kbase + swz(rh * PIECE_ROWS + r, c) + 8 * part;
+                            uint32_t f[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                f[e] = __float_as_uint(static_cast<float>(static_cast<int8_t>((a[j] >> (8 * e)) & 0xFFu)));
+                            st_shared_v2(dst, pack2(f[0], f[1]), pack2(f[2], f[3]));
+                        }
                     }
                 }
                 mbar_arrive(&bars->raw_empty[slot]);
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars->ks_full[ks]);
-            if (++ks == KS_STAGES) {
-                ks = 0;
-                ++ks_use;
-            }
         }
     }
 
@@ -510,6 +532,22 @@ bool encode_out_map(CUtensorMap *map, float *scores, int nq, int active) {
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, scores, dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map of the first `active` key rows ([active][128], fp32 or int8) for
+// raw pieces of 64 rows x 64 d, unswizzled; rows past `active` read as zeros.
+// The rows are 16-byte aligned (the boundary checks the pointer).
+bool encode_key_map(CUtensorMap *map, const void *keys, int active, bool int8) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(active)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * (int8 ? 1u : 4u)};
+    const cuuint32_t box[2] = {KHALF, PIECE_ROWS};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+               const_cast<void *>(keys), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -554,16 +592,19 @@ cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq
     attrs[1].val.clusterDim.z = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 2;
-    CUtensorMap out_map;
+    CUtensorMap out_map, key_map;
     memset(&out_map, 0, sizeof(out_map));
+    memset(&key_map, 0, sizeof(key_map));
     const int use_tma = encode_out_map(&out_map, scores, nq, active) ? 1 : 0;
-    if (kq8 != nullptr)
-        return cudaLaunchKernelEx(&cfg, scores_tc_kernel<true>, q, static_cast<const float *>(nullptr), kq8,
-                                  reinterpret_cast<const __half *>(kscale), nq, active, ntiles, per, scores,
-                                  out_map, use_tma, pair);
-    return cudaLaunchKernelEx(&cfg, scores_tc_kernel<false>, q, kblk, static_cast<const int8_t *>(nullptr),
-                              static_cast<const __half *>(nullptr), nq, active, ntiles, per, scores, out_map,
-                              use_tma, pair);
+    const bool int8 = kq8 != nullptr;
+    if (!encode_key_map(&key_map, int8 ? static_cast<const void *>(kq8) : static_cast<const void *>(kblk), active,
+                        int8))
+        return cudaErrorNotSupported;
+    if (int8)
+        return cudaLaunchKernelEx(&cfg, scores_tc_kernel<true>, q, reinterpret_cast<const __half *>(kscale), nq,
+                                  active, ntiles, per, scores, key_map, out_map, use_tma, pair);
+    return cudaLaunchKernelEx(&cfg, scores_tc_kernel<false>, q, static_cast<const __half *>(nullptr), nq, active,
+                              ntiles, per, scores, key_map, out_map, use_tma, pair);
 }
 
 cudaError_t tc_error_read_clear(uint32_t *word, cudaStream_t stream) {
