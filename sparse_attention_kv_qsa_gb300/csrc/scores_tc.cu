@@ -68,11 +68,11 @@ constexpr int OUT_ROWS = 8;                                // direct stores: row
 constexpr int OUT_ROW_BYTES = (TILE_N / 2) * 4 + 16;       // padded: conflict-free 16-byte stores
 // Warp roles. Warp w runs on SM sub-partition w % 4 and reads TMEM lanes
 // 32 (w % 4) .. +31. The MMA issuer (warp 1) shares its sub-partition with two
-// epilogue warps (5, 9) and one warp with no role (13), so no converter
-// competes with the issue of tcgen05.mma.
+// epilogue warps (5, 9) and one converter (13): at one MMA per ~70 cycles the
+// issuer needs few issue slots.
 constexpr int PRODUCER_WARP = 0, MMA_WARP = 1;
 constexpr int EPI_WARP0 = 2, EPI_WARPS = 8;       // warps 2..9: lane quarters 2, 3, 0, 1 twice
-constexpr int CONV_WARPS = 5;                     // warps 10, 11, 12, 14, 15
+constexpr int CONV_WARPS = 6;                     // warps 10..15
 constexpr int TC_THREADS = 16 * 32;
 constexpr int CONV_THREADS = CONV_WARPS * 32;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
@@ -95,8 +95,8 @@ struct TcBarriers {
     uint64_t raw_empty[RAW_SLOTS];  // converters -> producer
     uint64_t ks_full[KS_STAGES];    // converters -> MMA: key slices written
     uint64_t ks_empty[KS_STAGES];   // MMA -> converters: key slices consumed
-    uint64_t acc_full;              // MMA -> epilogue: the tile's accumulators are final
-    uint64_t acc_empty;             // epilogue -> MMA: accumulators read out
+    uint64_t acc_full[2];           // MMA -> epilogue: accumulator 0 (hi*hi) / 1 final for the tile
+    uint64_t acc_empty[2];          // epilogue -> MMA: accumulator 0 / 1 read out
     uint64_t a_ready;               // query slices in TMEM
     uint64_t q_peer;                // CTA pairs: the peer's half of the query slices landed
     uint32_t tmem_base;
@@ -119,10 +119,8 @@ static_assert(3 * QS_SLICE_BYTES <= KS_STAGES * KS_STAGE_BYTES, "query staging f
 static_assert(TC_SMEM <= 232448, "shared memory per CTA");
 constexpr uint32_t QS_PEER_BYTES = 3u * (QGROUP / 2) * (D / 8) * 16u;   // the peer's 64 rows, 3 slices
 
-// Converter index of a warp (warp 13 has no role), or -1.
-__device__ __forceinline__ int converter_index(int warp) {
-    return (warp < 10 || warp == 13) ? -1 : warp - 10 - (warp > 13);
-}
+// Converter index of a warp, or -1.
+__device__ __forceinline__ int converter_index(int warp) { return warp < 10 ? -1 : warp - 10; }
 
 __device__ __forceinline__ uint32_t qs_off(int s, int r, int c) {
     return QS_OFF + s * QS_SLICE_BYTES + r * 256 + ((c ^ (r & 15)) << 4);
@@ -179,8 +177,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(&bars->ks_full[s], CONV_THREADS);
             mbar_init(&bars->ks_empty[s], 1);
         }
-        mbar_init(&bars->acc_full, 1);
-        mbar_init(&bars->acc_empty, EPI_THREADS);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->acc_full[s], 1);
+            mbar_init(&bars->acc_empty[s], EPI_THREADS);
+        }
         mbar_init(&bars->a_ready, EPI_THREADS);
         mbar_init(&bars->q_peer, 1);
         if (pair) mbar_arrive_expect_tx(&bars->q_peer, QS_PEER_BYTES);
@@ -278,37 +278,49 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ---- MMA issuer ------------------------------------------------------------
+        // Per K-half: the 4 hi*hi MMAs, then the 20 corrections. In the second
+        // K-half the hi*hi MMAs come first and are committed on their own, so
+        // that accumulator is final (and drained) ~20 MMAs before the tile
+        // ends, and the next tile's hi*hi MMAs queue behind this tile's last
+        // ones while the corrections accumulator is read out.
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(QGROUP, TILE_N);
             const uint32_t d0 = tmem + ACC0_COL, d1 = tmem + ACC1_COL;
             wait_or_flag(&bars->a_ready, 0);
             tc_fence_after_sync();
             for (int li = 0; li < nlocal; ++li) {
-                wait_or_flag(&bars->acc_empty, (li & 1) ^ 1);
                 for (int kh = 0; kh < 2; ++kh) {
                     const int t = 2 * li + kh, ks = t % KS_STAGES;
                     wait_or_flag(&bars->ks_full[ks], (t / KS_STAGES) & 1);
+                    if (kh == 0) wait_or_flag(&bars->acc_empty[0], (li & 1) ^ 1);
                     tc_fence_after_sync();
                     // Slice s of this K-half at stage + s * KS_SUB_BYTES; +32 B per K-step.
                     const uint64_t kdesc = sw128_kmajor_desc(base + KS_OFF + ks * KS_STAGE_BYTES);
 #pragma unroll
+                    for (int kk = 0; kk < KHALF / 16; ++kk)   // hi . hi
+                        tc_mma_bf16_ta(d0, tmem + (4 * kh + kk) * 8, kdesc + static_cast<uint64_t>((kk * 32) >> 4),
+                                       idesc, (kh | kk) != 0 ? 1u : 0u);
+                    if (kh == 1) tc_commit(&bars->acc_full[0]);
+                    if (kh == 0) {
+                        wait_or_flag(&bars->acc_empty[1], (li & 1) ^ 1);
+                        tc_fence_after_sync();
+                    }
+#pragma unroll
                     for (int kk = 0; kk < KHALF / 16; ++kk) {
                         const uint64_t B0 = kdesc + static_cast<uint64_t>((kk * 32) >> 4);
                         const uint32_t A0 = tmem + (4 * kh + kk) * 8;
-                        const uint32_t acc = (kh | kk) != 0 ? 1u : 0u;
-                        tc_mma_bf16_ta(d0, A0, B0, idesc, acc);                                   // hi . hi
-                        tc_mma_bf16_ta(d1, A0 + A_COLS_PER_SLICE, B0, idesc, acc);               // mid . hi
-                        tc_mma_bf16_ta(d1, A0 + 2 * A_COLS_PER_SLICE, B0, idesc, 1u);            // lo . hi
+                        tc_mma_bf16_ta(d1, A0 + A_COLS_PER_SLICE, B0, idesc, (kh | kk) != 0 ? 1u : 0u);  // mid . hi
+                        tc_mma_bf16_ta(d1, A0 + 2 * A_COLS_PER_SLICE, B0, idesc, 1u);                 // lo . hi
                         if constexpr (!kInt8) {
                             const uint64_t B1 = B0 + (KS_SUB_BYTES >> 4), B2 = B0 + ((2 * KS_SUB_BYTES) >> 4);
-                            tc_mma_bf16_ta(d1, A0, B1, idesc, 1u);                                // hi . mid
-                            tc_mma_bf16_ta(d1, A0 + A_COLS_PER_SLICE, B1, idesc, 1u);           // mid . mid
-                            tc_mma_bf16_ta(d1, A0, B2, idesc, 1u);                                // hi . lo
+                            tc_mma_bf16_ta(d1, A0, B1, idesc, 1u);                                     // hi . mid
+                            tc_mma_bf16_ta(d1, A0 + A_COLS_PER_SLICE, B1, idesc, 1u);                // mid . mid
+                            tc_mma_bf16_ta(d1, A0, B2, idesc, 1u);                                     // hi . lo
                         }
                     }
                     tc_commit(&bars->ks_empty[ks]);
                 }
-                tc_commit(&bars->acc_full);
+                tc_commit(&bars->acc_full[1]);
             }
         }
         __syncwarp();
@@ -343,21 +355,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int li = 0; li < nlocal; ++li) {
             const int b0 = tile_b0(li);
             const int nb = min(TILE_N, active - b0);
-            wait_or_flag(&bars->acc_full, li & 1);
-            tc_fence_after_sync();
+            // hi*hi first (final early), then the corrections.
             float v[TILE_N / 2];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
+            wait_or_flag(&bars->acc_full[0], li & 1);
+            tc_fence_after_sync();
+            {
                 uint32_t x0[32], x1[32];
-                tmem_ld32(lane_addr + ACC0_COL + col0 + 32 * half, x0);
-                tmem_ld32(lane_addr + ACC1_COL + col0 + 32 * half, x1);
+                tmem_ld32(lane_addr + ACC0_COL + col0, x0);
+                tmem_ld32(lane_addr + ACC0_COL + col0 + 32, x1);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    v[32 * half + j] = __fadd_rn(__uint_as_float(x0[j]), __uint_as_float(x1[j]));
+                for (int j = 0; j < 32; ++j) {
+                    v[j] = __uint_as_float(x0[j]);
+                    v[32 + j] = __uint_as_float(x1[j]);
+                }
             }
             tc_fence_before_sync();
-            mbar_arrive(&bars->acc_empty);                  // TMEM free for the next tile
+            mbar_arrive(&bars->acc_empty[0]);
+            wait_or_flag(&bars->acc_full[1], li & 1);
+            tc_fence_after_sync();
+            {
+                uint32_t x0[32], x1[32];
+                tmem_ld32(lane_addr + ACC1_COL + col0, x0);
+                tmem_ld32(lane_addr + ACC1_COL + col0 + 32, x1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    v[j] = __fadd_rn(v[j], __uint_as_float(x0[j]));
+                    v[32 + j] = __fadd_rn(v[32 + j], __uint_as_float(x1[j]));
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&bars->acc_empty[1]);               // TMEM free for the next tile
             if constexpr (kInt8) {
 #pragma unroll
                 for (int j = 0; j < TILE_N / 2; ++j)
