@@ -1,8 +1,11 @@
 """Benchmark: QSA block scoring + exact top-k at 262,144 cells x 256 queries.
 
 One step = one pass of the whole selection path on resident inputs:
-qsa_block_scores (256 queries x 4 heads x D=128 against 65,536 active
-summary keys of a 65,538-block capacity) then qsa_block_topk (k=512). The
+qsa_block_scores_gmax (256 queries x 4 heads x D=128 against 65,536 active
+summary keys of a 65,538-block capacity; the scores plus each 32-block
+group's maximum) then qsa_block_topk_gmax (k=512), which gives the same ids
+as qsa_block_topk. ``--path plain`` times qsa_block_scores + qsa_block_topk
+instead; the other path is timed beside the headline (``other_path``). The
 inputs are the seeded synthetic full-capacity workload: q and keys
 Student-t(3) at unit variance.
 
@@ -290,6 +293,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--k", type=int, default=K)
     ap.add_argument("--scorer", default="default", choices=["default", "ffma"])
+    ap.add_argument("--path", default="gmax", choices=["gmax", "plain"],
+                    help="gmax: qsa_block_scores_gmax + qsa_block_topk_gmax (the group maxima let the "
+                         "top-k read only the groups that can hold its k); plain: qsa_block_scores + "
+                         "qsa_block_topk. Both give the same ids.")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -321,21 +328,44 @@ def main():
     q = torch.from_numpy(W.q).to(dev)
     kblk = torch.from_numpy(W.kblk).to(dev)
     scores = torch.empty((W.nq, W.active), dtype=torch.float32, device=dev)
+    gmax = torch.empty((W.nq, qsa.groups(W.active)), dtype=torch.int32, device=dev)
     ids = torch.empty((W.nq, W.k), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
 
+    path = "plain" if args.scorer == "ffma" else args.path
+    calls = {}
     if args.scorer == "ffma":
-        def score():
-            qsa.block_scores_ffma(q, W.active, kblk=kblk, out=scores)
+        calls["plain"] = (lambda: qsa.block_scores_ffma(q, W.active, kblk=kblk, out=scores),
+                          lambda: qsa.block_topk(scores, W.k, out=ids))
     else:
-        def score():
-            qsa.block_scores(q, kblk, W.active, out=scores)
+        calls["plain"] = (lambda: qsa.block_scores(q, kblk, W.active, out=scores),
+                          lambda: qsa.block_topk(scores, W.k, out=ids))
+        calls["gmax"] = (lambda: qsa.block_scores_gmax(q, kblk, W.active, out=scores, gmax_out=gmax),
+                         lambda: qsa.block_topk_gmax(scores, gmax, W.k, out=ids))
 
-    def topk():
-        qsa.block_topk(scores, W.k, out=ids)
+    def timed_steps(score, topk, n):
+        """n flushed steps. Even steps: one event pair around both calls (the
+        step time; the top-k may launch under the scorer's tail). Odd steps:
+        an extra event between the calls gives each kernel's duration."""
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        for i in range(n):
+            if not args.no_flush:
+                flush.fill_(float(i))
+            ev[i][0].record(stream)
+            score()
+            if i & 1 or n == 1:
+                ev[i][1].record(stream)
+            topk()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        split = [i for i in range(n) if i & 1 or n == 1]
+        whole = [i for i in range(n) if not i & 1]
+        return ([ev[i][0].elapsed_time(ev[i][1]) for i in split], [ev[i][1].elapsed_time(ev[i][2]) for i in split],
+                [ev[i][0].elapsed_time(ev[i][2]) for i in whole], len(split))
 
+    score, topk = calls[path]
     for i in range(args.warmup):
         if not args.no_flush:
             flush.fill_(float(i))
@@ -344,34 +374,30 @@ def main():
     torch.cuda.synchronize()
 
     K_ = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_)]
     sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
     if sampler:
         sampler.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    # Even steps: one event pair around both calls (the step time; the top-k
-    # may launch under the scorer's tail). Odd steps: an extra event between
-    # the calls gives each kernel's duration (the roofline's denominator).
-    for i in range(K_):
-        if not args.no_flush:
-            flush.fill_(float(i))
-        ev[i][0].record(stream)
-        score()
-        if i & 1 or K_ == 1:
-            ev[i][1].record(stream)
-        topk()
-        ev[i][2].record(stream)
-    torch.cuda.synchronize()
+    t_score, t_topk, t_step, n_split = timed_steps(score, topk, K_)
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
-    split = [i for i in range(K_) if i & 1 or K_ == 1]
-    whole = [i for i in range(K_) if not i & 1]
-    t_score = [ev[i][0].elapsed_time(ev[i][1]) for i in split]
-    t_topk = [ev[i][1].elapsed_time(ev[i][2]) for i in split]
-    t_step = [ev[i][0].elapsed_time(ev[i][2]) for i in whole]
+    ids_headline = ids.clone()
+    other = None
+    if len(calls) > 1:
+        # The other path, for comparison (same ids), outside the timed region.
+        o_score, o_topk = calls["plain" if path == "gmax" else "gmax"]
+        for i in range(args.warmup):
+            o_score()
+            o_topk()
+        n_o = min(K_, 400)
+        os_, ot_, ostep, _ = timed_steps(o_score, o_topk, n_o)
+        assert torch.equal(ids, ids_headline), "the two paths disagree"
+        other = {"path": "plain" if path == "gmax" else "gmax", "steps": n_o,
+                 "step_us": 1e3 * statistics.mean(ostep), "scores_us": 1e3 * statistics.mean(os_),
+                 "topk_us": 1e3 * statistics.mean(ot_)}
     step_ms_local = statistics.mean(t_step)
     step_ms = max_over_ranks(step_ms_local, world, dev)
     if qsa.device_error(dev) != 0:
@@ -415,12 +441,14 @@ def main():
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "nq": W.nq, "active_blocks": W.active, "max_blocks": W.max_blocks,
                    "k": W.k, "scorer": scorer_kernel,
+                   "path": ("qsa_block_scores_gmax + qsa_block_topk_gmax" if path == "gmax"
+                            else "qsa_block_scores + qsa_block_topk"),
                    "l2": "warm (no flush)" if args.no_flush else
                          f"flushed before every step by a {2 * l2 >> 20} MiB write, flush untimed",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kernels_us": {"scores": score_us, "topk": topk_us,
                        "scores_p50": 1e3 * statistics.median(t_score), "topk_p50": 1e3 * statistics.median(t_topk),
-                       "steps_timed_split": len(split)},
+                       "steps_timed_split": n_split},
         "step_us": {"mean": 1e3 * step_ms_local, "p10": 1e3 * pct(t_step, 10), "p50": 1e3 * pct(t_step, 50),
                     "p90": 1e3 * pct(t_step, 90), "steps": len(t_step)},
         "roofline": roof,
@@ -428,6 +456,7 @@ def main():
                           "note": "algorithmic step bytes at the HBM peak (the step's binding roof when "
                                   "scoring runs on tensor cores)"},
         "gpu_launches": 2 * K_,
+        "other_path": other,
         "clocks": clocks,
         "pages_context": {"r9700_score_plus_topk_ms": 2.8, "r9700_qblocks_per_s": 6.0e9,
                           "note": "AMD R9700 (gfx1201) numbers from the pages; context only"},
@@ -461,8 +490,15 @@ def main():
                     k_d[b][:W.active].copy_(k_h, non_blocking=True)
                     copied[i].record(copy_stream)
                 stream.wait_event(copied[i])
-                s = qsa.block_scores(q_d[b], k_d[b], W.active, out=scores)
-                qsa.block_topk(s, W.k, out=ids_d[b])
+                if path == "gmax":
+                    qsa.block_scores_gmax(q_d[b], k_d[b], W.active, out=scores, gmax_out=gmax)
+                    qsa.block_topk_gmax(scores, gmax, W.k, out=ids_d[b])
+                elif args.scorer == "ffma":
+                    qsa.block_scores_ffma(q_d[b], W.active, kblk=k_d[b], out=scores)
+                    qsa.block_topk(scores, W.k, out=ids_d[b])
+                else:
+                    qsa.block_scores(q_d[b], k_d[b], W.active, out=scores)
+                    qsa.block_topk(scores, W.k, out=ids_d[b])
                 ids_h[b].copy_(ids_d[b], non_blocking=True)
                 done[i].record(stream)
 
@@ -475,7 +511,7 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e, world, dev)
-        assert np.array_equal(ids_h[(n_e - 1) & 1].numpy(), ids.cpu().numpy())
+        assert np.array_equal(ids_h[(n_e - 1) & 1].numpy(), ids_headline.cpu().numpy())
         line["e2e"] = {"value": world * units_per_step / (e_ms * 1e-3), "unit": UNIT, "ms_per_step": e_ms,
                        "steps": n_e, "h2d_bytes_per_step": q_h.numel() * 4 + k_h.numel() * 4,
                        "d2h_bytes_per_step": ids_h[0].numel() * 4,

@@ -113,6 +113,51 @@ qsa_status qsa_block_scores_ffma(const float *q, const float *kblk, const int8_t
 qsa_status qsa_block_topk(const float *scores, int nq, int active_blocks, int k, int32_t *ids,
                           cudaStream_t stream);
 
+/* Blocks per group of the group-maximum side output (below). */
+#define QSA_GROUP_BLOCKS 32
+
+/*
+ * Block scores plus their group maxima, for qsa_block_topk_gmax.
+ * group_max  uint32 [nq][ceil(active_blocks / 32)], written: element [i][g]
+ *            is key(max of scores[i][32 g .. 32 g + 31]) over the blocks
+ *            < active_blocks, where key(x) is the order-preserving radix key
+ *            of the top-k (-0 counted as +0 and NaN as -inf, then the bits
+ *            of a negative x inverted and the sign bit of a positive x set),
+ *            so a larger score has a larger unsigned key.
+ * 16-byte aligned. Other arguments, layouts and accuracy as qsa_block_scores
+ * (the scores are the same bits); the maxima add 1/32 of the score bytes.
+ */
+qsa_status qsa_block_scores_gmax(const float *q, const float *kblk, int nq, int max_blocks,
+                                 int active_blocks, float *scores, uint32_t *group_max,
+                                 cudaStream_t stream);
+
+/* The int8-key form of qsa_block_scores_gmax (arguments as qsa_block_scores_q8). */
+qsa_status qsa_block_scores_q8_gmax(const float *q, const int8_t *kblk_q8, const uint16_t *kscale_f16,
+                                    int nq, int max_blocks, int active_blocks, float *scores,
+                                    uint32_t *group_max, cudaStream_t stream);
+
+/*
+ * Group maxima of given packed scores (the group_max of
+ * qsa_block_scores_gmax, for scores that come from elsewhere).
+ * scores     fp32   [nq][active_blocks]
+ * group_max  uint32 [nq][ceil(active_blocks / 32)], written (16-byte aligned).
+ */
+qsa_status qsa_block_group_max(const float *scores, int nq, int active_blocks, uint32_t *group_max,
+                               cudaStream_t stream);
+
+/*
+ * qsa_block_topk with the group maxima of the same scores (as written by
+ * qsa_block_scores_gmax or qsa_block_scores_q8_gmax; 16-byte aligned). The
+ * result is identical to qsa_block_topk's. The maxima fix a threshold that
+ * at least k groups, hence at least k scores, reach, so a row reads only the
+ * groups at or above it; rows where that does not pay (k above half the
+ * group count, a threshold list past capacity) take qsa_block_topk's path.
+ * group_max that does not match `scores` gives undefined ids (never an
+ * out-of-bounds access).
+ */
+qsa_status qsa_block_topk_gmax(const float *scores, const uint32_t *group_max, int nq, int active_blocks,
+                               int k, int32_t *ids, cudaStream_t stream);
+
 /*
  * Reads and clears the current device's error word: nonzero when a kernel
  * of this library gave up a bounded wait (its outputs are then invalid).

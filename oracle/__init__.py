@@ -104,6 +104,26 @@ class Oracle:
         self.lib.qsa_oracle_topk_f32(scores.ctypes.data, nq, active, k, ids.ctypes.data, nthreads)
         return ids
 
+    @staticmethod
+    def score_keys(scores: np.ndarray) -> np.ndarray:
+        """The order-preserving uint32 key of each fp32 score, as the
+        boundary's header defines it: -0 counts as +0 and NaN as -inf, then a
+        negative value's bits are inverted and a positive value gets the sign
+        bit set."""
+        x = np.ascontiguousarray(scores, dtype=np.float32)
+        x = np.where(np.isnan(x), np.float32(-np.inf), x) + np.float32(0.0)
+        bits = x.view(np.uint32)
+        return np.where(bits >> np.uint32(31) != 0, ~bits, bits | np.uint32(0x80000000)).astype(np.uint32)
+
+    @classmethod
+    def group_max_keys(cls, scores: np.ndarray, group: int = 32) -> np.ndarray:
+        """Per row, the key of the largest score of each run of ``group``
+        consecutive blocks (the last run may be shorter): ``[nq, ceil(active /
+        group)]`` uint32."""
+        keys = cls.score_keys(scores)
+        starts = np.arange(0, keys.shape[1], group)
+        return np.maximum.reduceat(keys, starts, axis=1).astype(np.uint32)
+
     def select(self, q, kblk, active: int, k: int, nthreads: int = 0):
         """Scores then ids: ``(S[nq, active] fp64, ids[nq, k])``."""
         S = self.scores(q, kblk, active, nthreads)

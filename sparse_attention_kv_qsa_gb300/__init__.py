@@ -7,11 +7,16 @@ the seeded synthetic input generator.
 
 from .qsa import (  # noqa: F401
     QSAError,
+    block_group_max,
     block_scores,
     block_scores_ffma,
+    block_scores_gmax,
     block_scores_q8,
+    block_scores_q8_gmax,
     block_select,
     block_topk,
+    block_topk_gmax,
+    groups,
     default_scorer_kernel,
     device_error,
 )

@@ -45,29 +45,73 @@ qsa_status check_score_args(const float *q, int nq, int max_blocks, int active_b
     return QSA_OK;
 }
 
+// Scores (and, when gmax is given, group maxima) through the kernel for nq.
+qsa_status run_scores(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale, int nq,
+                      int active, float *scores, uint32_t *gmax, cudaStream_t stream) {
+    if (nq <= qsa::SMALL_NQ_MAX) {
+        cudaError_t e = qsa::launch_scores_rows(q, kblk, kq8, kscale, nq, active, scores, stream);
+        if (e == cudaSuccess && gmax != nullptr) e = qsa::launch_group_max(scores, nq, active, gmax, stream);
+        return from_cuda(e);
+    }
+    return from_cuda(qsa::launch_scores_tc(q, kblk, kq8, kscale, nq, active, scores, gmax, stream));
+}
+
+qsa_status scores_f32(const float *q, const float *kblk, int nq, int max_blocks, int active_blocks, float *scores,
+                      uint32_t *gmax, bool want_gmax, cudaStream_t stream) {
+    qsa_status s = check_score_args(q, nq, max_blocks, active_blocks, scores);
+    if (s != QSA_OK || nq == 0 || active_blocks == 0) return s;
+    if (kblk == nullptr || !aligned16(kblk)) return QSA_ERR_INVALID;
+    if (want_gmax && (gmax == nullptr || !aligned16(gmax))) return QSA_ERR_INVALID;
+    return run_scores(q, kblk, nullptr, nullptr, nq, active_blocks, scores, gmax, stream);
+}
+
+qsa_status scores_q8(const float *q, const int8_t *kblk_q8, const uint16_t *kscale_f16, int nq, int max_blocks,
+                     int active_blocks, float *scores, uint32_t *gmax, bool want_gmax, cudaStream_t stream) {
+    qsa_status s = check_score_args(q, nq, max_blocks, active_blocks, scores);
+    if (s != QSA_OK || nq == 0 || active_blocks == 0) return s;
+    if (kblk_q8 == nullptr || kscale_f16 == nullptr || !aligned16(kblk_q8)) return QSA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(kscale_f16) & 1u) != 0) return QSA_ERR_INVALID;
+    if (want_gmax && (gmax == nullptr || !aligned16(gmax))) return QSA_ERR_INVALID;
+    return run_scores(q, nullptr, kblk_q8, kscale_f16, nq, active_blocks, scores, gmax, stream);
+}
+
+qsa_status topk(const float *scores, const uint32_t *gmax, bool want_gmax, int nq, int active_blocks, int k,
+                int32_t *ids, cudaStream_t stream) {
+    if (nq < 0 || active_blocks < 0 || k < 1) return QSA_ERR_INVALID;
+    if (nq == 0) return QSA_OK;
+    if (ids == nullptr || !aligned16(ids)) return QSA_ERR_INVALID;
+    if (active_blocks > QSA_TOPK_MAX_ACTIVE) return QSA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(nq) * k > (1LL << 40)) return QSA_ERR_UNSUPPORTED;
+    if (k >= active_blocks) return from_cuda(qsa::launch_topk_all(nq, active_blocks, k, ids, stream));
+    if (scores == nullptr || !aligned16(scores)) return QSA_ERR_INVALID;
+    if (want_gmax && (gmax == nullptr || !aligned16(gmax))) return QSA_ERR_INVALID;
+    if (static_cast<long long>(nq) * 8 > 0x7FFFFFFFLL) return QSA_ERR_UNSUPPORTED;
+    return from_cuda(qsa::launch_topk(scores, gmax, nq, active_blocks, k, ids, stream));
+}
+
 }  // namespace
 
 extern "C" {
 
 qsa_status qsa_block_scores(const float *q, const float *kblk, int nq, int max_blocks, int active_blocks,
                             float *scores, cudaStream_t stream) {
-    qsa_status s = check_score_args(q, nq, max_blocks, active_blocks, scores);
-    if (s != QSA_OK || nq == 0 || active_blocks == 0) return s;
-    if (kblk == nullptr || !aligned16(kblk)) return QSA_ERR_INVALID;
-    if (nq <= qsa::SMALL_NQ_MAX)
-        return from_cuda(qsa::launch_scores_rows(q, kblk, nullptr, nullptr, nq, active_blocks, scores, stream));
-    return from_cuda(qsa::launch_scores_tc(q, kblk, nullptr, nullptr, nq, active_blocks, scores, stream));
+    return scores_f32(q, kblk, nq, max_blocks, active_blocks, scores, nullptr, false, stream);
+}
+
+qsa_status qsa_block_scores_gmax(const float *q, const float *kblk, int nq, int max_blocks, int active_blocks,
+                                 float *scores, uint32_t *group_max, cudaStream_t stream) {
+    return scores_f32(q, kblk, nq, max_blocks, active_blocks, scores, group_max, true, stream);
 }
 
 qsa_status qsa_block_scores_q8(const float *q, const int8_t *kblk_q8, const uint16_t *kscale_f16, int nq,
                                int max_blocks, int active_blocks, float *scores, cudaStream_t stream) {
-    qsa_status s = check_score_args(q, nq, max_blocks, active_blocks, scores);
-    if (s != QSA_OK || nq == 0 || active_blocks == 0) return s;
-    if (kblk_q8 == nullptr || kscale_f16 == nullptr || !aligned16(kblk_q8)) return QSA_ERR_INVALID;
-    if ((reinterpret_cast<uintptr_t>(kscale_f16) & 1u) != 0) return QSA_ERR_INVALID;
-    if (nq <= qsa::SMALL_NQ_MAX)
-        return from_cuda(qsa::launch_scores_rows(q, nullptr, kblk_q8, kscale_f16, nq, active_blocks, scores, stream));
-    return from_cuda(qsa::launch_scores_tc(q, nullptr, kblk_q8, kscale_f16, nq, active_blocks, scores, stream));
+    return scores_q8(q, kblk_q8, kscale_f16, nq, max_blocks, active_blocks, scores, nullptr, false, stream);
+}
+
+qsa_status qsa_block_scores_q8_gmax(const float *q, const int8_t *kblk_q8, const uint16_t *kscale_f16, int nq,
+                                    int max_blocks, int active_blocks, float *scores, uint32_t *group_max,
+                                    cudaStream_t stream) {
+    return scores_q8(q, kblk_q8, kscale_f16, nq, max_blocks, active_blocks, scores, group_max, true, stream);
 }
 
 qsa_status qsa_block_scores_ffma(const float *q, const float *kblk, const int8_t *kblk_q8,
@@ -88,15 +132,21 @@ qsa_status qsa_block_scores_ffma(const float *q, const float *kblk, const int8_t
 
 qsa_status qsa_block_topk(const float *scores, int nq, int active_blocks, int k, int32_t *ids,
                           cudaStream_t stream) {
-    if (nq < 0 || active_blocks < 0 || k < 1) return QSA_ERR_INVALID;
-    if (nq == 0) return QSA_OK;
-    if (ids == nullptr || !aligned16(ids)) return QSA_ERR_INVALID;
-    if (active_blocks > QSA_TOPK_MAX_ACTIVE) return QSA_ERR_UNSUPPORTED;
-    if (static_cast<long long>(nq) * k > (1LL << 40)) return QSA_ERR_UNSUPPORTED;
-    if (k >= active_blocks) return from_cuda(qsa::launch_topk_all(nq, active_blocks, k, ids, stream));
-    if (scores == nullptr || !aligned16(scores)) return QSA_ERR_INVALID;
-    if (static_cast<long long>(nq) * 8 > 0x7FFFFFFFLL) return QSA_ERR_UNSUPPORTED;
-    return from_cuda(qsa::launch_topk(scores, nq, active_blocks, k, ids, stream));
+    return topk(scores, nullptr, false, nq, active_blocks, k, ids, stream);
+}
+
+qsa_status qsa_block_group_max(const float *scores, int nq, int active_blocks, uint32_t *group_max,
+                               cudaStream_t stream) {
+    if (nq < 0 || active_blocks < 0) return QSA_ERR_INVALID;
+    if (nq == 0 || active_blocks == 0) return QSA_OK;
+    if (scores == nullptr || group_max == nullptr || !aligned16(scores) || !aligned16(group_max))
+        return QSA_ERR_INVALID;
+    return from_cuda(qsa::launch_group_max(scores, nq, active_blocks, group_max, stream));
+}
+
+qsa_status qsa_block_topk_gmax(const float *scores, const uint32_t *group_max, int nq, int active_blocks, int k,
+                               int32_t *ids, cudaStream_t stream) {
+    return topk(scores, group_max, true, nq, active_blocks, k, ids, stream);
 }
 
 qsa_status qsa_get_device_error(uint32_t *code, cudaStream_t stream) {

@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI (qsa_api.cu) and the kernels.
 #pragma once
 
+#include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -8,6 +9,17 @@ namespace qsa {
 
 constexpr int D = 128;
 constexpr int HEADS = 4;
+// Consecutive blocks per group of the group-maximum side output.
+constexpr int GROUP_BLOCKS = 32;
+
+// Order-preserving radix key of a score: -0 becomes +0 (x + 0) and NaN
+// becomes -inf (max(., -inf)), then negatives are bit-inverted and positives
+// get the sign bit set, so a larger score has a larger unsigned key.
+__device__ __forceinline__ uint32_t score_key(float x) {
+    const float f = fmaxf(__fadd_rn(x, 0.0f), -INFINITY);
+    const uint32_t u = __float_as_uint(f);
+    return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
+}
 
 // Streaming multiprocessor count of the current device (cached per device).
 int device_sm_count();
@@ -18,9 +30,13 @@ cudaError_t launch_scores_ffma(const float *q, const float *kblk, const int8_t *
                                cudaStream_t stream);
 
 // Scores on the tensor cores (3-way bf16 split; int8 keys: one slice).
-// Exactly one of kblk / (kq8, kscale) is non-null.
+// Exactly one of kblk / (kq8, kscale) is non-null. gmax (may be null):
+// [nq][ceil(active / GROUP_BLOCKS)] keys of each group's largest score.
 cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,
-                             int nq, int active, float *scores, cudaStream_t stream);
+                             int nq, int active, float *scores, uint32_t *gmax, cudaStream_t stream);
+
+// gmax from packed scores (the decode scorer's companion).
+cudaError_t launch_group_max(const float *scores, int nq, int active, uint32_t *gmax, cudaStream_t stream);
 
 // Scores for nq <= 4 (decode) on CUDA cores, the grid spanning key rows.
 // Exactly one of kblk / (kq8, kscale) is non-null.
@@ -28,8 +44,10 @@ constexpr int SMALL_NQ_MAX = 4;
 cudaError_t launch_scores_rows(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,
                                int nq, int active, float *scores, cudaStream_t stream);
 
-// Exact top-k (k < active); one CTA per row.
-cudaError_t launch_topk(const float *scores, int nq, int active, int k, int32_t *ids,
+// Exact top-k (k < active); one CTA per row. gmax (may be null): the
+// group maxima of these scores, which let a row read only the groups that
+// can hold its top k.
+cudaError_t launch_topk(const float *scores, const uint32_t *gmax, int nq, int active, int k, int32_t *ids,
                         cudaStream_t stream);
 
 // ids[i][j] = j < active ? j : -1 (the k >= active case).

@@ -140,7 +140,43 @@ cudaError_t launch_rows(const float *q, const float *kblk, const int8_t *kq8, co
                               static_cast<const __half *>(nullptr), nq, active, scores);
 }
 
+// Group maxima of packed scores: one warp per 32-block group, lane j taking
+// block 32 g + j; the group's largest key is a warp max.
+__global__ void __launch_bounds__(ROWS_THREADS)
+    group_max_kernel(const float *__restrict__ scores, int nq, int active, int ngr, uint32_t *__restrict__ gmax) {
+    grid_dependency_wait();   // the scores come from the previous grid
+    grid_launch_dependents();
+    const long long w = (static_cast<long long>(blockIdx.x) * ROWS_THREADS + threadIdx.x) >> 5;   // warp-uniform
+    if (w >= static_cast<long long>(nq) * ngr) return;
+    const int lane = threadIdx.x & 31;
+    const int r = static_cast<int>(w / ngr), g = static_cast<int>(w % ngr);
+    const int b = g * GROUP_BLOCKS + lane;
+    uint32_t key = 0u;
+    if (b < active) key = score_key(__ldg(scores + static_cast<size_t>(r) * active + b));
+    key = __reduce_max_sync(FULL_MASK, key);
+    if (lane == 0) gmax[w] = key;
+}
+
 }  // namespace
+
+cudaError_t launch_group_max(const float *scores, int nq, int active, uint32_t *gmax, cudaStream_t stream) {
+    static_assert(GROUP_BLOCKS == 32, "one warp per group");
+    const int ngr = (active + GROUP_BLOCKS - 1) / GROUP_BLOCKS;
+    const long long threads = static_cast<long long>(nq) * ngr * 32;
+    const long long grid = (threads + ROWS_THREADS - 1) / ROWS_THREADS;
+    if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(ROWS_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, group_max_kernel, scores, nq, active, ngr, gmax);
+}
 
 cudaError_t launch_scores_rows(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,
                                int nq, int active, float *scores, cudaStream_t stream) {

@@ -150,7 +150,7 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 template <bool kInt8>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     scores_tc_kernel(const float *__restrict__ q, const __half *__restrict__ kscale, int nq, int active,
-                     int ntiles, int ctas_per_group, float *__restrict__ scores,
+                     int ntiles, int ctas_per_group, float *__restrict__ scores, uint32_t *__restrict__ gmax,
                      const __grid_constant__ CUtensorMap key_map, const __grid_constant__ CUtensorMap out_map,
                      int use_tma, int pair) {
     extern __shared__ uint8_t smem_raw[];
@@ -392,6 +392,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int j = 0; j < TILE_N / 2; ++j)
                     if (col0 + j < nb) v[j] = __fmul_rn(v[j], __half2float(kscale[b0 + col0 + j]));
             }
+            // Group maxima: this thread's 64 columns are two 32-block groups.
+            if (gmax != nullptr && row < qn) {
+                const int ngr = (active + GROUP_BLOCKS - 1) / GROUP_BLOCKS;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const int c0 = col0 + GROUP_BLOCKS * g;
+                    if (c0 < nb) {
+                        // fmaxf skips NaN (an all-NaN group stays NaN, whose key
+                        // is that of -inf) and the key maps -0 and +0 together,
+                        // so the key of the float maximum is the maximum key.
+                        float m = v[GROUP_BLOCKS * g];
+#pragma unroll
+                        for (int j = 1; j < GROUP_BLOCKS; ++j)
+                            if (c0 + j < nb) m = fmaxf(m, v[GROUP_BLOCKS * g + j]);
+                        gmax[static_cast<size_t>(q0 + row) * ngr + (b0 + c0) / GROUP_BLOCKS] = score_key(m);
+                    }
+                }
+            }
             if (use_tma) {
 #pragma unroll 1
                 for (int tm = 0; tm < 2; ++tm) {
@@ -583,7 +601,7 @@ bool encode_key_map(CUtensorMap *map, const void *keys, int active, bool int8) {
 }  // namespace
 
 cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale, int nq,
-                             int active, float *scores, cudaStream_t stream) {
+                             int active, float *scores, uint32_t *gmax, cudaStream_t stream) {
     static thread_local int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -631,9 +649,9 @@ cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq
         return cudaErrorNotSupported;
     if (int8)
         return cudaLaunchKernelEx(&cfg, scores_tc_kernel<true>, q, reinterpret_cast<const __half *>(kscale), nq,
-                                  active, ntiles, per, scores, key_map, out_map, use_tma, pair);
+                                  active, ntiles, per, scores, gmax, key_map, out_map, use_tma, pair);
     return cudaLaunchKernelEx(&cfg, scores_tc_kernel<false>, q, static_cast<const __half *>(nullptr), nq, active,
-                              ntiles, per, scores, key_map, out_map, use_tma, pair);
+                              ntiles, per, scores, gmax, key_map, out_map, use_tma, pair);
 }
 
 cudaError_t tc_error_read_clear(uint32_t *word, cudaStream_t stream) {

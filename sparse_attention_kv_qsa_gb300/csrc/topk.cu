@@ -52,6 +52,7 @@ constexpr int LIST_VEC = 8;              // 16-byte loads per thread per listing
 constexpr int CAND_MAX = 4096;           // candidate-list capacity
 constexpr int SAMPLE_STRIDE = 32;        // one 16-byte group of scores sampled per 512 bytes
 constexpr int SAMPLE_SHIFT = 18;         // sample bins: 2^18 keys = 1/32 octave; 256 bins span 8
+constexpr int GMAX_SUB_SHIFT = 10;       // group-maximum refinement: 2^10-key bins inside one of those
 constexpr int FAST_MIN_ACTIVE = 8192;    // shorter rows take the exact passes directly
 constexpr int MAX_ACTIVE = 393216;
 constexpr int SAMPLE_REGS = (MAX_ACTIVE / 4 / SAMPLE_STRIDE + ROW_THREADS - 1) / ROW_THREADS;
@@ -69,6 +70,7 @@ struct RowShared {
     alignas(16) uint32_t scan_tot[ROW_WARPS];
     uint32_t sel_bin, sel_above, sel_cnt;
     uint32_t cand_n;
+    uint32_t glist_n;  // groups listed from the group maxima (their ids in histA)
 };
 
 constexpr size_t SHARED_BYTES = (sizeof(RowShared) + 15) / 16 * 16;
@@ -207,7 +209,8 @@ __device__ __forceinline__ void stream_row(const uint32_t *g, int n, int head, i
 }
 
 __global__ void __launch_bounds__(ROW_THREADS, 2)
-    topk_row_kernel(const float *__restrict__ scores, int active, int k, int32_t *__restrict__ ids) {
+    topk_row_kernel(const float *__restrict__ scores, const uint32_t *__restrict__ gmax, int active, int k,
+                    int32_t *__restrict__ ids) {
     const size_t row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = active;
@@ -240,21 +243,46 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
     const uint32_t nsamp = 4u * static_cast<uint32_t>(nsv);
     const uint32_t r_target =
         static_cast<uint32_t>((9ull * static_cast<uint64_t>(k) * nsamp + 5ull * n - 1) / (5ull * n)) + 8u;
-    const bool try_list = n >= FAST_MIN_ACTIVE && r_target <= nsamp / 2;
+    // Group-maximum mode: with the maxima of the row's 32-block groups, the
+    // threshold comes from them instead of a sample, and the listing reads
+    // only the groups whose maximum reaches it (rows of at most 2,048 groups,
+    // k at most half of them).
+    const int ngr = (n + GROUP_BLOCKS - 1) / GROUP_BLOCKS;
+    const bool use_gmax = gmax != nullptr && 2 * k <= ngr && ngr <= 4 * ROW_THREADS;
+    const bool try_list = use_gmax || (n >= FAST_MIN_ACTIVE && r_target <= nsamp / 2);
 
     // The scores may come from the previous grid on the stream (launched as
     // its programmatic dependent); nothing global is read before this.
     grid_dependency_wait();
 
-    // The sample is requested before anything else.
+    // The sample (or this thread's 4 group maxima) is requested before anything else.
     uint4 sx[SAMPLE_REGS];
+    if (use_gmax) {
+        const uint32_t *gm = gmax + row * static_cast<size_t>(ngr);
+        sx[0] = make_uint4(0u, 0u, 0u, 0u);
+        if ((ngr & 3) == 0) {
+            if (4 * tid < ngr) sx[0] = __ldg(reinterpret_cast<const uint4 *>(gm) + tid);
+        } else {
+            if (4 * tid + 0 < ngr) sx[0].x = __ldg(gm + 4 * tid + 0);
+            if (4 * tid + 1 < ngr) sx[0].y = __ldg(gm + 4 * tid + 1);
+            if (4 * tid + 2 < ngr) sx[0].z = __ldg(gm + 4 * tid + 2);
+            if (4 * tid + 3 < ngr) sx[0].w = __ldg(gm + 4 * tid + 3);
+        }
 #pragma unroll
-    for (int u = 0; u < SAMPLE_REGS; ++u) {
-        const int s = tid + u * ROW_THREADS;
-        sx[u] = try_list && s < nsv ? __ldg(g4 + s * SAMPLE_STRIDE + SAMPLE_STRIDE / 2) : make_uint4(0u, 0u, 0u, 0u);
+        for (int u = 1; u < SAMPLE_REGS; ++u) sx[u] = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+#pragma unroll
+        for (int u = 0; u < SAMPLE_REGS; ++u) {
+            const int s = tid + u * ROW_THREADS;
+            sx[u] = try_list && s < nsv ? __ldg(g4 + s * SAMPLE_STRIDE + SAMPLE_STRIDE / 2)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+        }
     }
 
-    if (tid == 0) sh.cand_n = 0u;
+    if (tid == 0) {
+        sh.cand_n = 0u;
+        sh.glist_n = 0u;
+    }
     if (!try_list)
         for (int i = tid; i < HIST_A; i += ROW_THREADS) sh.histA[i] = 0u;   // the exact path's histogram
     for (int i = tid; i < BINS_R; i += ROW_THREADS) sh.histR[i] = 0u;
@@ -268,50 +296,97 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
     bool listed = false;
     uint32_t tg = 0u, kmax = 0u;
     if (try_list) {
-        // Sample threshold. The largest sample key smax tops a window of 256
-        // bins, each 2^18 keys wide (1/32 of an octave for normal floats),
-        // reaching 8 octaves below it. Counting the sample keys by their
-        // distance below smax spreads them over the bins (bins of fixed key
-        // digits crowd them into a few, which serialises the shared-memory
-        // atomics). tg is the lowest key of the bin where the count from the
-        // top reaches r, so at least r sample keys are >= tg. A sample whose
-        // r-th key lies below the window leaves tg = 0: the exact path.
-        uint32_t ks[SAMPLE_REGS][4];
-        uint32_t m = 0u;
+        const uint32_t gk[4] = {sx[0].x, sx[0].y, sx[0].z, sx[0].w};   // group-maximum mode's keys
+        if (use_gmax) {
+            // Group-maximum threshold: the distance-below-maximum bins of the
+            // sample (below), over the group maxima with target k, then once
+            // more with 2^10-key bins inside the bin found. tg is the lowest
+            // key of the finer bin where the count of groups from the top
+            // reaches k: at least k groups, hence at least k scores, are
+            // >= tg, and few groups beyond k are.
+            uint32_t m = 0u;
 #pragma unroll
-        for (int u = 0; u < SAMPLE_REGS; ++u) {
-            ks[u][0] = float_bits_to_key(sx[u].x);
-            ks[u][1] = float_bits_to_key(sx[u].y);
-            ks[u][2] = float_bits_to_key(sx[u].z);
-            ks[u][3] = float_bits_to_key(sx[u].w);
-            if (tid + u * ROW_THREADS < nsv) m = max(m, max(max(ks[u][0], ks[u][1]), max(ks[u][2], ks[u][3])));
-        }
-        m = __reduce_max_sync(FULL_MASK, m);
-        if (lane == 0) sh.scan_tot[warp] = m;
-        __syncthreads();
-        uint32_t smax = 0u;
+            for (int e = 0; e < 4; ++e)
+                if (4 * tid + e < ngr) m = max(m, gk[e]);
+            m = __reduce_max_sync(FULL_MASK, m);
+            if (lane == 0) sh.scan_tot[warp] = m;
+            __syncthreads();
+            uint32_t smax = 0u;
 #pragma unroll
-        for (int q = 0; q < ROW_WARPS / 4; ++q) {
-            const uint4 t = *reinterpret_cast<const uint4 *>(sh.scan_tot + 4 * q);
-            smax = max(max(smax, t.x), max(t.y, max(t.z, t.w)));
-        }
+            for (int q = 0; q < ROW_WARPS / 4; ++q) {
+                const uint4 t = *reinterpret_cast<const uint4 *>(sh.scan_tot + 4 * q);
+                smax = max(max(smax, t.x), max(t.y, max(t.z, t.w)));
+            }
 #pragma unroll
-        for (int u = 0; u < SAMPLE_REGS; ++u) {
-            if (tid + u * ROW_THREADS < nsv) {
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t d = smax - gk[e];
+                if (4 * tid + e < ngr && d < (static_cast<uint32_t>(BINS_R) << SAMPLE_SHIFT))
+                    atomicAdd(&sh.histR[BINS_R - 1 - (d >> SAMPLE_SHIFT)], 1u);
+            }
+            __syncthreads();
+            if (warp == 0) warp_select_256(sh.histR, kk, sh, lane);
+            __syncthreads();
+            if (sh.sel_cnt != 0u) {  // uniform; otherwise tg = 0: the exact path
+                const uint32_t b = static_cast<uint32_t>(BINS_R - 1) - sh.sel_bin;   // bins below smax
+                const uint32_t top = smax - (b << SAMPLE_SHIFT);                   // the bin's highest key
+                const uint32_t need = kk - sh.sel_above;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const uint32_t d = smax - ks[u][e];
-                    if (d < (static_cast<uint32_t>(BINS_R) << SAMPLE_SHIFT))
-                        atomicAdd(&sh.histR[BINS_R - 1 - (d >> SAMPLE_SHIFT)], 1u);
+                    if (4 * tid + e < ngr && ((smax - gk[e]) >> SAMPLE_SHIFT) == b)
+                        atomicAdd(&sh.histR[BINS_R - 1 - ((top - gk[e]) >> GMAX_SUB_SHIFT)], 1u);
+                }
+                __syncthreads();
+                if (warp == 0) warp_select_256(sh.histR, need, sh, lane);
+                __syncthreads();
+                const uint32_t below2 = (static_cast<uint32_t>(BINS_R) - sh.sel_bin) << GMAX_SUB_SHIFT;
+                tg = top >= below2 ? top - below2 + 1u : 0u;
+            }
+        } else {
+            // Sample threshold. The largest sample key smax tops a window of 256
+            // bins, each 2^18 keys wide (1/32 of an octave for normal floats),
+            // reaching 8 octaves below it. Counting the sample keys by their
+            // distance below smax spreads them over the bins (bins of fixed key
+            // digits crowd them into a few, which serialises the shared-memory
+            // atomics). tg is the lowest key of the bin where the count from the
+            // top reaches r, so at least r sample keys are >= tg. A sample whose
+            // r-th key lies below the window leaves tg = 0: the exact path.
+            uint32_t ks[SAMPLE_REGS][4];
+            uint32_t m = 0u;
+#pragma unroll
+            for (int u = 0; u < SAMPLE_REGS; ++u) {
+                ks[u][0] = float_bits_to_key(sx[u].x);
+                ks[u][1] = float_bits_to_key(sx[u].y);
+                ks[u][2] = float_bits_to_key(sx[u].z);
+                ks[u][3] = float_bits_to_key(sx[u].w);
+                if (tid + u * ROW_THREADS < nsv) m = max(m, max(max(ks[u][0], ks[u][1]), max(ks[u][2], ks[u][3])));
+            }
+            m = __reduce_max_sync(FULL_MASK, m);
+            if (lane == 0) sh.scan_tot[warp] = m;
+            __syncthreads();
+            uint32_t smax = 0u;
+#pragma unroll
+            for (int q = 0; q < ROW_WARPS / 4; ++q) {
+                const uint4 t = *reinterpret_cast<const uint4 *>(sh.scan_tot + 4 * q);
+                smax = max(max(smax, t.x), max(t.y, max(t.z, t.w)));
+            }
+#pragma unroll
+            for (int u = 0; u < SAMPLE_REGS; ++u) {
+                if (tid + u * ROW_THREADS < nsv) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t d = smax - ks[u][e];
+                        if (d < (static_cast<uint32_t>(BINS_R) << SAMPLE_SHIFT))
+                            atomicAdd(&sh.histR[BINS_R - 1 - (d >> SAMPLE_SHIFT)], 1u);
+                    }
                 }
             }
+            __syncthreads();
+            // A target past the window's count finds no bin (count 0).
+            if (warp == 0) warp_select_256(sh.histR, r_target, sh, lane);
+            __syncthreads();
+            const uint32_t below = (static_cast<uint32_t>(BINS_R) - sh.sel_bin) << SAMPLE_SHIFT;  // (b + 1) bins
+            tg = sh.sel_cnt != 0u && smax >= below ? smax - below + 1u : 0u;
         }
-        __syncthreads();
-        // A target past the window's count finds no bin (count 0).
-        if (warp == 0) warp_select_256(sh.histR, r_target, sh, lane);
-        __syncthreads();
-        const uint32_t below = (static_cast<uint32_t>(BINS_R) - sh.sel_bin) << SAMPLE_SHIFT;  // (b + 1) bins
-        tg = sh.sel_cnt != 0u && smax >= below ? smax - below + 1u : 0u;
 
         // Listing pass. key(x) >= tg is tested as the fp32 comparison x >= ft,
         // ft being the value whose key is tg: both orders agree on every x (NaN
@@ -327,44 +402,10 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         if (tg > NEG_INF_KEY) {
             const float ft = __uint_as_float(tg >= 0x80000000u ? (tg ^ 0x80000000u) : ~tg);
             const uint32_t key_base = smem_u32(sh.cand_key);
-            auto list_scalar = [&](int i) {
-                if (__uint_as_float(__ldg(g + i)) >= ft) {
-                    const uint32_t slot = atomicAdd(&sh.cand_n, 1u);
-                    if (slot < static_cast<uint32_t>(CAND_MAX)) {
-                        sh.cand_idx[slot] = static_cast<uint32_t>(i);
-                        cp_async_4(key_base + 4u * slot, g + i);
-                    }
-                }
-            };
-            for (int i = tid; i < head; i += ROW_THREADS) list_scalar(i);
-            for (int i = head + 4 * nvec + tid; i < n; i += ROW_THREADS) list_scalar(i);
-            // The next step's loads are issued as soon as this step's hit bits
-            // are taken, ahead of the slot bookkeeping.
-            uint4 x[LIST_VEC];
-            auto load_step = [&](int v0) {
-#pragma unroll
-                for (int u = 0; u < LIST_VEC; ++u) {
-                    const int v = v0 + u * ROW_THREADS + tid;
-                    // Past the end: NaN, which no comparison lists.
-                    x[u] = v < nvec ? __ldg(g4 + v) : make_uint4(QNAN_BITS, QNAN_BITS, QNAN_BITS, QNAN_BITS);
-                }
-            };
-            load_step(0);
-#pragma unroll 1
-            for (int v0 = 0; v0 < nvec; v0 += ROW_THREADS * LIST_VEC) {
-                // A list already past its capacity is abandoned (warp-uniform test).
-                if (__shfl_sync(FULL_MASK, *reinterpret_cast<volatile uint32_t *>(&sh.cand_n), 0) >
-                    static_cast<uint32_t>(CAND_MAX))
-                    break;
-                uint32_t hits = 0u;
-#pragma unroll
-                for (int u = 0; u < LIST_VEC; ++u) {
-                    hits |= static_cast<uint32_t>(__uint_as_float(x[u].x) >= ft) << (4 * u);
-                    hits |= static_cast<uint32_t>(__uint_as_float(x[u].y) >= ft) << (4 * u + 1);
-                    hits |= static_cast<uint32_t>(__uint_as_float(x[u].z) >= ft) << (4 * u + 2);
-                    hits |= static_cast<uint32_t>(__uint_as_float(x[u].w) >= ft) << (4 * u + 3);
-                }
-                if (v0 + ROW_THREADS * LIST_VEC < nvec) load_step(v0 + ROW_THREADS * LIST_VEC);
+            // Slots for one 32-score step's hits: bit j of `hits` is the score
+            // at index idx(j), which reaches its slot by an asynchronous 4-byte
+            // copy (the registers that held it are reused by then).
+            auto book = [&](uint32_t hits, auto idx) {
                 const uint32_t c = __popc(hits);
                 const uint32_t incl = warp_incl_scan(c, lane);
                 const uint32_t total = __shfl_sync(FULL_MASK, incl, 31);
@@ -372,17 +413,121 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
                     uint32_t base = 0u;
                     if (lane == 31) base = atomicAdd(&sh.cand_n, total);
                     uint32_t slot = __shfl_sync(FULL_MASK, base, 31) + incl - c;
-                    const int i0 = head + 4 * (v0 + tid);
                     while (hits != 0u) {
                         const int j = __ffs(hits) - 1;
                         hits &= hits - 1u;
                         if (slot < static_cast<uint32_t>(CAND_MAX)) {
-                            const int i = i0 + 4 * ROW_THREADS * (j >> 2) + (j & 3);
+                            const int i = idx(j);
                             sh.cand_idx[slot] = static_cast<uint32_t>(i);
                             cp_async_4(key_base + 4u * slot, g + i);
                         }
                         ++slot;
                     }
+                }
+            };
+            auto hit_bits = [&](const uint4 &y, int u) {
+                return static_cast<uint32_t>(__uint_as_float(y.x) >= ft) << (4 * u) |
+                       static_cast<uint32_t>(__uint_as_float(y.y) >= ft) << (4 * u + 1) |
+                       static_cast<uint32_t>(__uint_as_float(y.z) >= ft) << (4 * u + 2) |
+                       static_cast<uint32_t>(__uint_as_float(y.w) >= ft) << (4 * u + 3);
+            };
+            if (use_gmax) {
+                // The groups whose maximum reaches tg (every score >= tg lies in
+                // one) are compacted into histA, then each thread lists one
+                // group (32 scores, one 128-byte line) per round.
+                uint32_t mine = 0u;
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (4 * tid + e < ngr && gk[e] >= tg) mine |= 1u << e;
+                {
+                    const uint32_t c = __popc(mine);
+                    const uint32_t incl = warp_incl_scan(c, lane);
+                    const uint32_t total = __shfl_sync(FULL_MASK, incl, 31);
+                    uint32_t base = 0u;
+                    if (lane == 31 && total != 0u) base = atomicAdd(&sh.glist_n, total);
+                    uint32_t slot = __shfl_sync(FULL_MASK, base, 31) + incl - c;
+                    while (mine != 0u) {   // slot < ngr <= HIST_A
+                        const int e = __ffs(mine) - 1;
+                        mine &= mine - 1u;
+                        sh.histA[slot++] = static_cast<uint32_t>(4 * tid + e);
+                    }
+                }
+                __syncthreads();
+                // A warp lists 4 groups per load instruction: lane l reads the
+                // 16-byte piece l % 8 of group l / 8, so each instruction
+                // touches 4 whole 128-byte lines; GU instructions per round.
+                constexpr int GU = 8;
+                const int ngl = static_cast<int>(sh.glist_n);
+                const bool vec = (n & 3) == 0;   // every group starts 16-byte aligned
+                const int piece = lane & 7;
+#pragma unroll 1
+                for (int r0 = 4 * GU * warp; r0 < ngl; r0 += 4 * GU * ROW_WARPS) {   // warp-uniform
+                    int base[GU];                  // index of this lane's first score in each group
+                    uint32_t hits = 0u;
+#pragma unroll
+                    for (int u = 0; u < GU; ++u) {
+                        const int j = r0 + 4 * u + (lane >> 3);
+                        base[u] = j < ngl ? static_cast<int>(sh.histA[j]) * GROUP_BLOCKS + 4 * piece : n;
+                    }
+                    if (vec) {
+                        uint4 y[GU];
+#pragma unroll
+                        for (int u = 0; u < GU; ++u)
+                            y[u] = base[u] + 4 <= n ? __ldg(reinterpret_cast<const uint4 *>(g + base[u]))
+                                                    : make_uint4(QNAN_BITS, QNAN_BITS, QNAN_BITS, QNAN_BITS);
+#pragma unroll
+                        for (int u = 0; u < GU; ++u) hits |= hit_bits(y[u], u);
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < GU; ++u) {
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                if (base[u] + c < n && __uint_as_float(__ldg(g + base[u] + c)) >= ft)
+                                    hits |= 1u << (4 * u + c);
+                        }
+                    }
+                    // A hit's group is read again from the list (hits are few).
+                    book(hits, [&](int jj) {
+                        return static_cast<int>(sh.histA[r0 + 4 * (jj >> 2) + (lane >> 3)]) * GROUP_BLOCKS +
+                               4 * piece + (jj & 3);
+                    });
+                }
+            } else {
+                auto list_scalar = [&](int i) {
+                    if (__uint_as_float(__ldg(g + i)) >= ft) {
+                        const uint32_t slot = atomicAdd(&sh.cand_n, 1u);
+                        if (slot < static_cast<uint32_t>(CAND_MAX)) {
+                            sh.cand_idx[slot] = static_cast<uint32_t>(i);
+                            cp_async_4(key_base + 4u * slot, g + i);
+                        }
+                    }
+                };
+                for (int i = tid; i < head; i += ROW_THREADS) list_scalar(i);
+                for (int i = head + 4 * nvec + tid; i < n; i += ROW_THREADS) list_scalar(i);
+                // The next step's loads are issued as soon as this step's hit bits
+                // are taken, ahead of the slot bookkeeping.
+                uint4 x[LIST_VEC];
+                auto load_step = [&](int v0) {
+#pragma unroll
+                    for (int u = 0; u < LIST_VEC; ++u) {
+                        const int v = v0 + u * ROW_THREADS + tid;
+                        // Past the end: NaN, which no comparison lists.
+                        x[u] = v < nvec ? __ldg(g4 + v) : make_uint4(QNAN_BITS, QNAN_BITS, QNAN_BITS, QNAN_BITS);
+                    }
+                };
+                load_step(0);
+#pragma unroll 1
+                for (int v0 = 0; v0 < nvec; v0 += ROW_THREADS * LIST_VEC) {
+                    // A list already past its capacity is abandoned (warp-uniform test).
+                    if (__shfl_sync(FULL_MASK, *reinterpret_cast<volatile uint32_t *>(&sh.cand_n), 0) >
+                        static_cast<uint32_t>(CAND_MAX))
+                        break;
+                    uint32_t hits = 0u;
+#pragma unroll
+                    for (int u = 0; u < LIST_VEC; ++u) hits |= hit_bits(x[u], u);
+                    if (v0 + ROW_THREADS * LIST_VEC < nvec) load_step(v0 + ROW_THREADS * LIST_VEC);
+                    const int i0 = head + 4 * (v0 + tid);
+                    book(hits, [&](int jj) { return i0 + 4 * ROW_THREADS * (jj >> 2) + (jj & 3); });
                 }
             }
         } else if (tid == 0) {
@@ -593,7 +738,7 @@ __global__ void topk_all_kernel(int active, int k, size_t total, int32_t *__rest
 
 }  // namespace
 
-cudaError_t launch_topk(const float *scores, int nq, int active, int k, int32_t *ids,
+cudaError_t launch_topk(const float *scores, const uint32_t *gmax, int nq, int active, int k, int32_t *ids,
                         cudaStream_t stream) {
     if (active > MAX_ACTIVE) return cudaErrorInvalidValue;
     static thread_local int configured_device = -1;
@@ -615,7 +760,7 @@ cudaError_t launch_topk(const float *scores, int nq, int active, int k, int32_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, topk_row_kernel, scores, active, k, ids);
+    return cudaLaunchKernelEx(&cfg, topk_row_kernel, scores, gmax, active, k, ids);
 }
 
 cudaError_t launch_topk_all(int nq, int active, int k, int32_t *ids, cudaStream_t stream) {

@@ -17,11 +17,13 @@ from . import build as _build
 
 D = 128
 HEADS = 4
+GROUP_BLOCKS = 32   # blocks per group of the group-maximum side output
 TOPK_MAX_ACTIVE = 393216
 
 QSA_OK, QSA_ERR_INVALID, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
 
 EXPORTED = ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
+            "qsa_block_scores_gmax", "qsa_block_scores_q8_gmax", "qsa_block_group_max", "qsa_block_topk_gmax",
             "qsa_get_device_error", "qsa_status_string")
 
 
@@ -52,11 +54,16 @@ def lib() -> ctypes.CDLL:
         L.qsa_block_scores_q8.argtypes = [vp, vp, vp, i, i, i, vp, vp]
         L.qsa_block_scores_ffma.argtypes = [vp, vp, vp, vp, i, i, i, vp, vp]
         L.qsa_block_topk.argtypes = [vp, i, i, i, vp, vp]
+        L.qsa_block_scores_gmax.argtypes = [vp, vp, i, i, i, vp, vp, vp]
+        L.qsa_block_scores_q8_gmax.argtypes = [vp, vp, vp, i, i, i, vp, vp, vp]
+        L.qsa_block_topk_gmax.argtypes = [vp, vp, i, i, i, vp, vp]
+        L.qsa_block_group_max.argtypes = [vp, i, i, vp, vp]
         L.qsa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
         L.qsa_status_string.argtypes = [i]
         L.qsa_status_string.restype = ctypes.c_char_p
         for f in ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
-                  "qsa_get_device_error"):
+                  "qsa_block_scores_gmax", "qsa_block_scores_q8_gmax", "qsa_block_topk_gmax",
+                  "qsa_block_group_max", "qsa_get_device_error"):
             getattr(L, f).restype = i
         _lib = L
     return _lib
@@ -136,6 +143,56 @@ def block_scores_q8(q: torch.Tensor, kblk_q8: torch.Tensor, kscale_f16: torch.Te
     return out
 
 
+def groups(active_blocks: int) -> int:
+    """Number of 32-block groups of a row (the group-maximum row length)."""
+    return (active_blocks + GROUP_BLOCKS - 1) // GROUP_BLOCKS
+
+
+def _gmax_out(q: torch.Tensor, active_blocks: int, out: torch.Tensor | None) -> torch.Tensor:
+    shape = (q.shape[0], groups(active_blocks))
+    if out is None:
+        return torch.empty(shape, dtype=torch.int32, device=q.device)
+    _need(out, "gmax_out", torch.int32, 2)
+    if tuple(out.shape) != shape:
+        raise ValueError(f"gmax_out must have shape {shape}")
+    return out
+
+
+def block_scores_gmax(q: torch.Tensor, kblk: torch.Tensor, active_blocks: int,
+                      out: torch.Tensor | None = None, gmax_out: torch.Tensor | None = None):
+    """``qsa_block_scores_gmax``: ``(scores, gmax)``; ``gmax`` is an int32
+    tensor ``[nq, ceil(active_blocks / 32)]`` holding the uint32 radix keys
+    of each 32-block group's largest score (view it as uint32)."""
+    _check_q(q)
+    _need(kblk, "kblk", torch.float32, 2)
+    if kblk.shape[1] != D:
+        raise ValueError("kblk must be [max_blocks, 128]")
+    out = _scores_out(q, active_blocks, out)
+    gmax_out = _gmax_out(q, active_blocks, gmax_out)
+    _check(lib().qsa_block_scores_gmax(_ptr(q), _ptr(kblk), q.shape[0], kblk.shape[0], active_blocks,
+                                       _ptr(out), _ptr(gmax_out), _stream(q)), "qsa_block_scores_gmax")
+    return out, gmax_out
+
+
+def block_scores_q8_gmax(q: torch.Tensor, kblk_q8: torch.Tensor, kscale_f16: torch.Tensor, active_blocks: int,
+                         out: torch.Tensor | None = None, gmax_out: torch.Tensor | None = None):
+    """``qsa_block_scores_q8_gmax``: the int8-key form of block_scores_gmax."""
+    _check_q(q)
+    _need(kblk_q8, "kblk_q8", torch.int8, 2)
+    if kscale_f16.dtype not in (torch.float16, torch.int16, torch.uint16):
+        raise ValueError("kscale_f16 must hold binary16 values")
+    if not kscale_f16.is_cuda or kscale_f16.dim() != 1 or not kscale_f16.is_contiguous():
+        raise ValueError("kscale_f16 must be a contiguous 1-d CUDA tensor")
+    if kblk_q8.shape[1] != D or kscale_f16.shape[0] < kblk_q8.shape[0]:
+        raise ValueError("kblk_q8 must be [max_blocks, 128] with max_blocks scales")
+    out = _scores_out(q, active_blocks, out)
+    gmax_out = _gmax_out(q, active_blocks, gmax_out)
+    _check(lib().qsa_block_scores_q8_gmax(_ptr(q), _ptr(kblk_q8), _ptr(kscale_f16), q.shape[0], kblk_q8.shape[0],
+                                          active_blocks, _ptr(out), _ptr(gmax_out), _stream(q)),
+           "qsa_block_scores_q8_gmax")
+    return out, gmax_out
+
+
 def block_scores_ffma(q: torch.Tensor, active_blocks: int, kblk: torch.Tensor | None = None,
                       kblk_q8: torch.Tensor | None = None, kscale_f16: torch.Tensor | None = None,
                       out: torch.Tensor | None = None) -> torch.Tensor:
@@ -169,11 +226,49 @@ def block_topk(scores: torch.Tensor, k: int, out: torch.Tensor | None = None) ->
     return out
 
 
+def block_group_max(scores: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """``qsa_block_group_max``: the group maxima (int32 tensor of uint32
+    keys, as block_scores_gmax writes them) of given scores."""
+    _need(scores, "scores", torch.float32, 2)
+    nq, active = scores.shape
+    shape = (nq, groups(active))
+    if out is None:
+        out = torch.empty(shape, dtype=torch.int32, device=scores.device)
+    else:
+        _need(out, "out", torch.int32, 2)
+        if tuple(out.shape) != shape:
+            raise ValueError(f"out must have shape {shape}")
+    _check(lib().qsa_block_group_max(_ptr(scores), nq, active, _ptr(out), _stream(scores)), "qsa_block_group_max")
+    return out
+
+
+def block_topk_gmax(scores: torch.Tensor, gmax: torch.Tensor, k: int,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+    """``qsa_block_topk_gmax``: block_topk's result, using the group maxima
+    that block_scores_gmax wrote for these scores."""
+    _need(scores, "scores", torch.float32, 2)
+    nq, active = scores.shape
+    _need(gmax, "gmax", torch.int32, 2)
+    if tuple(gmax.shape) != (nq, groups(active)):
+        raise ValueError(f"gmax must have shape {(nq, groups(active))}")
+    if out is None:
+        out = torch.empty((nq, k), dtype=torch.int32, device=scores.device)
+    else:
+        _need(out, "out", torch.int32, 2)
+        if tuple(out.shape) != (nq, k):
+            raise ValueError(f"out must have shape {(nq, k)}")
+    _check(lib().qsa_block_topk_gmax(_ptr(scores), _ptr(gmax), nq, active, k, _ptr(out), _stream(scores)),
+           "qsa_block_topk_gmax")
+    return out
+
+
 def block_select(q: torch.Tensor, kblk: torch.Tensor, active_blocks: int, k: int,
-                 scores_out: torch.Tensor | None = None, ids_out: torch.Tensor | None = None):
-    """Scores then top-k, both on the current stream: ``(scores, ids)``."""
-    s = block_scores(q, kblk, active_blocks, scores_out)
-    return s, block_topk(s, k, ids_out)
+                 scores_out: torch.Tensor | None = None, ids_out: torch.Tensor | None = None,
+                 gmax_out: torch.Tensor | None = None):
+    """Scores (with group maxima) then top-k, both on the current stream:
+    ``(scores, ids)``; the ids equal ``block_topk(block_scores(...), k)``."""
+    s, gm = block_scores_gmax(q, kblk, active_blocks, scores_out, gmax_out)
+    return s, block_topk_gmax(s, gm, k, ids_out)
 
 
 def device_error(device: torch.device | None = None) -> int:

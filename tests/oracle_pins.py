@@ -259,6 +259,53 @@ def pin_golden_hand(o) -> None:
         assert np.array_equal(o.topk_f64(S, int(k)), np.array(want, dtype=np.int32)), (k, want)
 
 
+def pin_score_keys_order(o) -> None:
+    """The radix key of the boundary header is order-preserving: on values
+    listed in ascending order the keys ascend strictly, -0 and +0 share a
+    key, NaN has the key of -inf; and on random pairs (with NaN read as -inf)
+    key order equals value order."""
+    f32 = np.float32
+    asc = np.array([-np.inf, -3e38, -1.5, -1.0, -1e-30, -1e-45, 0.0, 1e-45, 1e-30, 1.0, 1.5, 3e38, np.inf],
+                   dtype=f32)
+    k = o.score_keys(asc)
+    assert np.all(np.diff(k.astype(np.int64)) > 0)
+    assert o.score_keys(np.array([-0.0], dtype=f32))[0] == o.score_keys(np.array([0.0], dtype=f32))[0]
+    assert o.score_keys(np.array([np.nan], dtype=f32))[0] == o.score_keys(np.array([-np.inf], dtype=f32))[0]
+    rng = _rng(61)
+    v = rng.standard_normal(600).astype(f32) * f32(10.0) ** rng.integers(-30, 30, 600).astype(f32)
+    v[::37] = np.nan
+    v[5::41] = -0.0
+    v[7::43] = 0.0
+    kv = o.score_keys(v).astype(np.int64)
+    w = np.where(np.isnan(v), -np.inf, v).astype(np.float64)
+    assert np.array_equal(kv[:, None] < kv[None, :], w[:, None] < w[None, :])
+    assert np.array_equal(kv[:, None] == kv[None, :], w[:, None] == w[None, :])
+
+
+def pin_group_max_keys(o) -> None:
+    """Group maxima: on an ascending row each group's maximum is its last
+    element (the short last group too); on random rows with NaN and signed
+    zeros it is the key of the element the oracle's own sort ranks first in
+    that group."""
+    f32 = np.float32
+    row = np.linspace(-5, 5, 100, dtype=f32)[None, :]
+    gm = o.group_max_keys(row)
+    assert gm.shape == (1, 4)
+    assert np.array_equal(gm[0], o.score_keys(row[0, [31, 63, 95, 99]]))
+    rng = _rng(62)
+    S = rng.standard_normal((3, 230)).astype(f32)
+    S[0, ::11] = np.nan
+    S[1, 40:72] = -0.0
+    S[1, 50] = 0.0
+    S[2, 200:230] = np.nan
+    gm = o.group_max_keys(S)
+    assert gm.shape == (3, 8)
+    for g in range(8):
+        part = np.ascontiguousarray(S[:, 32 * g:32 * g + 32])
+        top = o.topk_f32(part, 1)[:, 0]
+        assert np.array_equal(gm[:, g], o.score_keys(part[np.arange(3), top]))
+
+
 ALL_PINS = [
     pin_brute_force_topk,
     pin_closed_form_onehot,
@@ -271,4 +318,6 @@ ALL_PINS = [
     pin_capacity_independence,
     pin_selection_invariants,
     pin_golden_hand,
+    pin_score_keys_order,
+    pin_group_max_keys,
 ]

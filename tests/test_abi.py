@@ -99,3 +99,25 @@ def test_product_path_does_not_import_the_oracle():
             if fn.endswith((".py", ".cu", ".cuh", ".c", ".h")):
                 text = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in text and "qsa_oracle" not in text, fn
+
+
+def test_group_max_argument_errors(lib):
+    f = lib.qsa_block_scores_gmax
+    assert f(A, B, 8, 100, 10, A, None, None) == INVALID     # null group_max
+    assert f(A, B, 8, 100, 10, A, MIS, None) == INVALID      # misaligned group_max
+    assert f(A, B, 8, 100, 101, A, B, None) == INVALID       # active > max_blocks
+    assert f(None, None, 0, 100, 10, None, None, None) == OK  # no work
+    g = lib.qsa_block_scores_q8_gmax
+    assert g(A, B, B, 8, 100, 10, A, None, None) == INVALID
+    assert g(A, B, B + 1, 8, 100, 10, A, B, None) == INVALID  # odd scale address
+    h = lib.qsa_block_group_max
+    assert h(A, 4, 100, None, None) == INVALID
+    assert h(MIS, 4, 100, B, None) == INVALID
+    assert h(A, -1, 100, B, None) == INVALID
+    assert h(None, 0, 100, None, None) == OK
+    t = lib.qsa_block_topk_gmax
+    assert t(A, None, 4, 100, 5, B, None) == INVALID          # null group_max
+    assert t(A, MIS, 4, 100, 5, B, None) == INVALID
+    assert t(A, B, 4, 100, 0, B, None) == INVALID             # k < 1
+    assert t(A, B, 4, qsa.TOPK_MAX_ACTIVE + 1, 5, B, None) == UNSUPPORTED
+    assert t(None, None, 0, 100, 5, None, None) == OK
