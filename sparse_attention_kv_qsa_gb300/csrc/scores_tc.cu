@@ -102,7 +102,11 @@ struct TcBarriers {
     uint32_t tmem_base;
 };
 
-constexpr size_t TC_SMEM = BAR_OFF + sizeof(TcBarriers) + 1024;
+static_assert(sizeof(TcBarriers) <= 256, "barriers fit their slot");
+// Group-maximum exchange: the second column team's two keys per query row,
+// read by the first team, which stores the tile's four with one 16-byte store.
+constexpr int GX_OFF = BAR_OFF + 256;
+constexpr size_t TC_SMEM = GX_OFF + QGROUP * 8 + 1024;
 
 __device__ uint32_t g_tc_error;
 
@@ -393,28 +397,48 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (col0 + j < nb) v[j] = __fmul_rn(v[j], __half2float(kscale[b0 + col0 + j]));
             }
             // Group maxima: this thread's 64 columns are two 32-block groups.
-            if (gmax != nullptr && row < qn) {
-                const int ngr = (active + GROUP_BLOCKS - 1) / GROUP_BLOCKS;
+            // fmaxf skips NaN (an all-NaN group stays NaN, whose key is that of
+            // -inf) and the key maps -0 and +0 together, so the key of the
+            // float maximum is the maximum key.
+            const int ngr = (active + GROUP_BLOCKS - 1) / GROUP_BLOCKS;
+            uint32_t gk[2] = {0u, 0u};
+            if (gmax != nullptr) {
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
                     const int c0 = col0 + GROUP_BLOCKS * g;
-                    if (c0 < nb) {
-                        // fmaxf skips NaN (an all-NaN group stays NaN, whose key
-                        // is that of -inf) and the key maps -0 and +0 together,
-                        // so the key of the float maximum is the maximum key.
-                        float m = v[GROUP_BLOCKS * g];
+                    float m = v[GROUP_BLOCKS * g];
+                    if (c0 + GROUP_BLOCKS <= nb) {
+#pragma unroll
+                        for (int j = 1; j < GROUP_BLOCKS; ++j) m = fmaxf(m, v[GROUP_BLOCKS * g + j]);
+                    } else {
 #pragma unroll
                         for (int j = 1; j < GROUP_BLOCKS; ++j)
                             if (c0 + j < nb) m = fmaxf(m, v[GROUP_BLOCKS * g + j]);
-                        gmax[static_cast<size_t>(q0 + row) * ngr + (b0 + c0) / GROUP_BLOCKS] = score_key(m);
                     }
+                    gk[g] = score_key(m);
                 }
             }
+            // Whole tiles with 16-byte aligned maxima rows go out as one store
+            // of four keys per row (the teams meet at the store barriers);
+            // otherwise each thread stores its own.
+            const bool gvec = gmax != nullptr && use_tma && (ngr & 3) == 0 && nb == TILE_N;
+            if (gmax != nullptr && !gvec && row < qn) {
+#pragma unroll
+                for (int g = 0; g < 2; ++g)
+                    if (col0 + GROUP_BLOCKS * g < nb)
+                        gmax[static_cast<size_t>(q0 + row) * ngr + (b0 + col0) / GROUP_BLOCKS + g] = gk[g];
+            }
+            if (gvec && team == 1) st_shared_v2(base + GX_OFF + row * 8, gk[0], gk[1]);
             if (use_tma) {
 #pragma unroll 1
                 for (int tm = 0; tm < 2; ++tm) {
                     if (epi_tid == 0) bulk_wait_read0();    // earlier stores have read the staging
                     named_bar_sync(2, EPI_THREADS);
+                    if (tm == 0 && gvec && team == 0 && row < qn) {
+                        const uint2 o = ld_shared_v2(base + GX_OFF + row * 8);
+                        *reinterpret_cast<uint4 *>(gmax + static_cast<size_t>(q0 + row) * ngr + b0 / GROUP_BLOCKS) =
+                            make_uint4(gk[0], gk[1], o.x, o.y);
+                    }
                     if (team == tm) {
 #pragma unroll
                         for (int j = 0; j < TILE_N / 8; ++j) {
