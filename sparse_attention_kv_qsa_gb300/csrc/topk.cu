@@ -52,7 +52,7 @@ constexpr int LIST_VEC = 8;              // 16-byte loads per thread per listing
 constexpr int CAND_MAX = 4096;           // candidate-list capacity
 constexpr int SAMPLE_STRIDE = 32;        // one 16-byte group of scores sampled per 512 bytes
 constexpr int SAMPLE_SHIFT = 18;         // sample bins: 2^18 keys = 1/32 octave; 256 bins span 8
-constexpr int GMAX_SUB_SHIFT = 10;       // group-maximum refinement: 2^10-key bins inside one of those
+constexpr int GMAX_SHIFT = 15;           // group-maximum bins: 2^15 keys = 1/256 octave; 2,048 bins span 8
 constexpr int FAST_MIN_ACTIVE = 8192;    // shorter rows take the exact passes directly
 constexpr int MAX_ACTIVE = 393216;
 constexpr int SAMPLE_REGS = (MAX_ACTIVE / 4 / SAMPLE_STRIDE + ROW_THREADS - 1) / ROW_THREADS;
@@ -283,8 +283,10 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         sh.cand_n = 0u;
         sh.glist_n = 0u;
     }
-    if (!try_list)
-        for (int i = tid; i < HIST_A; i += ROW_THREADS) sh.histA[i] = 0u;   // the exact path's histogram
+    if (!try_list || use_gmax) {   // the exact path's histogram, or the group-maximum bins
+        static_assert(HIST_A == 4 * ROW_THREADS, "one 16-byte store per thread clears histA");
+        reinterpret_cast<uint4 *>(sh.histA)[tid] = make_uint4(0u, 0u, 0u, 0u);
+    }
     for (int i = tid; i < BINS_R; i += ROW_THREADS) sh.histR[i] = 0u;
     for (int i = tid; i < nwords; i += ROW_THREADS) {
         selbits[i] = 0u;
@@ -298,18 +300,20 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
     if (try_list) {
         const uint32_t gk[4] = {sx[0].x, sx[0].y, sx[0].z, sx[0].w};   // group-maximum mode's keys
         if (use_gmax) {
-            // Group-maximum threshold: the distance-below-maximum bins of the
-            // sample (below), over the group maxima with target k, then once
-            // more with 2^10-key bins inside the bin found. tg is the lowest
-            // key of the finer bin where the count of groups from the top
-            // reaches k: at least k groups, hence at least k scores, are
-            // >= tg, and few groups beyond k are.
+            // Group-maximum threshold: the group maxima are counted by their
+            // distance below the largest, smax, in 2,048 bins of 2^15 keys
+            // (1/256 of an octave for normal floats) spanning 8 octaves. tg is
+            // the lowest key of the bin where the count of groups from the top
+            // reaches k: at least k groups, hence at least k scores, are >= tg,
+            // and few groups beyond k are. A k-th group maximum below the
+            // window leaves tg = 0: the exact path.
             uint32_t m = 0u;
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 if (4 * tid + e < ngr) m = max(m, gk[e]);
             m = __reduce_max_sync(FULL_MASK, m);
             if (lane == 0) sh.scan_tot[warp] = m;
+            if (tid == 0) sh.sel_cnt = 0u;   // stays 0 when no bin is found
             __syncthreads();
             uint32_t smax = 0u;
 #pragma unroll
@@ -320,27 +324,20 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const uint32_t d = smax - gk[e];
-                if (4 * tid + e < ngr && d < (static_cast<uint32_t>(BINS_R) << SAMPLE_SHIFT))
-                    atomicAdd(&sh.histR[BINS_R - 1 - (d >> SAMPLE_SHIFT)], 1u);
+                if (4 * tid + e < ngr && d < (static_cast<uint32_t>(HIST_A) << GMAX_SHIFT))
+                    atomicAdd(&sh.histA[HIST_A - 1 - (d >> GMAX_SHIFT)], 1u);
             }
             __syncthreads();
-            if (warp == 0) warp_select_256(sh.histR, kk, sh, lane);
-            __syncthreads();
-            if (sh.sel_cnt != 0u) {  // uniform; otherwise tg = 0: the exact path
-                const uint32_t b = static_cast<uint32_t>(BINS_R - 1) - sh.sel_bin;   // bins below smax
-                const uint32_t top = smax - (b << SAMPLE_SHIFT);                   // the bin's highest key
-                const uint32_t need = kk - sh.sel_above;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if (4 * tid + e < ngr && ((smax - gk[e]) >> SAMPLE_SHIFT) == b)
-                        atomicAdd(&sh.histR[BINS_R - 1 - ((top - gk[e]) >> GMAX_SUB_SHIFT)], 1u);
-                }
-                __syncthreads();
-                if (warp == 0) warp_select_256(sh.histR, need, sh, lane);
-                __syncthreads();
-                const uint32_t below2 = (static_cast<uint32_t>(BINS_R) - sh.sel_bin) << GMAX_SUB_SHIFT;
-                tg = top >= below2 ? top - below2 + 1u : 0u;
+            if (tid < HIST_A / GROUP) {
+                const uint4 a = *reinterpret_cast<const uint4 *>(&sh.histA[GROUP * tid]);
+                const uint4 b = *reinterpret_cast<const uint4 *>(&sh.histA[GROUP * tid + 4]);
+                sh.groupA[tid] = a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w;
             }
+            __syncthreads();
+            if (warp == 0) warp_select_2048(kk, sh, lane);
+            __syncthreads();
+            const uint32_t below = (static_cast<uint32_t>(HIST_A) - sh.sel_bin) << GMAX_SHIFT;   // (b + 1) bins
+            tg = sh.sel_cnt != 0u && smax >= below ? smax - below + 1u : 0u;
         } else {
             // Sample threshold. The largest sample key smax tops a window of 256
             // bins, each 2^18 keys wide (1/32 of an octave for normal floats),
