@@ -292,6 +292,15 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         selbits[i] = 0u;
         tiebits[i] = 0u;
     }
+    if (use_gmax) {   // the group maxima's warp maxima ride on the same barrier
+        uint32_t m = 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (4 * tid + e < ngr) m = max(m, (&sx[0].x)[e]);
+        m = __reduce_max_sync(FULL_MASK, m);
+        if (lane == 0) sh.scan_tot[warp] = m;
+        if (tid == 0) sh.sel_cnt = 0u;   // stays 0 when no threshold bin is found
+    }
     __syncthreads();
 
     uint32_t kk = static_cast<uint32_t>(k);
@@ -307,20 +316,13 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
             // reaches k: at least k groups, hence at least k scores, are >= tg,
             // and few groups beyond k are. A k-th group maximum below the
             // window leaves tg = 0: the exact path.
-            uint32_t m = 0u;
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (4 * tid + e < ngr) m = max(m, gk[e]);
-            m = __reduce_max_sync(FULL_MASK, m);
-            if (lane == 0) sh.scan_tot[warp] = m;
-            if (tid == 0) sh.sel_cnt = 0u;   // stays 0 when no bin is found
-            __syncthreads();
             uint32_t smax = 0u;
 #pragma unroll
             for (int q = 0; q < ROW_WARPS / 4; ++q) {
                 const uint4 t = *reinterpret_cast<const uint4 *>(sh.scan_tot + 4 * q);
                 smax = max(max(smax, t.x), max(t.y, max(t.z, t.w)));
             }
+            kmax = smax;   // the row maximum: every listed key lies in [tg, smax]
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const uint32_t d = smax - gk[e];
@@ -534,7 +536,14 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         __syncthreads();
         const uint32_t nc = sh.cand_n;
         listed = nc >= kk && nc <= static_cast<uint32_t>(CAND_MAX);
-        if (listed) {
+        if (listed && use_gmax) {
+            // The listed scores become keys in place (their maximum, the row's,
+            // is known from the group maxima).
+#pragma unroll 4
+            for (int j = tid; j < static_cast<int>(nc); j += ROW_THREADS)
+                sh.cand_key[j] = float_bits_to_key(sh.cand_key[j]);
+            __syncthreads();
+        } else if (listed) {
             // The listed scores become keys in place; the largest is kept.
 #pragma unroll 4
             for (int j = tid; j < static_cast<int>(nc); j += ROW_THREADS) {
