@@ -158,6 +158,27 @@ qsa_status qsa_block_group_max(const float *scores, int nq, int active_blocks, u
 qsa_status qsa_block_topk_gmax(const float *scores, const uint32_t *group_max, int nq, int active_blocks,
                                int k, int32_t *ids, cudaStream_t stream);
 
+/* Largest nq * ceil(active_blocks / 32) qsa_block_select_static accepts:
+ * its scratch is a fixed 1 MiB device array of that many uint32. */
+#define QSA_SELECT_STATIC_GROUPS_MAX 262144
+
+/*
+ * Scores and exact top-k in one call that allocates nothing: exactly
+ * qsa_block_scores_gmax followed by qsa_block_topk_gmax, with the group
+ * maxima kept in a file-scope device array of QSA_SELECT_STATIC_GROUPS_MAX
+ * uint32 (1 MiB, part of the library image) instead of caller memory.
+ * scores  fp32  [nq][active_blocks], written (as qsa_block_scores).
+ * ids     int32 [nq][k], written (as qsa_block_topk).
+ * nq * ceil(active_blocks / 32) > QSA_SELECT_STATIC_GROUPS_MAX returns
+ * QSA_ERR_UNSUPPORTED before anything is launched (e.g. 256 queries up to
+ * 32,768 active blocks, 128 up to 65,536). The scratch is one per device:
+ * calls on one device must be ordered (one stream, or streams joined by
+ * events); overlapping calls on unordered streams give undefined ids.
+ * Other arguments, errors and accuracy as the two calls it stands for.
+ */
+qsa_status qsa_block_select_static(const float *q, const float *kblk, int nq, int max_blocks, int active_blocks,
+                                   int k, float *scores, int32_t *ids, cudaStream_t stream);
+
 /*
  * Reads and clears the current device's error word: nonzero when a kernel
  * of this library gave up a bounded wait (its outputs are then invalid).

@@ -89,6 +89,27 @@ qsa_status topk(const float *scores, const uint32_t *gmax, bool want_gmax, int n
     return from_cuda(qsa::launch_topk(scores, gmax, nq, active_blocks, k, ids, stream));
 }
 
+// Scratch of qsa_block_select_static: the group maxima between its two
+// kernels, in the library image (no allocation at call time).
+static __device__ __align__(256) uint32_t g_select_gmax[QSA_SELECT_STATIC_GROUPS_MAX];
+
+// Device address of g_select_gmax in the current device's context (looked up
+// once per device).
+uint32_t *select_scratch() {
+    static std::mutex mu;
+    static std::vector<uint32_t *> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= static_cast<int>(cache.size())) cache.resize(dev + 1, nullptr);
+    if (cache[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_select_gmax) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<uint32_t *>(p);
+    }
+    return cache[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -147,6 +168,26 @@ qsa_status qsa_block_group_max(const float *scores, int nq, int active_blocks, u
 qsa_status qsa_block_topk_gmax(const float *scores, const uint32_t *group_max, int nq, int active_blocks, int k,
                                int32_t *ids, cudaStream_t stream) {
     return topk(scores, group_max, true, nq, active_blocks, k, ids, stream);
+}
+
+qsa_status qsa_block_select_static(const float *q, const float *kblk, int nq, int max_blocks, int active_blocks,
+                                   int k, float *scores, int32_t *ids, cudaStream_t stream) {
+    // Arguments first (the scratch bound included), then both calls.
+    qsa_status s = check_score_args(q, nq, max_blocks, active_blocks, scores);
+    if (s != QSA_OK) return s;
+    if (k < 1) return QSA_ERR_INVALID;
+    if (nq == 0) return QSA_OK;
+    if (ids == nullptr || !aligned16(ids)) return QSA_ERR_INVALID;
+    if (active_blocks > 0 && (kblk == nullptr || !aligned16(kblk))) return QSA_ERR_INVALID;
+    const long long groups = static_cast<long long>(nq) * ((active_blocks + qsa::GROUP_BLOCKS - 1) / qsa::GROUP_BLOCKS);
+    if (groups > QSA_SELECT_STATIC_GROUPS_MAX) return QSA_ERR_UNSUPPORTED;
+    uint32_t *gm = select_scratch();
+    if (gm == nullptr) return QSA_ERR_CUDA;
+    if (active_blocks > 0) {
+        s = scores_f32(q, kblk, nq, max_blocks, active_blocks, scores, gm, true, stream);
+        if (s != QSA_OK) return s;
+    }
+    return topk(scores, gm, true, nq, active_blocks, k, ids, stream);
 }
 
 qsa_status qsa_get_device_error(uint32_t *code, cudaStream_t stream) {

@@ -19,12 +19,13 @@ D = 128
 HEADS = 4
 GROUP_BLOCKS = 32   # blocks per group of the group-maximum side output
 TOPK_MAX_ACTIVE = 393216
+SELECT_STATIC_GROUPS_MAX = 262144   # scratch bound of qsa_block_select_static
 
 QSA_OK, QSA_ERR_INVALID, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
 
 EXPORTED = ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
             "qsa_block_scores_gmax", "qsa_block_scores_q8_gmax", "qsa_block_group_max", "qsa_block_topk_gmax",
-            "qsa_get_device_error", "qsa_status_string")
+            "qsa_block_select_static", "qsa_get_device_error", "qsa_status_string")
 
 
 class QSAError(RuntimeError):
@@ -58,12 +59,13 @@ def lib() -> ctypes.CDLL:
         L.qsa_block_scores_q8_gmax.argtypes = [vp, vp, vp, i, i, i, vp, vp, vp]
         L.qsa_block_topk_gmax.argtypes = [vp, vp, i, i, i, vp, vp]
         L.qsa_block_group_max.argtypes = [vp, i, i, vp, vp]
+        L.qsa_block_select_static.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
         L.qsa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
         L.qsa_status_string.argtypes = [i]
         L.qsa_status_string.restype = ctypes.c_char_p
         for f in ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
                   "qsa_block_scores_gmax", "qsa_block_scores_q8_gmax", "qsa_block_topk_gmax",
-                  "qsa_block_group_max", "qsa_get_device_error"):
+                  "qsa_block_group_max", "qsa_block_select_static", "qsa_get_device_error"):
             getattr(L, f).restype = i
         _lib = L
     return _lib
@@ -269,6 +271,28 @@ def block_select(q: torch.Tensor, kblk: torch.Tensor, active_blocks: int, k: int
     ``(scores, ids)``; the ids equal ``block_topk(block_scores(...), k)``."""
     s, gm = block_scores_gmax(q, kblk, active_blocks, scores_out, gmax_out)
     return s, block_topk_gmax(s, gm, k, ids_out)
+
+
+def block_select_static(q: torch.Tensor, kblk: torch.Tensor, active_blocks: int, k: int,
+                        scores_out: torch.Tensor | None = None, ids_out: torch.Tensor | None = None):
+    """``qsa_block_select_static``: ``(scores, ids)`` as block_select, with
+    the group maxima in the library's fixed device scratch (the call
+    allocates nothing; calls on one device must be ordered)."""
+    _check_q(q)
+    _need(kblk, "kblk", torch.float32, 2)
+    if kblk.shape[1] != D:
+        raise ValueError("kblk must be [max_blocks, 128]")
+    nq = q.shape[0]
+    scores_out = _scores_out(q, active_blocks, scores_out)
+    if ids_out is None:
+        ids_out = torch.empty((nq, k), dtype=torch.int32, device=q.device)
+    else:
+        _need(ids_out, "ids_out", torch.int32, 2)
+        if tuple(ids_out.shape) != (nq, k):
+            raise ValueError(f"ids_out must have shape {(nq, k)}")
+    _check(lib().qsa_block_select_static(_ptr(q), _ptr(kblk), nq, kblk.shape[0], active_blocks, k, _ptr(scores_out),
+                                         _ptr(ids_out), _stream(q)), "qsa_block_select_static")
+    return scores_out, ids_out
 
 
 def device_error(device: torch.device | None = None) -> int:
