@@ -93,7 +93,8 @@ def decode_side_measurement(dev, stream):
     """Decode-shaped calls (int8 keys, k=128, 262,144 cells = 65,536 blocks;
     nq = 1 and 4): launch- and latency-bound, so reported in microseconds per
     score + top-k step, once with a CUDA-event pair per step (L2 flushed
-    first) and once per step of a CUDA graph of 20 back-to-back steps."""
+    first) and once per step of a CUDA graph of 20 back-to-back steps; for
+    the group-maximum calls (gmax) and the plain ones."""
     import torch
     import sparse_attention_kv_qsa_gb300 as qsa
     from sparse_attention_kv_qsa_gb300 import workloads as w
@@ -106,41 +107,49 @@ def decode_side_measurement(dev, stream):
         kq = torch.from_numpy(W.kq8).to(dev)
         ks = torch.from_numpy(W.kscale.view(np.int16)).to(dev)
         s = torch.empty((nq, W.active), dtype=torch.float32, device=dev)
+        gm = torch.empty((nq, qsa.groups(W.active)), dtype=torch.int32, device=dev)
         ids = torch.empty((nq, W.k), dtype=torch.int32, device=dev)
 
-        def step():
+        def step_gmax():
+            qsa.block_scores_q8_gmax(q, kq, ks, W.active, out=s, gmax_out=gm)
+            qsa.block_topk_gmax(s, gm, W.k, out=ids)
+
+        def step_plain():
             qsa.block_scores_q8(q, kq, ks, W.active, out=s)
             qsa.block_topk(s, W.k, out=ids)
 
-        for _ in range(5):
-            step()
-        torch.cuda.synchronize()
-        ts = []
-        for i in range(50):
-            flush.fill_(float(i))
+        res = {}
+        for name, step in (("gmax", step_gmax), ("plain", step_plain)):
+            for _ in range(5):
+                step()
+            torch.cuda.synchronize()
+            ts = []
+            for i in range(50):
+                flush.fill_(float(i))
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                step()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(1e3 * e0.elapsed_time(e1))
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                step()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g, stream=side):
+                    for _ in range(20):
+                        step()
+            torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            step()
+            g.replay()
             e1.record(stream)
-            e1.synchronize()
-            ts.append(1e3 * e0.elapsed_time(e1))
-        g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(side):
-            step()
             torch.cuda.synchronize()
-            with torch.cuda.graph(g, stream=side):
-                for _ in range(20):
-                    step()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        out[f"nq{nq}"] = {"step_p50": pct(ts, 50), "step_p10": pct(ts, 10), "step_p90": pct(ts, 90),
-                          "graph_step": 1e3 * e0.elapsed_time(e1) / 20}
+            res[name] = {"step_p50": pct(ts, 50), "step_p10": pct(ts, 10), "step_p90": pct(ts, 90),
+                         "graph_step": 1e3 * e0.elapsed_time(e1) / 20}
+        out[f"nq{nq}"] = res
     return out
 
 

@@ -48,11 +48,8 @@ qsa_status check_score_args(const float *q, int nq, int max_blocks, int active_b
 // Scores (and, when gmax is given, group maxima) through the kernel for nq.
 qsa_status run_scores(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale, int nq,
                       int active, float *scores, uint32_t *gmax, cudaStream_t stream) {
-    if (nq <= qsa::SMALL_NQ_MAX) {
-        cudaError_t e = qsa::launch_scores_rows(q, kblk, kq8, kscale, nq, active, scores, stream);
-        if (e == cudaSuccess && gmax != nullptr) e = qsa::launch_group_max(scores, nq, active, gmax, stream);
-        return from_cuda(e);
-    }
+    if (nq <= qsa::SMALL_NQ_MAX)
+        return from_cuda(qsa::launch_scores_rows(q, kblk, kq8, kscale, nq, active, scores, gmax, stream));
     return from_cuda(qsa::launch_scores_tc(q, kblk, kq8, kscale, nq, active, scores, gmax, stream));
 }
 

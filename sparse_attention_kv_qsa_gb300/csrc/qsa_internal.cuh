@@ -39,10 +39,10 @@ cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq
 cudaError_t launch_group_max(const float *scores, int nq, int active, uint32_t *gmax, cudaStream_t stream);
 
 // Scores for nq <= 4 (decode) on CUDA cores, the grid spanning key rows.
-// Exactly one of kblk / (kq8, kscale) is non-null.
+// Exactly one of kblk / (kq8, kscale) is non-null; gmax as launch_scores_tc.
 constexpr int SMALL_NQ_MAX = 4;
 cudaError_t launch_scores_rows(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,
-                               int nq, int active, float *scores, cudaStream_t stream);
+                               int nq, int active, float *scores, uint32_t *gmax, cudaStream_t stream);
 
 // Exact top-k (k < active); one CTA per row. gmax (may be null): the
 // group maxima of these scores, which let a row read only the groups that

@@ -33,7 +33,7 @@ template <int NQ, bool kInt8>
 __global__ void __launch_bounds__(ROWS_THREADS)
     scores_rows_kernel(const float *__restrict__ q, const float *__restrict__ kblk,
                        const int8_t *__restrict__ kq8, const __half *__restrict__ kscale, int nq, int active,
-                       float *__restrict__ scores) {
+                       float *__restrict__ scores, uint32_t *__restrict__ gmax) {
     constexpr int TPR = kInt8 ? 2 : 4;          // threads per key row
     constexpr int PER = D / TPR;                // values per thread: 64 (int8) or 32 (fp32)
     __shared__ __align__(16) float qs[NQ][QROW];   // head-summed queries, zero past nq
@@ -111,14 +111,38 @@ __global__ void __launch_bounds__(ROWS_THREADS)
     if (live && part == 0) {
         const float scale = kInt8 ? __half2float(kscale[b]) : 1.0f;
 #pragma unroll
-        for (int r = 0; r < NQ; ++r)
-            if (r < nq) scores[static_cast<size_t>(r) * active + b] = kInt8 ? __fmul_rn(acc[r], scale) : acc[r];
+        for (int r = 0; r < NQ; ++r) {
+            if (kInt8) acc[r] = __fmul_rn(acc[r], scale);
+            if (r < nq) scores[static_cast<size_t>(r) * active + b] = acc[r];
+        }
+    }
+    // Group maxima (when asked): this CTA's rows are whole 32-block groups;
+    // their keys meet in shared memory and one warp per (query, group) takes
+    // the maximum.
+    if (gmax != nullptr) {   // uniform
+        constexpr int ROWS = ROWS_THREADS / TPR;      // rows of this CTA: 64 (fp32) or 128 (int8)
+        constexpr int GROUPS = ROWS / GROUP_BLOCKS;
+        __shared__ uint32_t gk[NQ][ROWS];
+        const int rl = threadIdx.x / TPR;
+        if (part == 0) {
+#pragma unroll
+            for (int r = 0; r < NQ; ++r) gk[r][rl] = live ? score_key(acc[r]) : 0u;
+        }
+        __syncthreads();
+        const int ngr = (active + GROUP_BLOCKS - 1) / GROUP_BLOCKS;
+        const int lane = threadIdx.x & 31;
+        for (int w = threadIdx.x >> 5; w < NQ * GROUPS; w += ROWS_THREADS / 32) {   // warp-uniform
+            const int r = w / GROUPS, gl = w % GROUPS;
+            const uint32_t key = __reduce_max_sync(FULL_MASK, gk[r][gl * GROUP_BLOCKS + lane]);
+            const long long g = static_cast<long long>(blockIdx.x) * GROUPS + gl;
+            if (lane == 0 && r < nq && g < ngr) gmax[static_cast<size_t>(r) * ngr + g] = key;
+        }
     }
 }
 
 template <int NQ>
 cudaError_t launch_rows(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale, int nq,
-                        int active, float *scores, cudaStream_t stream) {
+                        int active, float *scores, uint32_t *gmax, cudaStream_t stream) {
     const int tpr = kq8 != nullptr ? 2 : 4;
     const long long threads = static_cast<long long>(active) * tpr;
     const long long grid = (threads + ROWS_THREADS - 1) / ROWS_THREADS;
@@ -135,9 +159,9 @@ cudaError_t launch_rows(const float *q, const float *kblk, const int8_t *kq8, co
     cfg.numAttrs = 1;
     if (kq8 != nullptr)
         return cudaLaunchKernelEx(&cfg, scores_rows_kernel<NQ, true>, q, static_cast<const float *>(nullptr), kq8,
-                                  reinterpret_cast<const __half *>(kscale), nq, active, scores);
+                                  reinterpret_cast<const __half *>(kscale), nq, active, scores, gmax);
     return cudaLaunchKernelEx(&cfg, scores_rows_kernel<NQ, false>, q, kblk, static_cast<const int8_t *>(nullptr),
-                              static_cast<const __half *>(nullptr), nq, active, scores);
+                              static_cast<const __half *>(nullptr), nq, active, scores, gmax);
 }
 
 // Group maxima of packed scores: one warp per 32-block group, lane j taking
@@ -179,12 +203,12 @@ cudaError_t launch_group_max(const float *scores, int nq, int active, uint32_t *
 }
 
 cudaError_t launch_scores_rows(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,
-                               int nq, int active, float *scores, cudaStream_t stream) {
+                               int nq, int active, float *scores, uint32_t *gmax, cudaStream_t stream) {
     switch (nq) {
-        case 1: return launch_rows<1>(q, kblk, kq8, kscale, nq, active, scores, stream);
-        case 2: return launch_rows<2>(q, kblk, kq8, kscale, nq, active, scores, stream);
+        case 1: return launch_rows<1>(q, kblk, kq8, kscale, nq, active, scores, gmax, stream);
+        case 2: return launch_rows<2>(q, kblk, kq8, kscale, nq, active, scores, gmax, stream);
         case 3:
-        case 4: return launch_rows<4>(q, kblk, kq8, kscale, nq, active, scores, stream);
+        case 4: return launch_rows<4>(q, kblk, kq8, kscale, nq, active, scores, gmax, stream);
         default: return cudaErrorInvalidValue;
     }
 }
