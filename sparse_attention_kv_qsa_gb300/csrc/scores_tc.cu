@@ -36,7 +36,9 @@
 //  - 8 epilogue warps (two per TMEM lane quarter, one per column half;
 //    thread = query row) read both accumulators out at once, so the next
 //    tile's MMAs can start, add them, and store the scores by 2-D tensor
-//    stores (or coalesced direct stores when rows are not 16-byte aligned).
+//    stores (or coalesced direct stores when rows are not 16-byte aligned);
+//    on request they also store the key of each 32-block group's largest
+//    score (the group maxima the top-k can use).
 //  - Key rows at or beyond `active` are never read; the grid comes from
 //    `active` and nq alone.
 // Every mbarrier wait is bounded; a timeout sets the error word.

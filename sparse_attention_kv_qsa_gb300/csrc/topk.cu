@@ -20,7 +20,12 @@
 //
 // GB300 layout. One 512-thread CTA owns one row (two CTAs per SM, so every row
 // of a 256-query call is in flight at once):
-//  Rows of at least 8,192 scores first try a listing path. A strided 1/32
+//  With the scorer's group maxima (the key of each 32-block group's largest
+//  score), a threshold that at least k groups reach is at most the k-th
+//  score, so every score of the top k lies in a group at or above it: the row
+//  lists only those groups (about k of them, one 128-byte line each) and the
+//  digits below run on that list.
+//  Without them, rows of at least 8,192 scores first try a listing path. A strided 1/32
 //  sample of the row fixes a threshold expected to pass about 1.8k scores;
 //  one pass of 16-byte read-only loads then lists every score at or above
 //  the threshold, and the digits below run on that list alone. A list shorter than k or longer
