@@ -318,6 +318,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="warm L2 (back-to-back steps)")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped side measurement")
+    ap.add_argument("--no-ksweep", action="store_true", help="skip the k sweep (64, 256, 1024) side measurement")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -535,6 +536,25 @@ def main():
 
     if rank == 0 and not args.no_decode:
         line["decode"] = decode_side_measurement(dev, stream)
+
+    if rank == 0 and not args.no_ksweep and path == "gmax":
+        # The headline workload's k sweep, same calls and flushes, 200 steps
+        # each; ids checked against the plain path once per k.
+        sweep = {}
+        for ks in (64, 256, 1024):
+            ids_k = torch.empty((W.nq, ks), dtype=torch.int32, device=dev)
+            ids_p = torch.empty((W.nq, ks), dtype=torch.int32, device=dev)
+            sc = lambda: qsa.block_scores_gmax(q, kblk, W.active, out=scores, gmax_out=gmax)
+            tk = lambda: qsa.block_topk_gmax(scores, gmax, ks, out=ids_k)
+            for _ in range(args.warmup):
+                sc()
+                tk()
+            t_s, t_k, t_st, _ = timed_steps(sc, tk, 200)
+            qsa.block_topk(scores, ks, out=ids_p)
+            torch.cuda.synchronize()
+            assert torch.equal(ids_k, ids_p), f"k={ks}: the two top-k paths disagree"
+            sweep[f"k{ks}"] = {"step_us": 1e3 * statistics.mean(t_st), "topk_us": 1e3 * statistics.mean(t_k)}
+        line["k_sweep"] = sweep
 
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_baseline(W)
