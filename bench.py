@@ -94,7 +94,8 @@ def decode_side_measurement(dev, stream):
     nq = 1 and 4): launch- and latency-bound, so reported in microseconds per
     score + top-k step, once with a CUDA-event pair per step (L2 flushed
     first) and once per step of a CUDA graph of 20 back-to-back steps; for
-    the group-maximum calls (gmax) and the plain ones."""
+    the one-launch call (fused: qsa_block_select_small), the group-maximum
+    calls (gmax) and the plain ones."""
     import torch
     import sparse_attention_kv_qsa_gb300 as qsa
     from sparse_attention_kv_qsa_gb300 import workloads as w
@@ -118,8 +119,11 @@ def decode_side_measurement(dev, stream):
             qsa.block_scores_q8(q, kq, ks, W.active, out=s)
             qsa.block_topk(s, W.k, out=ids)
 
+        def step_fused():
+            qsa.block_select_small(q, W.active, W.k, kblk_q8=kq, kscale_f16=ks, scores_out=s, ids_out=ids)
+
         res = {}
-        for name, step in (("gmax", step_gmax), ("plain", step_plain)):
+        for name, step in (("fused", step_fused), ("gmax", step_gmax), ("plain", step_plain)):
             for _ in range(5):
                 step()
             torch.cuda.synchronize()

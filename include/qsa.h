@@ -180,6 +180,29 @@ qsa_status qsa_block_select_static(const float *q, const float *kblk, int nq, in
                                    int k, float *scores, int32_t *ids, cudaStream_t stream);
 
 /*
+ * Scores and exact top-k for a few queries (decode: 1 <= nq <= 4) in one
+ * cooperative kernel launch: the whole grid scores every active block (and
+ * its 32-block group maxima, kept in a fixed device array of the library),
+ * then nq of its CTAs each select one query's top k from those maxima. The
+ * scores and ids equal qsa_block_scores(_q8) followed by qsa_block_topk.
+ * Give kblk (fp32 keys) or kblk_q8 + kscale_f16 (int8 keys), not both; the
+ * layouts are those of qsa_block_scores / qsa_block_scores_q8.
+ * scores  fp32  [nq][active_blocks], written.
+ * ids     int32 [nq][k], written (as qsa_block_topk).
+ * nq > 4 or active_blocks > QSA_TOPK_MAX_ACTIVE returns QSA_ERR_UNSUPPORTED.
+ * Nothing is allocated. The grid meets at a device-wide counter and a
+ * generation word of library state, so calls on one device must be ordered
+ * (one stream, or streams joined by events). When k >= active_blocks the call
+ * runs the scorer and a fill.
+ * Passage: "#3108 optimize exact QSA block scoring and top-k selection on
+ * gfx12", Summary item 4 (a row kernel for a handful of queries) and the
+ * Microbenchmark & Parity Evidence table (decode scores + top-k per layer).
+ */
+qsa_status qsa_block_select_small(const float *q, const float *kblk, const int8_t *kblk_q8,
+                                  const uint16_t *kscale_f16, int nq, int max_blocks, int active_blocks, int k,
+                                  float *scores, int32_t *ids, cudaStream_t stream);
+
+/*
  * Reads and clears the current device's error word: nonzero when a kernel
  * of this library gave up a bounded wait (its outputs are then invalid).
  * Synchronises `stream`. *code receives the word.

@@ -14,6 +14,7 @@ from .qsa import (  # noqa: F401
     block_scores_q8,
     block_scores_q8_gmax,
     block_select,
+    block_select_small,
     block_select_static,
     block_topk,
     block_topk_gmax,

@@ -1,0 +1,150 @@
+// Block scoring for a handful of queries (decode: nq <= 4) on CUDA cores,
+// one chunk of key rows at a time: shared by the decode scorer and the fused
+// decode select.
+//
+//   score[i][b] = sum_{d<128} s[i][d] * key[b][d],   s[i][d] = ((q0 + q1) + q2) + q3
+//
+// Passages: "#3108 optimize exact QSA block scoring and top-k selection on
+// gfx12", Summary items 1 and 4 (the 4-head block score); "#337 gfx12 QSA
+// select", What (decode with `--kv int8`: int8 keys, one binary16 scale per
+// block).
+//
+// With one to four query rows the scoring is a matrix-vector product: every
+// key byte is used nq times, so the tensor-core tile (128 query rows) would be
+// almost all padding. A key row is split over TPR threads (fp32: 4 threads x
+// 32 values; int8: 2 threads x 64 values); each thread streams its part with
+// 16-byte read-only loads and accumulates one fp32 FMA chain per query
+// against the head-summed queries in shared memory (read as broadcasts), and
+// the TPR partial sums meet by warp shuffles. Rows at or beyond `active` are
+// never read.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "qsa_internal.cuh"
+
+namespace qsa {
+
+// Shared query rows get 4 floats of padding after every 32, so the TPR parts
+// of a row (32 or 64 values apart) read different banks.
+constexpr int DEC_QROW = D + D / 8;
+__device__ __forceinline__ int dec_qidx(int d) { return d + (d >> 5) * 4; }
+
+template <bool kInt8>
+__host__ __device__ constexpr int dec_tpr() { return kInt8 ? 2 : 4; }   // threads per key row
+
+// Head-summed queries into shared memory, zero past nq (the caller syncs).
+template <int NQ, int THREADS>
+__device__ __forceinline__ void dec_build_queries(const float *__restrict__ q, int nq, float (*qs)[DEC_QROW]) {
+    for (int e = threadIdx.x; e < NQ * D; e += THREADS) {
+        const int r = e / D, d = e % D;
+        float v = 0.0f;
+        if (r < nq) {
+            const float *p = q + static_cast<size_t>(r) * (HEADS * D) + d;
+            v = __fadd_rn(__fadd_rn(__fadd_rn(__ldg(p), __ldg(p + D)), __ldg(p + 2 * D)), __ldg(p + 3 * D));
+        }
+        qs[r][dec_qidx(d)] = v;
+    }
+}
+
+// Scores of key rows chunk * ROWS .. + ROWS - 1 (ROWS = THREADS / TPR) for
+// all queries, and, when gmax is given, the key of each of the chunk's
+// 32-block groups' largest score (the chunk's rows are whole groups; their
+// keys meet in gk and one warp per (query, group) takes the maximum). Every
+// thread of the CTA calls this; it ends with the CTA synchronised.
+template <int NQ, bool kInt8, int THREADS>
+__device__ __forceinline__ void dec_score_chunk(const float (*qs)[DEC_QROW], long long chunk,
+                                                const float *__restrict__ kblk, const int8_t *__restrict__ kq8,
+                                                const __half *__restrict__ kscale, int nq, int active,
+                                                float *__restrict__ scores, uint32_t *__restrict__ gmax,
+                                                uint32_t (*gk)[THREADS / dec_tpr<kInt8>()]) {
+    constexpr int TPR = dec_tpr<kInt8>();
+    constexpr int PER = D / TPR;                // values per thread: 64 (int8) or 32 (fp32)
+    constexpr int ROWS = THREADS / TPR;
+    static_assert(ROWS % GROUP_BLOCKS == 0, "a chunk holds whole groups");
+    const long long b = chunk * ROWS + threadIdx.x / TPR;   // key row
+    const int part = static_cast<int>(threadIdx.x % TPR);
+    const bool live = b < active;
+    float acc[NQ];
+#pragma unroll
+    for (int r = 0; r < NQ; ++r) acc[r] = 0.0f;
+    if (live) {
+        if constexpr (!kInt8) {
+            const float4 *row = reinterpret_cast<const float4 *>(kblk + b * D + part * PER);
+            float4 kv[PER / 4];
+#pragma unroll
+            for (int c = 0; c < PER / 4; ++c) kv[c] = __ldg(row + c);
+#pragma unroll
+            for (int c = 0; c < PER / 4; ++c) {
+#pragma unroll
+                for (int r = 0; r < NQ; ++r) {
+                    const float4 qv = *reinterpret_cast<const float4 *>(&qs[r][dec_qidx(part * PER + 4 * c)]);
+                    acc[r] = fmaf(qv.x, kv[c].x, acc[r]);
+                    acc[r] = fmaf(qv.y, kv[c].y, acc[r]);
+                    acc[r] = fmaf(qv.z, kv[c].z, acc[r]);
+                    acc[r] = fmaf(qv.w, kv[c].w, acc[r]);
+                }
+            }
+        } else {
+            const uint4 *row = reinterpret_cast<const uint4 *>(kq8 + b * D + part * PER);
+            uint4 kv[PER / 16];
+#pragma unroll
+            for (int c = 0; c < PER / 16; ++c) kv[c] = __ldg(row + c);
+#pragma unroll
+            for (int c = 0; c < PER / 16; ++c) {
+                const uint32_t w4[4] = {kv[c].x, kv[c].y, kv[c].z, kv[c].w};
+#pragma unroll
+                for (int wi = 0; wi < 4; ++wi) {
+                    float kf[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        kf[e] = static_cast<float>(static_cast<int8_t>((w4[wi] >> (8 * e)) & 0xFFu));
+#pragma unroll
+                    for (int r = 0; r < NQ; ++r) {
+                        const float4 qv =
+                            *reinterpret_cast<const float4 *>(&qs[r][dec_qidx(part * PER + 16 * c + 4 * wi)]);
+                        acc[r] = fmaf(qv.x, kf[0], acc[r]);
+                        acc[r] = fmaf(qv.y, kf[1], acc[r]);
+                        acc[r] = fmaf(qv.z, kf[2], acc[r]);
+                        acc[r] = fmaf(qv.w, kf[3], acc[r]);
+                    }
+                }
+            }
+        }
+    }
+    // The TPR threads of a row are adjacent lanes: add their partial sums.
+#pragma unroll
+    for (int r = 0; r < NQ; ++r) {
+#pragma unroll
+        for (int o = 1; o < TPR; o <<= 1) acc[r] = __fadd_rn(acc[r], __shfl_xor_sync(FULL_MASK, acc[r], o));
+    }
+    if (live && part == 0) {
+        const float scale = kInt8 ? __half2float(kscale[b]) : 1.0f;
+#pragma unroll
+        for (int r = 0; r < NQ; ++r) {
+            if (kInt8) acc[r] = __fmul_rn(acc[r], scale);
+            if (r < nq) scores[static_cast<size_t>(r) * active + b] = acc[r];
+        }
+    }
+    if (gmax != nullptr) {   // uniform
+        constexpr int GROUPS = ROWS / GROUP_BLOCKS;
+        if (part == 0) {
+            const int rl = threadIdx.x / TPR;
+#pragma unroll
+            for (int r = 0; r < NQ; ++r) gk[r][rl] = live ? score_key(acc[r]) : 0u;
+        }
+        __syncthreads();
+        const int ngr = (active + GROUP_BLOCKS - 1) / GROUP_BLOCKS;
+        const int lane = threadIdx.x & 31;
+        for (int w = threadIdx.x >> 5; w < NQ * GROUPS; w += THREADS / 32) {   // warp-uniform
+            const int r = w / GROUPS, gl = w % GROUPS;
+            const uint32_t key = __reduce_max_sync(FULL_MASK, gk[r][gl * GROUP_BLOCKS + lane]);
+            const long long g = chunk * GROUPS + gl;
+            if (lane == 0 && r < nq && g < ngr) gmax[static_cast<size_t>(r) * ngr + g] = key;
+        }
+    }
+    __syncthreads();   // gk may be rewritten by the next chunk
+}
+
+}  // namespace qsa

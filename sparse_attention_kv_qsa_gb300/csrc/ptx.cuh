@@ -127,6 +127,29 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst_smem, const void *src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Release store / acquire load of a global word at GPU scope.
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits (bounded by WAIT_LIMIT_NS) until the word at p differs from `old`,
+// with acquire semantics at GPU scope. Returns false if it gave up.
+__device__ __forceinline__ bool wait_word_changes(const uint32_t *p, uint32_t old) {
+    if (ld_acquire_gpu(p) != old) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (ld_acquire_gpu(p) != old) return true;
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+    }
+}
+
 // Asks the TMA unit to bring [src, src + bytes) into L2 (no destination, no
 // completion to wait for). src 16-byte aligned; bytes % 16 == 0.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {

@@ -187,6 +187,34 @@ qsa_status qsa_block_select_static(const float *q, const float *kblk, int nq, in
     return topk(scores, gm, true, nq, active_blocks, k, ids, stream);
 }
 
+qsa_status qsa_block_select_small(const float *q, const float *kblk, const int8_t *kblk_q8,
+                                  const uint16_t *kscale_f16, int nq, int max_blocks, int active_blocks, int k,
+                                  float *scores, int32_t *ids, cudaStream_t stream) {
+    qsa_status s = check_score_args(q, nq, max_blocks, active_blocks, scores);
+    if (s != QSA_OK) return s;
+    if (k < 1) return QSA_ERR_INVALID;
+    if (nq == 0) return QSA_OK;
+    if (nq > qsa::SMALL_NQ_MAX) return QSA_ERR_UNSUPPORTED;
+    if (ids == nullptr || !aligned16(ids)) return QSA_ERR_INVALID;
+    const bool f32 = kblk != nullptr;
+    const bool i8 = kblk_q8 != nullptr || kscale_f16 != nullptr;
+    if (f32 == i8) return QSA_ERR_INVALID;
+    if (f32 && !aligned16(kblk)) return QSA_ERR_INVALID;
+    if (i8 && (kblk_q8 == nullptr || kscale_f16 == nullptr || !aligned16(kblk_q8) ||
+               (reinterpret_cast<uintptr_t>(kscale_f16) & 1u) != 0))
+        return QSA_ERR_INVALID;
+    if (active_blocks > QSA_TOPK_MAX_ACTIVE) return QSA_ERR_UNSUPPORTED;
+    if (active_blocks == 0) return from_cuda(qsa::launch_topk_all(nq, 0, k, ids, stream));
+    if (k >= active_blocks) {
+        cudaError_t e = qsa::launch_scores_rows(q, kblk, kblk_q8, kscale_f16, nq, active_blocks, scores, nullptr,
+                                                stream);
+        if (e == cudaSuccess) e = qsa::launch_topk_all(nq, active_blocks, k, ids, stream);
+        return from_cuda(e);
+    }
+    return from_cuda(qsa::launch_select_decode(q, kblk, kblk_q8, kscale_f16, nq, active_blocks, k, scores, ids,
+                                               stream));
+}
+
 qsa_status qsa_get_device_error(uint32_t *code, cudaStream_t stream) {
     if (code == nullptr) return QSA_ERR_INVALID;
     *code = 0;

@@ -50,6 +50,12 @@ cudaError_t launch_scores_rows(const float *q, const float *kblk, const int8_t *
 cudaError_t launch_topk(const float *scores, const uint32_t *gmax, int nq, int active, int k, int32_t *ids,
                         cudaStream_t stream);
 
+// Scores and top-k for nq <= 4 in one cooperative launch (k < active):
+// scores written, group maxima in a fixed device array; calls on one device
+// must be ordered (the launch shares that array and two sync words).
+cudaError_t launch_select_decode(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,
+                                 int nq, int active, int k, float *scores, int32_t *ids, cudaStream_t stream);
+
 // ids[i][j] = j < active ? j : -1 (the k >= active case).
 cudaError_t launch_topk_all(int nq, int active, int k, int32_t *ids, cudaStream_t stream);
 

@@ -41,6 +41,7 @@
 //  scanned by warp 0 alone (two block barriers per digit).
 // No CTA ever waits on another: no cluster, no grid-wide synchronisation, no
 // global scratch.
+#include "decode_rows.cuh"
 #include "ptx.cuh"
 #include "qsa_internal.cuh"
 
@@ -90,6 +91,34 @@ __device__ __forceinline__ uint32_t float_bits_to_key(uint32_t bits) {
     const float f = fmaxf(__fadd_rn(__uint_as_float(bits), 0.0f), -INFINITY);
     const uint32_t u = __float_as_uint(f);
     return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
+}
+
+// Score and group-maximum loads. The top-k kernel reads data that no thread
+// of its grid writes, through the read-only path (kCoherent false); the fused
+// decode kernel reads scores its own grid wrote before a grid-wide release,
+// so it uses coherent global loads (kCoherent true).
+template <bool kCoherent>
+__device__ __forceinline__ uint32_t ld_word(const uint32_t *p) {
+    if constexpr (kCoherent) {
+        uint32_t v;
+        asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        return v;
+    } else {
+        return __ldg(p);
+    }
+}
+template <bool kCoherent>
+__device__ __forceinline__ uint4 ld_quad(const uint4 *p) {
+    if constexpr (kCoherent) {
+        uint4 v;
+        asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(p)
+                     : "memory");
+        return v;
+    } else {
+        return __ldg(p);
+    }
 }
 
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, int lane) {
@@ -185,10 +214,10 @@ __device__ __forceinline__ void warp_select_2048(uint32_t target, RowShared &sh,
 // fp32 bits), each from some thread; every thread must call it. The aligned
 // body moves as 16-byte read-only loads, UNROLL in flight per thread; the
 // <= 3 ragged scores at either end as single words.
-template <typename Fn>
+template <bool kCoherent, typename Fn>
 __device__ __forceinline__ void stream_row(const uint32_t *g, int n, int head, int nvec, int tid, Fn &&fn) {
-    for (int i = tid; i < head; i += ROW_THREADS) fn(i, __ldg(g + i));
-    for (int i = head + 4 * nvec + tid; i < n; i += ROW_THREADS) fn(i, __ldg(g + i));
+    for (int i = tid; i < head; i += ROW_THREADS) fn(i, ld_word<kCoherent>(g + i));
+    for (int i = head + 4 * nvec + tid; i < n; i += ROW_THREADS) fn(i, ld_word<kCoherent>(g + i));
     const uint4 *g4 = reinterpret_cast<const uint4 *>(g + head);
 #pragma unroll 1
     for (int v0 = 0; v0 < nvec; v0 += ROW_THREADS * UNROLL) {
@@ -196,7 +225,7 @@ __device__ __forceinline__ void stream_row(const uint32_t *g, int n, int head, i
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int v = v0 + u * ROW_THREADS + tid;
-            x[u] = v < nvec ? __ldg(g4 + v) : make_uint4(0u, 0u, 0u, 0u);
+            x[u] = v < nvec ? ld_quad<kCoherent>(g4 + v) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
@@ -213,10 +242,12 @@ __device__ __forceinline__ void stream_row(const uint32_t *g, int n, int head, i
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(ROW_THREADS, 2)
-    topk_row_kernel(const float *__restrict__ scores, const uint32_t *__restrict__ gmax, int active, int k,
-                    int32_t *__restrict__ ids) {
-    const size_t row = blockIdx.x;
+// One row's exact top-k by one 512-thread CTA (the whole of topk_row_kernel;
+// also the second phase of the fused decode kernel). Dynamic shared memory:
+// row_smem_bytes(active).
+template <bool kCoherent>
+__device__ __forceinline__ void topk_row(const float *__restrict__ scores, const uint32_t *__restrict__ gmax,
+                                         int active, int k, int32_t *__restrict__ ids, size_t row) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = active;
     const int nwords = (n + 31) >> 5;
@@ -266,12 +297,12 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         const uint32_t *gm = gmax + row * static_cast<size_t>(ngr);
         sx[0] = make_uint4(0u, 0u, 0u, 0u);
         if ((ngr & 3) == 0) {
-            if (4 * tid < ngr) sx[0] = __ldg(reinterpret_cast<const uint4 *>(gm) + tid);
+            if (4 * tid < ngr) sx[0] = ld_quad<kCoherent>(reinterpret_cast<const uint4 *>(gm) + tid);
         } else {
-            if (4 * tid + 0 < ngr) sx[0].x = __ldg(gm + 4 * tid + 0);
-            if (4 * tid + 1 < ngr) sx[0].y = __ldg(gm + 4 * tid + 1);
-            if (4 * tid + 2 < ngr) sx[0].z = __ldg(gm + 4 * tid + 2);
-            if (4 * tid + 3 < ngr) sx[0].w = __ldg(gm + 4 * tid + 3);
+            if (4 * tid + 0 < ngr) sx[0].x = ld_word<kCoherent>(gm + 4 * tid + 0);
+            if (4 * tid + 1 < ngr) sx[0].y = ld_word<kCoherent>(gm + 4 * tid + 1);
+            if (4 * tid + 2 < ngr) sx[0].z = ld_word<kCoherent>(gm + 4 * tid + 2);
+            if (4 * tid + 3 < ngr) sx[0].w = ld_word<kCoherent>(gm + 4 * tid + 3);
         }
 #pragma unroll
         for (int u = 1; u < SAMPLE_REGS; ++u) sx[u] = make_uint4(0u, 0u, 0u, 0u);
@@ -279,7 +310,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
 #pragma unroll
         for (int u = 0; u < SAMPLE_REGS; ++u) {
             const int s = tid + u * ROW_THREADS;
-            sx[u] = try_list && s < nsv ? __ldg(g4 + s * SAMPLE_STRIDE + SAMPLE_STRIDE / 2)
+            sx[u] = try_list && s < nsv ? ld_quad<kCoherent>(g4 + s * SAMPLE_STRIDE + SAMPLE_STRIDE / 2)
                                         : make_uint4(0u, 0u, 0u, 0u);
         }
     }
@@ -477,7 +508,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
                         uint4 y[GU];
 #pragma unroll
                         for (int u = 0; u < GU; ++u)
-                            y[u] = base[u] + 4 <= n ? __ldg(reinterpret_cast<const uint4 *>(g + base[u]))
+                            y[u] = base[u] + 4 <= n ? ld_quad<kCoherent>(reinterpret_cast<const uint4 *>(g + base[u]))
                                                     : make_uint4(QNAN_BITS, QNAN_BITS, QNAN_BITS, QNAN_BITS);
 #pragma unroll
                         for (int u = 0; u < GU; ++u) hits |= hit_bits(y[u], u);
@@ -486,7 +517,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
                         for (int u = 0; u < GU; ++u) {
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
-                                if (base[u] + c < n && __uint_as_float(__ldg(g + base[u] + c)) >= ft)
+                                if (base[u] + c < n && __uint_as_float(ld_word<kCoherent>(g + base[u] + c)) >= ft)
                                     hits |= 1u << (4 * u + c);
                         }
                     }
@@ -498,7 +529,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
                 }
             } else {
                 auto list_scalar = [&](int i) {
-                    if (__uint_as_float(__ldg(g + i)) >= ft) {
+                    if (__uint_as_float(ld_word<kCoherent>(g + i)) >= ft) {
                         const uint32_t slot = atomicAdd(&sh.cand_n, 1u);
                         if (slot < static_cast<uint32_t>(CAND_MAX)) {
                             sh.cand_idx[slot] = static_cast<uint32_t>(i);
@@ -516,7 +547,8 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
                     for (int u = 0; u < LIST_VEC; ++u) {
                         const int v = v0 + u * ROW_THREADS + tid;
                         // Past the end: NaN, which no comparison lists.
-                        x[u] = v < nvec ? __ldg(g4 + v) : make_uint4(QNAN_BITS, QNAN_BITS, QNAN_BITS, QNAN_BITS);
+                        x[u] = v < nvec ? ld_quad<kCoherent>(g4 + v)
+                                        : make_uint4(QNAN_BITS, QNAN_BITS, QNAN_BITS, QNAN_BITS);
                     }
                 };
                 load_step(0);
@@ -586,7 +618,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         done = sh.cand_n == kk;  // the whole list is the top-k
     } else {
         // Pass A: the 11-bit leading-digit histogram of the whole row.
-        stream_row(g, n, head, nvec, tid, [&](int, uint32_t bits) {
+        stream_row<kCoherent>(g, n, head, nvec, tid, [&](int, uint32_t bits) {
             atomicAdd(&sh.histA[float_bits_to_key(bits) >> 21], 1u);
         });
         if (tid < HIST_A / GROUP) {
@@ -610,7 +642,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
 
         // Pass B: keys above the leading bin are selected; keys inside it are
         // listed as candidates (or all selected, when the bin is taken whole).
-        stream_row(g, n, head, nvec, tid, [&](int i, uint32_t bits) {
+        stream_row<kCoherent>(g, n, head, nvec, tid, [&](int i, uint32_t bits) {
             const uint32_t key = float_bits_to_key(bits);
             const uint32_t d = key >> 21;
             if (d < T1) return;
@@ -641,7 +673,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
             }
             __syncthreads();
         } else {
-            stream_row(g, n, head, nvec, tid, [&](int, uint32_t bits) {
+            stream_row<kCoherent>(g, n, head, nvec, tid, [&](int, uint32_t bits) {
                 const uint32_t key = float_bits_to_key(bits);
                 if ((key & mask) == prefix) atomicAdd(&sh.histR[(key >> shift) & dmask], 1u);
             });
@@ -670,7 +702,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
             }
             __syncthreads();
         } else {
-            stream_row(g, n, head, nvec, tid, [&](int i, uint32_t bits) {
+            stream_row<kCoherent>(g, n, head, nvec, tid, [&](int i, uint32_t bits) {
                 const uint32_t key = float_bits_to_key(bits);
                 if ((key >> 21) != T1) return;
                 const uint32_t km = key & mask;
@@ -739,6 +771,56 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
     }
 }
 
+__global__ void __launch_bounds__(ROW_THREADS, 2)
+    topk_row_kernel(const float *__restrict__ scores, const uint32_t *__restrict__ gmax, int active, int k,
+                    int32_t *__restrict__ ids) {
+    topk_row<false>(scores, gmax, active, k, ids, blockIdx.x);
+}
+
+// Fused decode select (nq <= 4): one cooperative launch scores every key row
+// (and the group maxima) across the whole grid, then its first nq CTAs each
+// take one row's top-k. The CTAs release their scores through an arrival
+// counter; the last to arrive resets the counter and advances a generation
+// word that the top-k CTAs wait on (bounded; a cooperative launch keeps every
+// CTA resident, so all of them arrive). Each CTA reads the generation before
+// it arrives, and it cannot advance before every CTA has arrived, so all of
+// them see the same value; the words need no clearing between launches. The
+// group maxima live in a fixed device array, so the call allocates nothing.
+// Launches of this kernel on one device therefore run one at a time.
+__device__ uint32_t g_decode_sync[2];   // arrivals, generation
+static __device__ __align__(256) uint32_t g_decode_gmax[SMALL_NQ_MAX * (MAX_ACTIVE / GROUP_BLOCKS)];
+
+template <int NQ, bool kInt8>
+__global__ void __launch_bounds__(ROW_THREADS, 2)
+    select_decode_kernel(const float *__restrict__ q, const float *__restrict__ kblk,
+                         const int8_t *__restrict__ kq8, const __half *__restrict__ kscale, int nq, int active,
+                         int k, float *__restrict__ scores, int32_t *__restrict__ ids) {
+    constexpr int ROWS = ROW_THREADS / dec_tpr<kInt8>();
+    __shared__ __align__(16) float qs[NQ][DEC_QROW];   // head-summed queries, zero past nq
+    __shared__ uint32_t gk[NQ][ROWS];
+    grid_dependency_wait();   // q and the keys may come from the previous grid
+    grid_launch_dependents();
+    uint32_t gen = 0u;
+    if (threadIdx.x == 0) gen = ld_acquire_gpu(&g_decode_sync[1]);
+    dec_build_queries<NQ, ROW_THREADS>(q, nq, qs);
+    __syncthreads();
+    const long long nchunks = (static_cast<long long>(active) + ROWS - 1) / ROWS;
+    for (long long c = blockIdx.x; c < nchunks; c += gridDim.x)
+        dec_score_chunk<NQ, kInt8, ROW_THREADS>(qs, c, kblk, kq8, kscale, nq, active, scores, g_decode_gmax, gk);
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&g_decode_sync[0], 1u) == gridDim.x - 1) {
+            atomicExch(&g_decode_sync[0], 0u);
+            __threadfence();
+            st_release_gpu(&g_decode_sync[1], gen + 1u);
+        }
+    }
+    if (blockIdx.x >= static_cast<unsigned>(nq)) return;   // the whole CTA
+    if (threadIdx.x == 0 && !wait_word_changes(&g_decode_sync[1], gen)) atomicOr(&g_topk_error, 2u);
+    __syncthreads();
+    topk_row<true>(scores, g_decode_gmax, active, k, ids, blockIdx.x);
+}
+
 __global__ void topk_all_kernel(int active, int k, size_t total, int32_t *__restrict__ ids) {
     for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < total;
          t += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -772,6 +854,62 @@ cudaError_t launch_topk(const float *scores, const uint32_t *gmax, int nq, int a
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, topk_row_kernel, scores, gmax, active, k, ids);
+}
+
+template <int NQ, bool kInt8>
+cudaError_t launch_decode_nq(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale, int nq,
+                             int active, int k, float *scores, int32_t *ids, cudaStream_t stream) {
+    auto kernel = select_decode_kernel<NQ, kInt8>;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(row_smem_bytes(MAX_ACTIVE)));
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    const size_t smem = row_smem_bytes(active);
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, ROW_THREADS, smem);
+    if (e != cudaSuccess) return e;
+    constexpr int ROWS = ROW_THREADS / dec_tpr<kInt8>();
+    const long long nchunks = (static_cast<long long>(active) + ROWS - 1) / ROWS;
+    long long grid = static_cast<long long>(per_sm) * device_sm_count();   // all resident at once
+    if (grid > nchunks) grid = nchunks;
+    if (grid < nq) grid = nq;
+    if (per_sm < 1 || grid > static_cast<long long>(per_sm) * device_sm_count()) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(ROW_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, q, kblk, kq8, reinterpret_cast<const __half *>(kscale), nq, active, k,
+                              scores, ids);
+}
+
+cudaError_t launch_select_decode(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,
+                                 int nq, int active, int k, float *scores, int32_t *ids, cudaStream_t stream) {
+    if (active > MAX_ACTIVE || k >= active || nq < 1 || nq > SMALL_NQ_MAX) return cudaErrorInvalidValue;
+    const bool i8 = kq8 != nullptr;
+    switch (nq) {
+        case 1:
+            return i8 ? launch_decode_nq<1, true>(q, kblk, kq8, kscale, nq, active, k, scores, ids, stream)
+                      : launch_decode_nq<1, false>(q, kblk, kq8, kscale, nq, active, k, scores, ids, stream);
+        case 2:
+            return i8 ? launch_decode_nq<2, true>(q, kblk, kq8, kscale, nq, active, k, scores, ids, stream)
+                      : launch_decode_nq<2, false>(q, kblk, kq8, kscale, nq, active, k, scores, ids, stream);
+        default:
+            return i8 ? launch_decode_nq<4, true>(q, kblk, kq8, kscale, nq, active, k, scores, ids, stream)
+                      : launch_decode_nq<4, false>(q, kblk, kq8, kscale, nq, active, k, scores, ids, stream);
+    }
 }
 
 cudaError_t launch_topk_all(int nq, int active, int k, int32_t *ids, cudaStream_t stream) {

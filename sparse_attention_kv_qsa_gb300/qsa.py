@@ -25,7 +25,7 @@ QSA_OK, QSA_ERR_INVALID, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
 
 EXPORTED = ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
             "qsa_block_scores_gmax", "qsa_block_scores_q8_gmax", "qsa_block_group_max", "qsa_block_topk_gmax",
-            "qsa_block_select_static", "qsa_get_device_error", "qsa_status_string")
+            "qsa_block_select_static", "qsa_block_select_small", "qsa_get_device_error", "qsa_status_string")
 
 
 class QSAError(RuntimeError):
@@ -60,12 +60,14 @@ def lib() -> ctypes.CDLL:
         L.qsa_block_topk_gmax.argtypes = [vp, vp, i, i, i, vp, vp]
         L.qsa_block_group_max.argtypes = [vp, i, i, vp, vp]
         L.qsa_block_select_static.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
+        L.qsa_block_select_small.argtypes = [vp, vp, vp, vp, i, i, i, i, vp, vp, vp]
         L.qsa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
         L.qsa_status_string.argtypes = [i]
         L.qsa_status_string.restype = ctypes.c_char_p
         for f in ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
                   "qsa_block_scores_gmax", "qsa_block_scores_q8_gmax", "qsa_block_topk_gmax",
-                  "qsa_block_group_max", "qsa_block_select_static", "qsa_get_device_error"):
+                  "qsa_block_group_max", "qsa_block_select_static", "qsa_block_select_small",
+                  "qsa_get_device_error"):
             getattr(L, f).restype = i
         _lib = L
     return _lib
@@ -292,6 +294,34 @@ def block_select_static(q: torch.Tensor, kblk: torch.Tensor, active_blocks: int,
             raise ValueError(f"ids_out must have shape {(nq, k)}")
     _check(lib().qsa_block_select_static(_ptr(q), _ptr(kblk), nq, kblk.shape[0], active_blocks, k, _ptr(scores_out),
                                          _ptr(ids_out), _stream(q)), "qsa_block_select_static")
+    return scores_out, ids_out
+
+
+def block_select_small(q: torch.Tensor, active_blocks: int, k: int, kblk: torch.Tensor | None = None,
+                       kblk_q8: torch.Tensor | None = None, kscale_f16: torch.Tensor | None = None,
+                       scores_out: torch.Tensor | None = None, ids_out: torch.Tensor | None = None):
+    """``qsa_block_select_small``: ``(scores, ids)`` for 1..4 queries in one
+    cooperative launch (fp32 keys, or int8 keys with binary16 scales)."""
+    _check_q(q)
+    if kblk is not None:
+        _need(kblk, "kblk", torch.float32, 2)
+        max_blocks = kblk.shape[0]
+    else:
+        _need(kblk_q8, "kblk_q8", torch.int8, 2)
+        if kscale_f16 is None or not kscale_f16.is_cuda or kscale_f16.dim() != 1:
+            raise ValueError("kscale_f16 must be a 1-d CUDA tensor of binary16 values")
+        max_blocks = kblk_q8.shape[0]
+    nq = q.shape[0]
+    scores_out = _scores_out(q, active_blocks, scores_out)
+    if ids_out is None:
+        ids_out = torch.empty((nq, k), dtype=torch.int32, device=q.device)
+    else:
+        _need(ids_out, "ids_out", torch.int32, 2)
+        if tuple(ids_out.shape) != (nq, k):
+            raise ValueError(f"ids_out must have shape {(nq, k)}")
+    _check(lib().qsa_block_select_small(_ptr(q), _ptr(kblk), _ptr(kblk_q8), _ptr(kscale_f16), nq, max_blocks,
+                                        active_blocks, k, _ptr(scores_out), _ptr(ids_out), _stream(q)),
+           "qsa_block_select_small")
     return scores_out, ids_out
 
 
