@@ -50,8 +50,9 @@ class Oracle:
         L.qsa_oracle_scores_q8.argtypes = [vp, vp, vp, lg, lg, vp, i]
         L.qsa_oracle_topk_f64.argtypes = [vp, lg, lg, lg, vp, i]
         L.qsa_oracle_topk_f32.argtypes = [vp, lg, lg, lg, vp, i]
+        L.qsa_oracle_sparse_attn.argtypes = [vp, vp, vp, vp, vp, lg, vp, lg, lg, vp, i]
         for f in ("qsa_oracle_scores", "qsa_oracle_scores_q8", "qsa_oracle_topk_f64",
-                  "qsa_oracle_topk_f32"):
+                  "qsa_oracle_topk_f32", "qsa_oracle_sparse_attn"):
             getattr(L, f).restype = None
 
     def default_threads(self) -> int:
@@ -123,6 +124,25 @@ class Oracle:
         keys = cls.score_keys(scores)
         starts = np.arange(0, keys.shape[1], group)
         return np.maximum.reduceat(keys, starts, axis=1).astype(np.uint32)
+
+    def sparse_attn(self, q: np.ndarray, kq: np.ndarray, ks: np.ndarray, vq: np.ndarray, vs: np.ndarray,
+                    ids: np.ndarray, nthreads: int = 0) -> np.ndarray:
+        """FP64 attention of each query's 4 heads over the cells of its
+        selected blocks ``[nq, 4, 128]`` (int8 K/V cells ``[ncells, 128]``,
+        binary16 scales ``[ncells]`` as uint16, ids ``[nq, k]``)."""
+        q = self._c(q, np.float32)
+        kq, vq = self._c(kq, np.int8), self._c(vq, np.int8)
+        ks, vs = self._c(ks, np.uint16), self._c(vs, np.uint16)
+        ids = self._c(ids, np.int32)
+        nq, k = ids.shape
+        ncells = kq.shape[0]
+        assert q.shape == (nq, H, D) and kq.shape == (ncells, D) and vq.shape == (ncells, D)
+        assert ks.shape == (ncells,) and vs.shape == (ncells,)
+        out = np.empty((nq, H, D), dtype=np.float64)
+        self.lib.qsa_oracle_sparse_attn(q.ctypes.data, kq.ctypes.data, ks.ctypes.data, vq.ctypes.data,
+                                        vs.ctypes.data, ncells, ids.ctypes.data, nq, k, out.ctypes.data,
+                                        nthreads)
+        return out
 
     def select(self, q, kblk, active: int, k: int, nthreads: int = 0):
         """Scores then ids: ``(S[nq, active] fp64, ids[nq, k])``."""

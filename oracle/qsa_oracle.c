@@ -211,3 +211,87 @@ void qsa_oracle_topk_f32(const float *scores, long nq, long active, long k, int3
     topk_ctx c = {NULL, scores, active, k, ids};
     for_each_row(topk_row, &c, nq, nthreads);
 }
+
+/* ---- sparse attention over the selected blocks ------------------------ */
+/*
+ * Passages: "#3224 [Engine] perf(hip): tune RDNA4 QSA prompt WMMA path
+ * (STRATA_HIP_WMMA stays opt-in)", Summary and Evidence section 2 (the QSA
+ * attention reads int8 K and V cells, each with a binary16 scale, and is
+ * gated against an FP64 host reference); "#3102 perf(hip): enable wave32 QSA
+ * decode attention and MMVQ row reuse on gfx12", item D5 (decode attention
+ * runs over the KV cells in chunks whose partial results are merged in the
+ * chunks' sequential order).
+ *
+ * The pages name the kernels but print no formula; the readings taken:
+ *  - query i attends the cells of the blocks listed in ids[i][0..k): block b
+ *    holds cells 4b .. 4b+3 (those below ncells); a negative id, or one at or
+ *    past the last block, is padding and contributes nothing; a listed block
+ *    contributes once per listing;
+ *  - cell c's key and value are kq[c][d] * ks[c] and vq[c][d] * vs[c] (int8
+ *    times one IEEE binary16 scale per cell; both products exact in double);
+ *  - the 4 query heads share the cells, as they share the block keys:
+ *    logit[h][c] = (sum_d q[i][h][d] * key[c][d]) / sqrt(128);
+ *  - out[i][h][d] = sum_c w[h][c] * value[c][d] with w[h][.] the softmax of
+ *    logit[h][.] over the attended cells (the largest logit is subtracted
+ *    before exponentiating, which leaves w unchanged);
+ *  - a query with no attended cell gets out = 0.
+ * Each product of a float with a key element is exact in double; the sums
+ * run in the cells' listing order, then cell order within a block.
+ */
+typedef struct {
+    const float *q;
+    const int8_t *kq, *vq;
+    const uint16_t *ks, *vs;
+    long ncells, k;
+    const int32_t *ids;
+    double *out;
+} attn_ctx;
+
+static void attn_row(void *vctx, long i) {
+    const attn_ctx *c = (const attn_ctx *)vctx;
+    const long nblocks = (c->ncells + 3) / 4;
+    double *o = c->out + (size_t)i * QSA_H * QSA_D;
+    for (int e = 0; e < QSA_H * QSA_D; ++e) o[e] = 0.0;
+    long *cells = (long *)malloc(sizeof(long) * (size_t)(4 * (c->k > 0 ? c->k : 1)));
+    long n = 0;
+    for (long j = 0; j < c->k; ++j) {
+        const long b = c->ids[(size_t)i * (size_t)c->k + (size_t)j];
+        if (b < 0 || b >= nblocks) continue;
+        for (long t = 0; t < 4; ++t)
+            if (4 * b + t < c->ncells) cells[n++] = 4 * b + t;
+    }
+    double *w = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    const double temperature = 1.0 / sqrt((double)QSA_D);
+    for (int h = 0; h < QSA_H && n > 0; ++h) {
+        const float *qh = c->q + ((size_t)i * QSA_H + (size_t)h) * QSA_D;
+        double top = -INFINITY;
+        for (long t = 0; t < n; ++t) {
+            const int8_t *kc = c->kq + (size_t)cells[t] * QSA_D;
+            const double scale = qsa_oracle_half_to_double(c->ks[cells[t]]);
+            double dot = 0.0;
+            for (int d = 0; d < QSA_D; ++d) dot += (double)qh[d] * ((double)kc[d] * scale);
+            w[t] = dot * temperature;
+            if (w[t] > top) top = w[t];
+        }
+        double total = 0.0;
+        for (long t = 0; t < n; ++t) {
+            w[t] = exp(w[t] - top);
+            total += w[t];
+        }
+        for (long t = 0; t < n; ++t) {
+            const int8_t *vc = c->vq + (size_t)cells[t] * QSA_D;
+            const double scale = qsa_oracle_half_to_double(c->vs[cells[t]]);
+            const double p = w[t] / total;
+            for (int d = 0; d < QSA_D; ++d) o[h * QSA_D + d] += p * ((double)vc[d] * scale);
+        }
+    }
+    free(w);
+    free(cells);
+}
+
+void qsa_oracle_sparse_attn(const float *q, const int8_t *kq, const uint16_t *ks, const int8_t *vq,
+                            const uint16_t *vs, long ncells, const int32_t *ids, long nq, long k,
+                            double *out, int nthreads) {
+    attn_ctx c = {q, kq, vq, ks, vs, ncells, k, ids, out};
+    for_each_row(attn_row, &c, nq, nthreads);
+}

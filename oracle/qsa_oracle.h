@@ -10,6 +10,8 @@
  *   S       double [nq][active]      (scores, written)
  *   scores  float  [nq][active]      (given fp32 scores, read)
  *   ids     int32  [nq][k]           (written: ascending ids, -1 padding)
+ *   attention: kq, vq int8 [ncells][128], ks, vs uint16 (binary16) [ncells],
+ *              ids int32 [nq][k] (read), out double [nq][4][128] (written)
  * nthreads <= 0 uses every online core.
  */
 #ifndef QSA_ORACLE_H
@@ -31,6 +33,9 @@ void qsa_oracle_topk_f64(const double *S, long nq, long active, long k, int32_t 
                          int nthreads);
 void qsa_oracle_topk_f32(const float *scores, long nq, long active, long k, int32_t *ids,
                          int nthreads);
+void qsa_oracle_sparse_attn(const float *q, const int8_t *kq, const uint16_t *ks, const int8_t *vq,
+                            const uint16_t *vs, long ncells, const int32_t *ids, long nq, long k,
+                            double *out, int nthreads);
 
 #ifdef __cplusplus
 }

@@ -306,8 +306,126 @@ def pin_group_max_keys(o) -> None:
         assert np.array_equal(gm[:, g], o.score_keys(part[np.arange(3), top]))
 
 
+# ---- attention over the selected blocks ------------------------------------
+# The definition pinned: query i's 4 heads attend the cells of its listed
+# blocks (block b = cells 4b .. 4b+3 below ncells; negative or past-the-end
+# ids are padding), key/value = int8 x one binary16 scale per cell, logits
+# scaled by 1/sqrt(128), softmax per head, output the weighted sum of values
+# ("#3224 [Engine] perf(hip): tune RDNA4 QSA prompt WMMA path", Summary and
+# Evidence section 2; "#3102 perf(hip): enable wave32 QSA decode attention and
+# MMVQ row reuse on gfx12", item D5).
+
+def _half_bits(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float16).view(np.uint16)
+
+
+def _attn_case(ncells: int, seed: int):
+    r = _rng(seed)
+    kq = r.integers(-127, 128, (ncells, D)).astype(np.int8)
+    vq = r.integers(-127, 128, (ncells, D)).astype(np.int8)
+    ks = _half_bits(r.uniform(0.002, 0.02, ncells))
+    vs = _half_bits(r.uniform(0.01, 0.1, ncells))
+    return kq, vq, ks, vs
+
+
+def pin_attn_single_cell(o) -> None:
+    """One attended cell: every head's output is that cell's value exactly
+    (weight 1), whatever the query."""
+    kq, vq, ks, vs = _attn_case(9, 101)          # block 2 holds only cell 8
+    q = _rng(102).standard_normal((3, H, D)).astype(np.float32)
+    ids = np.array([[2, -1], [-1, 2], [2, 7]], dtype=np.int32)   # 7 is past the last block
+    out = o.sparse_attn(q, kq, ks, vq, vs, ids)
+    value = vq[8].astype(np.float64) * float(np.uint16(vs[8]).view(np.float16))
+    for i in range(3):
+        for h in range(H):
+            assert np.array_equal(out[i, h], value), (i, h)
+
+
+def pin_attn_uniform_weights(o) -> None:
+    """Zero keys give equal logits, so each head's output is the plain mean
+    of the attended values (numpy, cell by cell)."""
+    _, vq, ks, vs = _attn_case(16, 103)
+    kq = np.zeros((16, D), dtype=np.int8)
+    q = _rng(104).standard_normal((1, H, D)).astype(np.float32)
+    ids = np.array([[3, 0, 1]], dtype=np.int32)
+    out = o.sparse_attn(q, kq, ks, vq, vs, ids)
+    cells = [12, 13, 14, 15, 0, 1, 2, 3, 4, 5, 6, 7]
+    vals = np.stack([vq[c].astype(np.float64) * float(np.uint16(vs[c]).view(np.float16)) for c in cells])
+    want = vals.mean(axis=0)
+    for h in range(H):
+        assert np.allclose(out[0, h], want, rtol=0, atol=1e-14 * np.abs(vals).max()), h
+
+
+def pin_attn_two_cells_logistic(o) -> None:
+    """Two cells whose logits differ by a known amount: the weights are the
+    logistic function of that difference, which fixes the 1/sqrt(128)
+    temperature and both scales. Head h has its own query scale."""
+    kq = np.zeros((4, D), dtype=np.int8)
+    vq = np.zeros((4, D), dtype=np.int8)
+    kq[0, 5], kq[1, 5] = 3, -2                   # key elements on d = 5
+    vq[0, :], vq[1, :] = 7, -5
+    ks = _half_bits([0.5, 0.5, 0.5, 0.5])
+    vs = _half_bits([0.25, 0.125, 1.0, 1.0])
+    ncells = 2                                   # block 0 holds cells 0 and 1 only
+    q = np.zeros((1, H, D), dtype=np.float32)
+    for h in range(H):
+        q[0, h, 5] = 1.5 * (h + 1)
+    out = o.sparse_attn(q, kq[:ncells], ks[:ncells], vq[:ncells], vs[:ncells], np.array([[0]], dtype=np.int32))
+    import math
+    for h in range(H):
+        a = 1.5 * (h + 1)
+        l0, l1 = a * 3 * 0.5 / math.sqrt(128.0), a * (-2) * 0.5 / math.sqrt(128.0)
+        w0 = 1.0 / (1.0 + math.exp(l1 - l0))
+        want = w0 * 7 * 0.25 + (1.0 - w0) * (-5) * 0.125
+        assert abs(out[0, h, 0] - want) <= 1e-15 * 2, (h, out[0, h, 0], want)
+        assert np.all(out[0, h] == out[0, h, 0])
+
+
+def pin_attn_python_loops(o) -> None:
+    """A small ragged case against a pure-Python FP64 restatement that sums
+    in the reverse order and does not subtract the maximum (duplicated and
+    padded ids, a partial last block)."""
+    import math
+    ncells = 23                                   # blocks 0..5, block 5 holds cells 20..22
+    kq, vq, ks, vs = _attn_case(ncells, 105)
+    q = _rng(106).standard_normal((3, H, D)).astype(np.float32)
+    ids = np.array([[5, 1, -1, 3], [0, 0, 2, -1], [-1, -1, -1, 4]], dtype=np.int32)
+    out = o.sparse_attn(q, kq, ks, vq, vs, ids)
+    half = lambda u: float(np.uint16(u).view(np.float16))
+    for i in range(ids.shape[0]):
+        cells = [4 * int(b) + t for b in ids[i] if b >= 0 for t in range(4) if 4 * int(b) + t < ncells]
+        for h in range(H):
+            qh = [float(x) for x in q[i, h]]
+            lg = []
+            for c in reversed(cells):
+                kc = [int(x) * half(ks[c]) for x in kq[c]]
+                lg.append((c, sum(qh[d] * kc[d] for d in reversed(range(D))) / math.sqrt(D)))
+            e = [(c, math.exp(x)) for c, x in lg]
+            tot = sum(x for _, x in e)
+            want = [sum(x / tot * int(vq[c, d]) * half(vs[c]) for c, x in e) for d in range(D)]
+            scale = max(abs(w) for w in want) + 1e-300
+            assert np.allclose(out[i, h], want, rtol=0, atol=1e-12 * scale), (i, h)
+
+
+def pin_attn_padding_and_order(o) -> None:
+    """No attended cell gives zeros; the order of the listed ids and extra
+    padding do not change the result beyond rounding."""
+    kq, vq, ks, vs = _attn_case(40, 107)
+    q = _rng(108).standard_normal((2, H, D)).astype(np.float32)
+    empty = o.sparse_attn(q, kq, ks, vq, vs, np.array([[-1, -1], [10, 99]], dtype=np.int32))
+    assert np.array_equal(empty, np.zeros_like(empty))
+    a = o.sparse_attn(q, kq, ks, vq, vs, np.array([[1, 4, 7, -1], [9, 0, 2, 3]], dtype=np.int32))
+    b = o.sparse_attn(q, kq, ks, vq, vs, np.array([[7, -1, 1, 4], [3, 2, 0, 9]], dtype=np.int32))
+    assert np.allclose(a, b, rtol=0, atol=1e-13 * np.abs(a).max())
+
+
 ALL_PINS = [
     pin_brute_force_topk,
+    pin_attn_single_cell,
+    pin_attn_uniform_weights,
+    pin_attn_two_cells_logistic,
+    pin_attn_python_loops,
+    pin_attn_padding_and_order,
     pin_closed_form_onehot,
     pin_all_ties_lower_id,
     pin_integer_exact,

@@ -30,6 +30,14 @@ MUTANTS = {
     "half_subnormal": ("ldexp((double)m, -24)", "ldexp((double)m, -25)"),
     "scale_dropped": ("((double)kb[d] * scale)", "((double)kb[d])"),
     "float_key_trunc": ("(double)c->S32[(size_t)i * n + b]", "(double)(int)c->S32[(size_t)i * n + b]"),
+    "attn_no_temperature": ("w[t] = dot * temperature;", "w[t] = dot;"),
+    "attn_cell_index": ("if (4 * b + t < c->ncells) cells[n++] = 4 * b + t;",
+                        "if (4 * b + t < c->ncells) cells[n++] = 4 * b;"),
+    "attn_k_scale_dropped": ("((double)kc[d] * scale)", "((double)kc[d])"),
+    "attn_v_scale_dropped": ("((double)vc[d] * scale)", "((double)vc[d])"),
+    "attn_head_stride": ("((size_t)i * QSA_H + (size_t)h) * QSA_D", "((size_t)i * QSA_H) * QSA_D"),
+    "attn_unnormalised": ("const double p = w[t] / total;", "const double p = w[t];"),
+    "attn_exponent_sign": ("w[t] = exp(w[t] - top);", "w[t] = exp(top - w[t]);"),
 }
 
 
