@@ -203,6 +203,35 @@ qsa_status qsa_block_select_small(const float *q, const float *kblk, const int8_
                                   float *scores, int32_t *ids, cudaStream_t stream);
 
 /*
+ * Attention over the selected blocks: each query's 4 heads attend the KV
+ * cells of the blocks listed in its row of ids (block b holds cells
+ * 4b .. 4b+3; cells at or past ncells, negative ids and ids at or past the
+ * last block are skipped; a block listed twice counts twice):
+ *   logit[h][c] = (sum_d q[i][h][d] * k_cells[c][d]) * k_scale[c] / sqrt(128)
+ *   out[i][h][d] = sum_c softmax_c(logit[h][.]) * v_cells[c][d] * v_scale[c]
+ * and out = 0 for a query with no attended cell. Accumulation is fp32 in a
+ * fixed order (the result does not depend on scheduling).
+ * q        fp32 [nq][4][128], 16-byte aligned.
+ * k_cells, v_cells  int8 [ncells][128], 16-byte aligned; k_scale_f16,
+ *          v_scale_f16  IEEE binary16 bit patterns [ncells], 2-byte aligned
+ *          (may be NULL when ncells == 0).
+ * ids      int32 [nq][k] (e.g. qsa_block_topk's output), 16-byte aligned.
+ * out      fp32 [nq][4][128], written, 16-byte aligned.
+ * nq < 0, k < 1 or ncells < 0 returns QSA_ERR_INVALID; nq == 0 is a no-op.
+ * Allocates nothing and keeps no state.
+ * Passages: "#3224 [Engine] perf(hip): tune RDNA4 QSA prompt WMMA path
+ * (STRATA_HIP_WMMA stays opt-in)", Summary and Evidence section 2 (int8-KV
+ * QSA attention with binary16 k/v scales, gated against FP64); "#3102
+ * perf(hip): enable wave32 QSA decode attention and MMVQ row reuse on
+ * gfx12", item D5 (decode attention in chunks merged in sequential order).
+ * The softmax temperature 1/sqrt(128), the per-cell scales and the 4 heads
+ * sharing the cells are readings: the pages print no formula.
+ */
+qsa_status qsa_sparse_attn(const float *q, const int8_t *k_cells, const uint16_t *k_scale_f16,
+                           const int8_t *v_cells, const uint16_t *v_scale_f16, int ncells, const int32_t *ids,
+                           int nq, int k, float *out, cudaStream_t stream);
+
+/*
  * Reads and clears the current device's error word: nonzero when a kernel
  * of this library gave up a bounded wait (its outputs are then invalid).
  * Synchronises `stream`. *code receives the word.

@@ -1,4 +1,5 @@
-"""Exact QSA block selection on GB300: block scoring and per-query top-k.
+"""Exact QSA block selection on GB300: block scoring, per-query top-k, and
+attention over the selected blocks.
 
 The computation lives in ``libqsa.so`` (CUDA kernels for sm_103a behind the C
 ABI of ``include/qsa.h``); ``qsa`` is its Python binding and ``workloads``
@@ -21,4 +22,5 @@ from .qsa import (  # noqa: F401
     groups,
     default_scorer_kernel,
     device_error,
+    sparse_attn,
 )

@@ -1,0 +1,295 @@
+// Attention of each query's 4 heads over the KV cells of its selected blocks
+// (int8 K and V cells, one binary16 scale per cell for each).
+//
+//   logit[h][c] = (sum_d q[i][h][d] * kq[c][d]) * ks[c] / sqrt(128)
+//   out[i][h][d] = sum_c softmax_c(logit[h][.]) * vq[c][d] * vs[c]
+//
+// over the cells c = 4b .. 4b+3 (< ncells) of every listed block b of query i
+// (negative or past-the-end ids are padding).
+//
+// Passages: "#3224 [Engine] perf(hip): tune RDNA4 QSA prompt WMMA path
+// (STRATA_HIP_WMMA stays opt-in)", Summary and Evidence section 2 (the QSA
+// attention reads int8 K and V cells with binary16 k/v scales and is gated
+// against an FP64 reference); "#3102 perf(hip): enable wave32 QSA decode
+// attention and MMVQ row reuse on gfx12", item D5 (decode attention in
+// chunks of cells whose partial results merge in sequential order).
+//
+// GB300 mapping. One CTA of 16 warps per query, or a cluster of up to 8 CTAs
+// per query when there are few queries (decode), so that the cells of one
+// query stream through several SMs. A warp step covers two listed blocks
+// (8 cells): every lane loads its 4 bytes (d = 4 lane .. +3) of each cell's
+// K and V row (one 128-byte line per row and warp), forms the 8 x 4 partial
+// dot products against its slice of the 4 head queries, and a butterfly
+// reduce-scatter (31 shuffles) leaves lane l with the full logit of cell
+// l / 4 for head l % 4. Each warp keeps an online softmax per head (running
+// maximum, normaliser, and the head's 128 output values, 4 per lane); the
+// next step's rows are loaded before the current step is used. Partial
+// results merge in a fixed order: the CTA's warps in warp order, then the
+// cluster's CTAs in rank order through distributed shared memory, so the
+// output does not depend on scheduling.
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "qsa_internal.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int AT_WARPS = 16;
+constexpr int AT_THREADS = AT_WARPS * 32;
+constexpr int STEP_IDS = 2;                              // listed blocks per warp step
+constexpr int STEP_CELLS = STEP_IDS * 4;                 // 8 cells
+constexpr float TEMPERATURE = 0.08838834764831845f;      // 1 / sqrt(128) = 2^-3.5, exact in fp32
+constexpr int MAX_CLUSTER = 8;
+
+struct AttnShared {
+    alignas(16) float p[AT_WARPS][32];          // a step's weights times the value scales, per warp
+    float m[AT_WARPS][HEADS];                   // warp partials: running maximum,
+    float l[AT_WARPS][HEADS];                   // normaliser,
+    alignas(16) float acc[AT_WARPS][HEADS][D];  // and unnormalised outputs
+    float cm[HEADS], cl[HEADS];                 // the CTA's merged partial (read by rank 0)
+    alignas(16) float cacc[HEADS][D];
+};
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Lane l returns the warp-wide sum of v[l]: five halving steps, each lane
+// keeping the half of its values selected by one bit of its lane index and
+// adding the partner's copy of that half.
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int n = 16; n >= 1; n >>= 1) {
+        const bool up = (lane & n) != 0;
+#pragma unroll
+        for (int j = 0; j < n; ++j) {
+            const float keep = up ? v[j + n] : v[j];
+            const float send = up ? v[j] : v[j + n];
+            v[j] = keep + __shfl_xor_sync(FULL_MASK, send, n);
+        }
+    }
+    return v[0];
+}
+
+// The signed byte e of w as a float, exactly, without an integer-to-float
+// conversion: with the sign bit flipped the byte is b + 128 in [0, 255];
+// placed as the low mantissa byte of 2^23 it reads 2^23 + b + 128, and
+// subtracting 2^23 + 128 leaves b.
+__device__ __forceinline__ float byte_f(uint32_t w, int e) {
+    const uint32_t bits = __byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u + static_cast<uint32_t>(e));
+    return __uint_as_float(bits) - 8388736.0f;
+}
+
+// The cell index of cell t (0..3) of listed slot j of query row `ids_i`, or
+// -1 when the slot is past k, padding, past the last block, or past ncells.
+__device__ __forceinline__ long long cell_of(const int32_t *__restrict__ ids_i, int k, int nblocks, int ncells,
+                                             long long j, int t) {
+    if (j >= k) return -1;
+    const int b = __ldg(ids_i + j);
+    if (b < 0 || b >= nblocks) return -1;
+    const long long c = 4LL * b + t;
+    return c < ncells ? c : -1;
+}
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    attn_kernel(const float *__restrict__ q, const int8_t *__restrict__ kc, const __half *__restrict__ ks,
+                const int8_t *__restrict__ vc, const __half *__restrict__ vs, int ncells,
+                const int32_t *__restrict__ ids, int k, float *__restrict__ out, int csize) {
+    __shared__ AttnShared sh;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t rank = csize > 1 ? cluster_ctarank() : 0u;
+    const long long i = blockIdx.x / csize;   // query
+    const int32_t *ids_i = ids + i * k;
+    const int nblocks = (ncells + 3) / 4;
+
+    grid_dependency_wait();   // q, the cells and the ids may come from the previous grid
+
+    float qv[HEADS][4];       // this lane's slice d = 4 lane .. +3 of each head's query
+#pragma unroll
+    for (int h = 0; h < HEADS; ++h) {
+        const float4 t = __ldg(reinterpret_cast<const float4 *>(q + (i * HEADS + h) * D) + lane);
+        qv[h][0] = t.x, qv[h][1] = t.y, qv[h][2] = t.z, qv[h][3] = t.w;
+    }
+
+    const long long nsteps = (static_cast<long long>(k) + STEP_IDS - 1) / STEP_IDS;
+    const long long wg = static_cast<long long>(rank) * AT_WARPS + warp;
+    const long long nw = static_cast<long long>(csize) * AT_WARPS;
+
+    // A step's rows: word `lane` of each cell's K and V row (0 for dead cells).
+    auto load_step = [&](long long st, uint32_t (&kw)[STEP_CELLS], uint32_t (&vw)[STEP_CELLS]) {
+#pragma unroll
+        for (int c = 0; c < STEP_CELLS; ++c) {
+            const long long cell = cell_of(ids_i, k, nblocks, ncells, STEP_IDS * st + (c >> 2), c & 3);
+            kw[c] = cell >= 0 ? __ldg(reinterpret_cast<const uint32_t *>(kc + cell * D) + lane) : 0u;
+            vw[c] = cell >= 0 ? __ldg(reinterpret_cast<const uint32_t *>(vc + cell * D) + lane) : 0u;
+        }
+    };
+
+    const int mc = lane >> 2;                  // this lane holds the logit of cell mc for head lane % 4
+    float m = -INFINITY, lsum = 0.0f;          // that head: running maximum, this lane's normaliser part
+    float acc[HEADS][4];
+#pragma unroll
+    for (int h = 0; h < HEADS; ++h)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[h][e] = 0.0f;
+
+    uint32_t kw[STEP_CELLS], vw[STEP_CELLS];
+    if (wg < nsteps) load_step(wg, kw, vw);
+    for (long long st = wg; st < nsteps; st += nw) {   // warp-uniform
+        uint32_t nkw[STEP_CELLS], nvw[STEP_CELLS];
+        if (st + nw < nsteps) load_step(st + nw, nkw, nvw);
+
+        float v[32];   // v[4 c + h]: this lane's part of cell c's dot product with head h
+#pragma unroll
+        for (int c = 0; c < STEP_CELLS; ++c) {
+            const float k0 = byte_f(kw[c], 0), k1 = byte_f(kw[c], 1), k2 = byte_f(kw[c], 2), k3 = byte_f(kw[c], 3);
+#pragma unroll
+            for (int h = 0; h < HEADS; ++h)
+                v[4 * c + h] = fmaf(qv[h][3], k3, fmaf(qv[h][2], k2, fmaf(qv[h][1], k1, qv[h][0] * k0)));
+        }
+        const float dot = reduce_scatter32(v, lane);
+        const long long cell = cell_of(ids_i, k, nblocks, ncells, STEP_IDS * st + (mc >> 2), mc & 3);
+        const float logit = cell >= 0 ? dot * __half2float(ks[cell]) * TEMPERATURE : -INFINITY;
+
+        // Online softmax of head lane % 4 over this step's cells (the lanes with that head).
+        float bm = logit;
+        bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 4));
+        bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 8));
+        bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 16));
+        const float mn = fmaxf(m, bm);
+        const float alpha = mn == -INFINITY ? 1.0f : expf(m - mn);
+        const float p = cell >= 0 ? expf(logit - mn) : 0.0f;
+        m = mn;
+        lsum = fmaf(lsum, alpha, p);
+        sh.p[warp][lane] = cell >= 0 ? p * __half2float(vs[cell]) : 0.0f;
+        float al[HEADS];
+#pragma unroll
+        for (int h = 0; h < HEADS; ++h) al[h] = __shfl_sync(FULL_MASK, alpha, h);
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < HEADS; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[h][e] *= al[h];
+#pragma unroll
+        for (int c = 0; c < STEP_CELLS; ++c) {
+            const float4 pc = *reinterpret_cast<const float4 *>(&sh.p[warp][4 * c]);   // heads 0..3
+            const float pw[HEADS] = {pc.x, pc.y, pc.z, pc.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float ve = byte_f(vw[c], e);
+#pragma unroll
+                for (int h = 0; h < HEADS; ++h) acc[h][e] = fmaf(pw[h], ve, acc[h][e]);
+            }
+        }
+        __syncwarp();   // sh.p is rewritten by the next step
+#pragma unroll
+        for (int c = 0; c < STEP_CELLS; ++c) {
+            kw[c] = nkw[c];
+            vw[c] = nvw[c];
+        }
+    }
+
+    // Warp partials: the normaliser of head lane % 4 sums over the lanes holding it.
+    lsum += __shfl_xor_sync(FULL_MASK, lsum, 4);
+    lsum += __shfl_xor_sync(FULL_MASK, lsum, 8);
+    lsum += __shfl_xor_sync(FULL_MASK, lsum, 16);
+    if (lane < HEADS) {
+        sh.m[warp][lane] = m;
+        sh.l[warp][lane] = lsum;
+    }
+#pragma unroll
+    for (int h = 0; h < HEADS; ++h)
+        *reinterpret_cast<float4 *>(&sh.acc[warp][h][4 * lane]) = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+    __syncthreads();
+
+    // The CTA's warps merged in warp order: thread = (head, d).
+    const int h = threadIdx.x >> 7, d = threadIdx.x & (D - 1);
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < AT_WARPS; ++w) M = fmaxf(M, sh.m[w][h]);
+    float A = 0.0f, L = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < AT_WARPS; ++w) {
+            const float mw = sh.m[w][h];
+            if (mw != -INFINITY) {
+                const float f = expf(mw - M);
+                A = fmaf(sh.acc[w][h][d], f, A);
+                L = fmaf(sh.l[w][h], f, L);
+            }
+        }
+    }
+    float *o = out + (i * HEADS + h) * D + d;
+    if (csize == 1) {
+        *o = L > 0.0f ? A / L : 0.0f;
+        return;
+    }
+    // The cluster's CTAs merged by rank 0, in rank order.
+    sh.cacc[h][d] = A;
+    if (d == 0) {
+        sh.cm[h] = M;
+        sh.cl[h] = L;
+    }
+    cluster_sync_all();
+    if (rank == 0) {
+        float Mc = -INFINITY, mr[MAX_CLUSTER];
+#pragma unroll
+        for (int r = 0; r < MAX_CLUSTER; ++r) {
+            mr[r] = -INFINITY;
+            if (r < csize) mr[r] = ld_shared_cluster_f32(map_shared_rank(smem_u32(&sh.cm[h]), r));
+            Mc = fmaxf(Mc, mr[r]);
+        }
+        float Ac = 0.0f, Lc = 0.0f;
+        if (Mc != -INFINITY) {
+#pragma unroll
+            for (int r = 0; r < MAX_CLUSTER; ++r) {
+                if (r < csize && mr[r] != -INFINITY) {
+                    const float f = expf(mr[r] - Mc);
+                    Ac = fmaf(ld_shared_cluster_f32(map_shared_rank(smem_u32(&sh.cacc[h][d]), r)), f, Ac);
+                    Lc = fmaf(ld_shared_cluster_f32(map_shared_rank(smem_u32(&sh.cl[h]), r)), f, Lc);
+                }
+            }
+        }
+        *o = Lc > 0.0f ? Ac / Lc : 0.0f;
+    }
+    cluster_sync_all();   // no CTA leaves while rank 0 may still read it
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_attn(const float *q, const int8_t *kc, const uint16_t *ks, const int8_t *vc,
+                               const uint16_t *vs, int ncells, const int32_t *ids, int nq, int k, float *out,
+                               cudaStream_t stream) {
+    // Few queries: a cluster per query spreads its cells over several SMs.
+    const int sms = device_sm_count();
+    int csize = 1;
+    for (int c = MAX_CLUSTER; c > 1; c >>= 1) {
+        if (static_cast<long long>(nq) * c <= sms) {
+            csize = c;
+            break;
+        }
+    }
+    const long long grid = static_cast<long long>(nq) * csize;
+    if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(AT_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = static_cast<unsigned>(csize);
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, attn_kernel, q, kc, reinterpret_cast<const __half *>(ks), vc,
+                              reinterpret_cast<const __half *>(vs), ncells, ids, k, out, csize);
+}
+
+}  // namespace qsa

@@ -215,6 +215,22 @@ qsa_status qsa_block_select_small(const float *q, const float *kblk, const int8_
                                                stream));
 }
 
+qsa_status qsa_sparse_attn(const float *q, const int8_t *k_cells, const uint16_t *k_scale_f16,
+                           const int8_t *v_cells, const uint16_t *v_scale_f16, int ncells, const int32_t *ids,
+                           int nq, int k, float *out, cudaStream_t stream) {
+    if (nq < 0 || k < 1 || ncells < 0) return QSA_ERR_INVALID;
+    if (nq == 0) return QSA_OK;
+    if (q == nullptr || ids == nullptr || out == nullptr || !aligned16(q) || !aligned16(ids) || !aligned16(out))
+        return QSA_ERR_INVALID;
+    if (ncells > 0 && (k_cells == nullptr || v_cells == nullptr || k_scale_f16 == nullptr ||
+                       v_scale_f16 == nullptr || !aligned16(k_cells) || !aligned16(v_cells) ||
+                       (reinterpret_cast<uintptr_t>(k_scale_f16) & 1u) != 0 ||
+                       (reinterpret_cast<uintptr_t>(v_scale_f16) & 1u) != 0))
+        return QSA_ERR_INVALID;
+    return from_cuda(qsa::launch_sparse_attn(q, k_cells, k_scale_f16, v_cells, v_scale_f16, ncells, ids, nq, k, out,
+                                             stream));
+}
+
 qsa_status qsa_get_device_error(uint32_t *code, cudaStream_t stream) {
     if (code == nullptr) return QSA_ERR_INVALID;
     *code = 0;

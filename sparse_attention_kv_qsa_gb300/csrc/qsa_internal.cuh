@@ -56,6 +56,12 @@ cudaError_t launch_topk(const float *scores, const uint32_t *gmax, int nq, int a
 cudaError_t launch_select_decode(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,
                                  int nq, int active, int k, float *scores, int32_t *ids, cudaStream_t stream);
 
+// Attention of each query's 4 heads over the int8 KV cells of its listed
+// blocks (csrc/attn.cu).
+cudaError_t launch_sparse_attn(const float *q, const int8_t *kc, const uint16_t *ks, const int8_t *vc,
+                               const uint16_t *vs, int ncells, const int32_t *ids, int nq, int k, float *out,
+                               cudaStream_t stream);
+
 // ids[i][j] = j < active ? j : -1 (the k >= active case).
 cudaError_t launch_topk_all(int nq, int active, int k, int32_t *ids, cudaStream_t stream);
 

@@ -25,7 +25,8 @@ QSA_OK, QSA_ERR_INVALID, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
 
 EXPORTED = ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
             "qsa_block_scores_gmax", "qsa_block_scores_q8_gmax", "qsa_block_group_max", "qsa_block_topk_gmax",
-            "qsa_block_select_static", "qsa_block_select_small", "qsa_get_device_error", "qsa_status_string")
+            "qsa_block_select_static", "qsa_block_select_small", "qsa_sparse_attn", "qsa_get_device_error",
+            "qsa_status_string")
 
 
 class QSAError(RuntimeError):
@@ -61,13 +62,14 @@ def lib() -> ctypes.CDLL:
         L.qsa_block_group_max.argtypes = [vp, i, i, vp, vp]
         L.qsa_block_select_static.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
         L.qsa_block_select_small.argtypes = [vp, vp, vp, vp, i, i, i, i, vp, vp, vp]
+        L.qsa_sparse_attn.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, vp, vp]
         L.qsa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
         L.qsa_status_string.argtypes = [i]
         L.qsa_status_string.restype = ctypes.c_char_p
         for f in ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
                   "qsa_block_scores_gmax", "qsa_block_scores_q8_gmax", "qsa_block_topk_gmax",
                   "qsa_block_group_max", "qsa_block_select_static", "qsa_block_select_small",
-                  "qsa_get_device_error"):
+                  "qsa_sparse_attn", "qsa_get_device_error"):
             getattr(L, f).restype = i
         _lib = L
     return _lib
@@ -323,6 +325,36 @@ def block_select_small(q: torch.Tensor, active_blocks: int, k: int, kblk: torch.
                                         active_blocks, k, _ptr(scores_out), _ptr(ids_out), _stream(q)),
            "qsa_block_select_small")
     return scores_out, ids_out
+
+
+def sparse_attn(q: torch.Tensor, k_cells: torch.Tensor, k_scale_f16: torch.Tensor, v_cells: torch.Tensor,
+                v_scale_f16: torch.Tensor, ids: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """``qsa_sparse_attn``: each query's 4 heads attend the int8 KV cells of
+    the blocks listed in its row of ``ids`` -> ``out [nq, 4, 128]`` fp32.
+    ``k_cells``/``v_cells`` int8 ``[ncells, 128]``; the scales are binary16
+    bit patterns ``[ncells]`` (int16 or uint16 storage)."""
+    _check_q(q)
+    _need(k_cells, "k_cells", torch.int8, 2)
+    _need(v_cells, "v_cells", torch.int8, 2)
+    _need(ids, "ids", torch.int32, 2)
+    ncells = k_cells.shape[0]
+    if tuple(v_cells.shape) != tuple(k_cells.shape) or k_cells.shape[1] != 128:
+        raise ValueError("k_cells and v_cells must both be [ncells, 128]")
+    for name, t in (("k_scale_f16", k_scale_f16), ("v_scale_f16", v_scale_f16)):
+        if not t.is_cuda or t.dim() != 1 or t.shape[0] != ncells or t.element_size() != 2 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a 1-d CUDA tensor of {ncells} binary16 values")
+    nq, k = ids.shape
+    if nq != q.shape[0]:
+        raise ValueError("ids must have one row per query")
+    if out is None:
+        out = torch.empty((nq, 4, 128), dtype=torch.float32, device=q.device)
+    else:
+        _need(out, "out", torch.float32, 3)
+        if tuple(out.shape) != (nq, 4, 128):
+            raise ValueError(f"out must have shape {(nq, 4, 128)}")
+    _check(lib().qsa_sparse_attn(_ptr(q), _ptr(k_cells), _ptr(k_scale_f16), _ptr(v_cells), _ptr(v_scale_f16),
+                                 ncells, _ptr(ids), nq, k, _ptr(out), _stream(q)), "qsa_sparse_attn")
+    return out
 
 
 def device_error(device: torch.device | None = None) -> int:

@@ -35,6 +35,9 @@ STREAM_DIRECTION = 3
 STREAM_NEEDLES = 4
 STREAM_TIES = 5
 STREAM_SCALES = 6
+STREAM_V = 7         # attention: value cells
+STREAM_V_SCALES = 8
+STREAM_IDS = 9
 
 SEED_BASE = 0x9E3779B9
 
@@ -268,6 +271,59 @@ def int8_case(nq: int, active: int, k: int, max_blocks: int | None = None,
     sc[:active] = np.exp(lo + (hi - lo) * u).astype(np.float16).view(np.uint16)
     return Workload(f"int8_{active}_nq{nq}_k{k}", nq, active, max_blocks, k, q,
                     kq8=kq, kscale=sc)
+
+
+@dataclass
+class AttnWorkload:
+    """One seeded attention-over-selected-blocks problem.
+
+    q:      float32 [nq, H, D]
+    kc, vc: int8 [ncells, D] (key and value cells of one KV head)
+    ks, vs: uint16 [ncells] (IEEE binary16 bit patterns, one scale per cell)
+    ids:    int32 [nq, k] (listed blocks per query; -1 = padding)
+    """
+    name: str
+    nq: int
+    ncells: int
+    k: int
+    q: np.ndarray
+    kc: np.ndarray
+    ks: np.ndarray
+    vc: np.ndarray
+    vs: np.ndarray
+    ids: np.ndarray
+
+
+def _log_uniform_half(seed: int, stream: int, n: int, lo: float, hi: float) -> np.ndarray:
+    u = uniform(seed, stream, n)
+    a, b = math.log(lo), math.log(hi)
+    return np.exp(a + (b - a) * u).astype(np.float16).view(np.uint16)
+
+
+def attn_case(nq: int, ncells: int, k: int, pad: int = 0, config_index: int = 10) -> AttnWorkload:
+    """KV cells for attention over the selected blocks, with the decode
+    recipe's distributions: K and V int8 uniform on [-127, 127], one binary16
+    scale per cell each, log-uniform in [1e-3, 1e-1]; q is N(0,1). Each query
+    lists k - pad distinct blocks (drawn from the seeded stream, ascending, as
+    the top-k returns them) followed by pad slots of -1."""
+    s = seed_for(config_index)
+    q = normal32(s, STREAM_Q, nq * H * D).reshape(nq, H, D)
+    kc = int8_127(s, STREAM_KBLK, ncells * D).reshape(ncells, D)
+    vc = int8_127(s, STREAM_V, ncells * D).reshape(ncells, D)
+    ks = _log_uniform_half(s, STREAM_SCALES, ncells, 1e-3, 1e-1)
+    vs = _log_uniform_half(s, STREAM_V_SCALES, ncells, 1e-3, 1e-1)
+    nblocks = (ncells + CELLS_PER_BLOCK - 1) // CELLS_PER_BLOCK
+    take = k - pad
+    assert 0 <= take <= nblocks
+    ids = np.full((nq, k), -1, dtype=np.int32)
+    draws = u32(s, STREAM_IDS, nq * 4 * max(take, 1)).reshape(nq, -1) % np.uint32(max(nblocks, 1))
+    for i in range(nq):
+        _, first = np.unique(draws[i], return_index=True)
+        picked = draws[i][np.sort(first)][:take]
+        if picked.shape[0] < take:                 # few blocks: take them all in a seeded order
+            picked = permutation(s + i, STREAM_IDS, nblocks)[:take]
+        ids[i, :take] = np.sort(picked.astype(np.int32))
+    return AttnWorkload(f"attn_{ncells}_nq{nq}_k{k}", nq, ncells, k, q, kc, ks, vc, vs, ids)
 
 
 def pcg32_reference(seed: int, stream: int, n: int) -> list[int]:
