@@ -305,6 +305,67 @@ def run_reference(args, world, rank):
             "gpu_launches": 0}
 
 
+def attention_side_measurement(dev, stream):
+    """qsa_sparse_attn over the selected blocks' int8 KV cells (262,144 cells,
+    binary16 scales): decode shapes (nq = 1 and 4, k = 128) per call of a CUDA
+    graph of 20 calls, and a prompt-like shape (256 queries, k = 512, L2
+    flushed before each call) with its HBM and FP32 fractions. The FP32 peak
+    is 152 SMs x 128 lanes x 2 FLOP x the sampled SM clock's maximum."""
+    import torch
+    import sparse_attention_kv_qsa_gb300 as qsa
+    from sparse_attention_kv_qsa_gb300 import workloads as w
+    out = {"workload": "attention over the selected blocks: int8 K/V cells + binary16 scales, 262,144 cells",
+           "unit": "us"}
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    for nq, k, name in ((1, 128, "decode_nq1_k128"), (4, 128, "decode_nq4_k128"), (256, 512, "nq256_k512")):
+        W = w.attn_case(nq, 262144, k)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        q, kc, vc, ids = t(W.q), t(W.kc), t(W.vc), t(W.ids)
+        ks = torch.from_numpy(W.ks.view(np.int16)).to(dev)
+        vs = torch.from_numpy(W.vs.view(np.int16)).to(dev)
+        o = torch.empty((nq, 4, 128), dtype=torch.float32, device=dev)
+        call = lambda: qsa.sparse_attn(q, kc, ks, vc, vs, ids, out=o)
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        if nq <= 4:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                call()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g, stream=side):
+                    for _ in range(20):
+                        call()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            out[name] = {"graph_call_us": 1e3 * e0.elapsed_time(e1) / 20}
+            continue
+        ts = []
+        for i in range(30):
+            flush.fill_(float(i))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(1e3 * e0.elapsed_time(e1))
+        us = statistics.median(ts)
+        cells = nq * k * 4
+        bytes_ = cells * 2 * (128 + 2) + nq * 4 * 128 * 4 * 2 + nq * k * 4
+        flops = cells * 4 * 128 * 2 * 2
+        peak_fp32 = 152 * 128 * 2 * 2.07e9
+        out[name] = {"call_us_p50": us, "algorithmic_bytes": bytes_, "hbm_gbs": bytes_ / us / 1e3,
+                     "fp32_tflops": flops / us / 1e6, "fp32_frac_of_nominal": flops / (us * 1e-6) / peak_fp32}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -323,6 +384,7 @@ def main():
     ap.add_argument("--no-flush", action="store_true", help="warm L2 (back-to-back steps)")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped side measurement")
     ap.add_argument("--no-ksweep", action="store_true", help="skip the k sweep (64, 256, 1024) side measurement")
+    ap.add_argument("--no-attn", action="store_true", help="skip the attention side measurement")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -540,6 +602,8 @@ def main():
 
     if rank == 0 and not args.no_decode:
         line["decode"] = decode_side_measurement(dev, stream)
+    if rank == 0 and not args.no_attn:
+        line["attention"] = attention_side_measurement(dev, stream)
 
     if rank == 0 and not args.no_ksweep and path == "gmax":
         # The headline workload's k sweep, same calls and flushes, 200 steps
