@@ -137,6 +137,13 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
     return v;
 }
 
+// Atomic add at GPU scope with acquire-release semantics; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Waits (bounded by WAIT_LIMIT_NS) until the word at p differs from `old`,
 // with acquire semantics at GPU scope. Returns false if it gave up.
 __device__ __forceinline__ bool wait_word_changes(const uint32_t *p, uint32_t old) {

@@ -808,11 +808,14 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
     for (long long c = blockIdx.x; c < nchunks; c += gridDim.x)
         dec_score_chunk<NQ, kInt8, ROW_THREADS>(qs, c, kblk, kq8, kscale, nq, active, scores, g_decode_gmax, gk);
     if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(&g_decode_sync[0], 1u) == gridDim.x - 1) {
-            atomicExch(&g_decode_sync[0], 0u);
-            __threadfence();
+        // The arrival releases this CTA's scores and group maxima (ordered
+        // before it by the CTA barrier that ends the scoring); the last one
+        // also acquires every other CTA's through the counter, publishes them
+        // with the generation's release store, and then resets the counter
+        // (read again only by the next launch, after this grid completes).
+        if (atom_add_acq_rel_gpu(&g_decode_sync[0], 1u) == gridDim.x - 1) {
             st_release_gpu(&g_decode_sync[1], gen + 1u);
+            g_decode_sync[0] = 0u;
         }
     }
     if (blockIdx.x >= static_cast<unsigned>(nq)) return;   // the whole CTA
