@@ -83,17 +83,6 @@ __device__ __forceinline__ float byte_f(uint32_t w, int e) {
     return __uint_as_float(bits) - 8388736.0f;
 }
 
-// The cell index of cell t (0..3) of listed slot j of query row `ids_i`, or
-// -1 when the slot is past k, padding, past the last block, or past ncells.
-__device__ __forceinline__ long long cell_of(const int32_t *__restrict__ ids_i, int k, int nblocks, int ncells,
-                                             long long j, int t) {
-    if (j >= k) return -1;
-    const int b = __ldg(ids_i + j);
-    if (b < 0 || b >= nblocks) return -1;
-    const long long c = 4LL * b + t;
-    return c < ncells ? c : -1;
-}
-
 __global__ void __launch_bounds__(AT_THREADS, 1)
     attn_kernel(const float *__restrict__ q, const int8_t *__restrict__ kc, const __half *__restrict__ ks,
                 const int8_t *__restrict__ vc, const __half *__restrict__ vs, int ncells,
@@ -118,13 +107,27 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const long long wg = static_cast<long long>(rank) * AT_WARPS + warp;
     const long long nw = static_cast<long long>(csize) * AT_WARPS;
 
-    // A step's rows: word `lane` of each cell's K and V row (0 for dead cells).
-    auto load_step = [&](long long st, uint32_t (&kw)[STEP_CELLS], uint32_t (&vw)[STEP_CELLS]) {
+    // A step's data: its two listed blocks (-1 when past k, padding or past
+    // the last block) and word `lane` of each of their cells' K and V rows
+    // (0 for dead cells).
+    struct Step {
+        int b[STEP_IDS];
+        uint32_t kw[STEP_CELLS], vw[STEP_CELLS];
+    };
+    auto load_step = [&](long long st, Step &s) {
+#pragma unroll
+        for (int j = 0; j < STEP_IDS; ++j) {
+            const long long slot = STEP_IDS * st + j;
+            const int b = st < nsteps && slot < k ? __ldg(ids_i + slot) : -1;
+            s.b[j] = b >= 0 && b < nblocks ? b : -1;
+        }
 #pragma unroll
         for (int c = 0; c < STEP_CELLS; ++c) {
-            const long long cell = cell_of(ids_i, k, nblocks, ncells, STEP_IDS * st + (c >> 2), c & 3);
-            kw[c] = cell >= 0 ? __ldg(reinterpret_cast<const uint32_t *>(kc + cell * D) + lane) : 0u;
-            vw[c] = cell >= 0 ? __ldg(reinterpret_cast<const uint32_t *>(vc + cell * D) + lane) : 0u;
+            const int b = s.b[c >> 2];
+            const long long cell = 4LL * b + (c & 3);
+            const bool live = b >= 0 && cell < ncells;
+            s.kw[c] = live ? __ldg(reinterpret_cast<const uint32_t *>(kc + cell * D) + lane) : 0u;
+            s.vw[c] = live ? __ldg(reinterpret_cast<const uint32_t *>(vc + cell * D) + lane) : 0u;
         }
     };
 
@@ -136,23 +139,21 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[h][e] = 0.0f;
 
-    uint32_t kw[STEP_CELLS], vw[STEP_CELLS];
-    if (wg < nsteps) load_step(wg, kw, vw);
-    for (long long st = wg; st < nsteps; st += nw) {   // warp-uniform
-        uint32_t nkw[STEP_CELLS], nvw[STEP_CELLS];
-        if (st + nw < nsteps) load_step(st + nw, nkw, nvw);
-
+    auto run_step = [&](const Step &s) {
         float v[32];   // v[4 c + h]: this lane's part of cell c's dot product with head h
 #pragma unroll
         for (int c = 0; c < STEP_CELLS; ++c) {
-            const float k0 = byte_f(kw[c], 0), k1 = byte_f(kw[c], 1), k2 = byte_f(kw[c], 2), k3 = byte_f(kw[c], 3);
+            const float k0 = byte_f(s.kw[c], 0), k1 = byte_f(s.kw[c], 1);
+            const float k2 = byte_f(s.kw[c], 2), k3 = byte_f(s.kw[c], 3);
 #pragma unroll
             for (int h = 0; h < HEADS; ++h)
                 v[4 * c + h] = fmaf(qv[h][3], k3, fmaf(qv[h][2], k2, fmaf(qv[h][1], k1, qv[h][0] * k0)));
         }
         const float dot = reduce_scatter32(v, lane);
-        const long long cell = cell_of(ids_i, k, nblocks, ncells, STEP_IDS * st + (mc >> 2), mc & 3);
-        const float logit = cell >= 0 ? dot * __half2float(ks[cell]) * TEMPERATURE : -INFINITY;
+        const int b = (mc >> 2) != 0 ? s.b[1] : s.b[0];
+        const long long cell = 4LL * b + (mc & 3);
+        const bool live = b >= 0 && cell < ncells;
+        const float logit = live ? dot * __half2float(ks[cell]) * TEMPERATURE : -INFINITY;
 
         // Online softmax of head lane % 4 over this step's cells (the lanes with that head).
         float bm = logit;
@@ -161,10 +162,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 16));
         const float mn = fmaxf(m, bm);
         const float alpha = mn == -INFINITY ? 1.0f : expf(m - mn);
-        const float p = cell >= 0 ? expf(logit - mn) : 0.0f;
+        const float p = live ? expf(logit - mn) : 0.0f;
         m = mn;
         lsum = fmaf(lsum, alpha, p);
-        sh.p[warp][lane] = cell >= 0 ? p * __half2float(vs[cell]) : 0.0f;
+        sh.p[warp][lane] = live ? p * __half2float(vs[cell]) : 0.0f;
         float al[HEADS];
 #pragma unroll
         for (int h = 0; h < HEADS; ++h) al[h] = __shfl_sync(FULL_MASK, alpha, h);
@@ -179,17 +180,26 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             const float pw[HEADS] = {pc.x, pc.y, pc.z, pc.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float ve = byte_f(vw[c], e);
+                const float ve = byte_f(s.vw[c], e);
 #pragma unroll
                 for (int h = 0; h < HEADS; ++h) acc[h][e] = fmaf(pw[h], ve, acc[h][e]);
             }
         }
         __syncwarp();   // sh.p is rewritten by the next step
-#pragma unroll
-        for (int c = 0; c < STEP_CELLS; ++c) {
-            kw[c] = nkw[c];
-            vw[c] = nvw[c];
-        }
+    };
+
+    // Two step buffers in turn: the next step's rows load while this one runs.
+    Step s0, s1;
+    long long st = wg;
+    load_step(st, s0);
+    while (st < nsteps) {   // warp-uniform
+        load_step(st + nw, s1);
+        run_step(s0);
+        st += nw;
+        if (st >= nsteps) break;
+        load_step(st + nw, s0);
+        run_step(s1);
+        st += nw;
     }
 
     // Warp partials: the normaliser of head lane % 4 sums over the lanes holding it.
