@@ -385,6 +385,9 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped side measurement")
     ap.add_argument("--no-ksweep", action="store_true", help="skip the k sweep (64, 256, 1024) side measurement")
     ap.add_argument("--no-attn", action="store_true", help="skip the attention side measurement")
+    ap.add_argument("--attn-launches", type=int, default=0,
+                    help="only launch qsa_sparse_attn this many times on 256 queries x k=512 over 262,144 "
+                         "cells (a short run for a profiler to capture), then exit")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -403,6 +406,17 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.attn_launches > 0:
+        A = workloads.attn_case(256, 262144, 512)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        ks, vs = t(A.ks.view(np.int16)), t(A.vs.view(np.int16))
+        q, kc, vc, ids = t(A.q), t(A.kc), t(A.vc), t(A.ids)
+        out = torch.empty((A.nq, 4, 128), dtype=torch.float32, device=dev)
+        for _ in range(args.attn_launches):
+            qsa.sparse_attn(q, kc, ks, vc, vs, ids, out=out)
+        torch.cuda.synchronize()
+        print(json.dumps({"attn_launches": args.attn_launches, "workload": A.name}), flush=True)
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
