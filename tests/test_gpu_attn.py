@@ -94,7 +94,9 @@ def _check(W, out):
                                              (200, 16384, 512, 17),     # one CTA per query
                                              (3, 4099 * 4 + 3, 60, 7),  # partial last block
                                              (2, 17, 5, 0),             # every block, ragged
-                                             (5, 4096, 1, 0)])          # one block
+                                             (5, 4096, 1, 0),           # one block
+                                             (2, 262144, 4096, 0),      # long lists: 16,384 cells per query
+                                             (7, 65536, 300, 290)])     # mostly padding
 def test_sparse_attn_matches_oracle(nq, ncells, k, pad):
     import torch
     from sparse_attention_kv_qsa_gb300 import workloads as w
