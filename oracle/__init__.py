@@ -51,6 +51,10 @@ class Oracle:
         L.qsa_oracle_topk_f64.argtypes = [vp, lg, lg, lg, vp, i]
         L.qsa_oracle_topk_f32.argtypes = [vp, lg, lg, lg, vp, i]
         L.qsa_oracle_sparse_attn.argtypes = [vp, vp, vp, vp, vp, lg, vp, lg, lg, vp, i]
+        L.qsa_oracle_block_summary.argtypes = [vp, vp, lg, lg, lg, vp, vp, vp]
+        L.qsa_oracle_block_summary.restype = None
+        L.qsa_oracle_float_to_half.argtypes = [ctypes.c_float]
+        L.qsa_oracle_float_to_half.restype = ctypes.c_uint16
         for f in ("qsa_oracle_scores", "qsa_oracle_scores_q8", "qsa_oracle_topk_f64",
                   "qsa_oracle_topk_f32", "qsa_oracle_sparse_attn"):
             getattr(L, f).restype = None
@@ -143,6 +147,24 @@ class Oracle:
                                         vs.ctypes.data, ncells, ids.ctypes.data, nq, k, out.ctypes.data,
                                         nthreads)
         return out
+
+    def float_to_half(self, x: float) -> int:
+        return int(self.lib.qsa_oracle_float_to_half(float(x)))
+
+    def block_summary(self, kq: np.ndarray, ks: np.ndarray, b0: int, b1: int):
+        """Summary keys of blocks b0..b1-1 from int8 cells ``[ncells, 128]``
+        with binary16 scales ``[ncells]``: ``(key fp32 [n, 128], kq8 int8
+        [n, 128], kscale uint16 [n])``, n = b1 - b0."""
+        kq, ks = self._c(kq, np.int8), self._c(ks, np.uint16)
+        ncells = kq.shape[0]
+        assert kq.shape == (ncells, D) and ks.shape == (ncells,) and 0 <= b0 <= b1
+        n = b1 - b0
+        key = np.empty((n, D), dtype=np.float32)
+        kq8 = np.empty((n, D), dtype=np.int8)
+        ksc = np.empty(n, dtype=np.uint16)
+        self.lib.qsa_oracle_block_summary(kq.ctypes.data, ks.ctypes.data, ncells, b0, b1, key.ctypes.data,
+                                          kq8.ctypes.data, ksc.ctypes.data)
+        return key, kq8, ksc
 
     def select(self, q, kblk, active: int, k: int, nthreads: int = 0):
         """Scores then ids: ``(S[nq, active] fp64, ids[nq, k])``."""

@@ -295,3 +295,81 @@ void qsa_oracle_sparse_attn(const float *q, const int8_t *kq, const uint16_t *ks
     attn_ctx c = {q, kq, vq, ks, vs, ncells, k, ids, out};
     for_each_row(attn_row, &c, nq, nthreads);
 }
+
+/* ---- block summary keys ------------------------------------------------ */
+/*
+ * Passages: "#3108 optimize exact QSA block scoring and top-k selection on
+ * gfx12", the Microbenchmark & Parity Evidence table (its decode layer times
+ * "append + scores + topk + attn": a block's summary key is brought up to
+ * date when cells are appended). The pages do not say how a key is built
+ * from its cells; the reading taken:
+ *  - block b's key is the element-wise mean of its present cells (cells
+ *    4b .. 4b+3 below ncells), each cell being kq[c][d] * ks[c] (int8 times
+ *    a binary16 scale; the product is exact in fp32);
+ *  - the int8 form (the decode scorer's key format) has one binary16 scale
+ *    per block, s = binary16(max_d |key[d]| / 127) rounded to nearest even,
+ *    and codes rint(key[d] / s) (0 when s is 0);
+ *  - a block with no present cell gets a zero key, zero codes, scale 0.
+ * Because the integer codes are decided by float arithmetic, this restates
+ * the computation in fp32, in one order: sum = ((0 + x0) + x1) + ... over the
+ * present cells, key = sum / n, s32 = max / 127, each an IEEE single
+ * operation (the products are exact, so contracting them into fused
+ * multiply-adds changes nothing).
+ */
+static uint16_t float_to_half_rne(float f) {
+    /* binary32 -> binary16, round to nearest even, from the formats'
+     * definitions (no NaN or infinity arises here). */
+    union { float f; uint32_t u; } v = {f};
+    const uint32_t sign = (v.u >> 16) & 0x8000u;
+    const uint32_t a = v.u & 0x7FFFFFFFu;
+    if (a >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u);       /* rounds past 65504: infinity */
+    const int e = (int)(a >> 23) - 127;                              /* unbiased exponent */
+    if (e >= -14) {                                                  /* normal binary16 */
+        uint32_t m = a & 0x7FFFFFu;                                  /* 23-bit fraction */
+        uint32_t h = (uint32_t)(e + 15) << 10 | (m >> 13);
+        const uint32_t rest = m & 0x1FFFu;                           /* the 13 dropped bits */
+        if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u;   /* may carry into the exponent */
+        return (uint16_t)(sign | h);
+    }
+    /* subnormal binary16: value = k * 2^-24 with k = |f| * 2^24 rounded to
+     * nearest even (k = 1024 is the smallest normal, whose encoding it is) */
+    const double r = rint(fabs((double)f) * 16777216.0);
+    return (uint16_t)(sign | (uint16_t)r);
+}
+
+uint16_t qsa_oracle_float_to_half(float f) { return float_to_half_rne(f); }
+
+void qsa_oracle_block_summary(const int8_t *kq, const uint16_t *ks, long ncells, long b0, long b1,
+                              float *key, int8_t *kq8, uint16_t *kscale) {
+    for (long b = b0; b < b1; ++b) {
+        long n = ncells - 4 * b;
+        if (n > 4) n = 4;
+        if (n < 0) n = 0;
+        float mean[QSA_D];
+        for (int d = 0; d < QSA_D; ++d) {
+            float sum = 0.0f;
+            for (long t = 0; t < n; ++t) {
+                const long c = 4 * b + t;
+                const float x = (float)kq[(size_t)c * QSA_D + d] * (float)qsa_oracle_half_to_double(ks[c]);
+                sum = sum + x;
+            }
+            mean[d] = n > 0 ? sum / (float)n : 0.0f;
+        }
+        const size_t row = (size_t)(b - b0);
+        if (key != NULL)
+            for (int d = 0; d < QSA_D; ++d) key[row * QSA_D + d] = mean[d];
+        if (kq8 != NULL) {
+            float top = 0.0f;
+            for (int d = 0; d < QSA_D; ++d) top = fmaxf(top, fabsf(mean[d]));
+            const uint16_t sh = float_to_half_rne(top / 127.0f);
+            const float s = (float)qsa_oracle_half_to_double(sh);
+            kscale[row] = sh;
+            for (int d = 0; d < QSA_D; ++d) {
+                float c = s > 0.0f ? rintf(mean[d] / s) : 0.0f;
+                if (c > 127.0f) c = 127.0f;
+                if (c < -127.0f) c = -127.0f;
+                kq8[row * QSA_D + d] = (int8_t)c;
+            }
+        }
+    }
+}

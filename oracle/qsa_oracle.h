@@ -12,6 +12,8 @@
  *   ids     int32  [nq][k]           (written: ascending ids, -1 padding)
  *   attention: kq, vq int8 [ncells][128], ks, vs uint16 (binary16) [ncells],
  *              ids int32 [nq][k] (read), out double [nq][4][128] (written)
+ *   summary:   key float [b1-b0][128], kq8 int8 [b1-b0][128], kscale uint16 [b1-b0]
+ *              (rows of blocks b0..b1-1, written; key or kq8+kscale may be NULL)
  * nthreads <= 0 uses every online core.
  */
 #ifndef QSA_ORACLE_H
@@ -33,6 +35,9 @@ void qsa_oracle_topk_f64(const double *S, long nq, long active, long k, int32_t 
                          int nthreads);
 void qsa_oracle_topk_f32(const float *scores, long nq, long active, long k, int32_t *ids,
                          int nthreads);
+uint16_t qsa_oracle_float_to_half(float f);
+void qsa_oracle_block_summary(const int8_t *kq, const uint16_t *ks, long ncells, long b0, long b1,
+                              float *key, int8_t *kq8, uint16_t *kscale);
 void qsa_oracle_sparse_attn(const float *q, const int8_t *kq, const uint16_t *ks, const int8_t *vq,
                             const uint16_t *vs, long ncells, const int32_t *ids, long nq, long k,
                             double *out, int nthreads);

@@ -419,8 +419,94 @@ def pin_attn_padding_and_order(o) -> None:
     assert np.allclose(a, b, rtol=0, atol=1e-13 * np.abs(a).max())
 
 
+# ---- block summary keys -----------------------------------------------------
+# The reading pinned (the pages time an "append" step but define no summary
+# function, so the definition itself stays a reading): a block's key is the
+# element-wise mean of its present cells (int8 x binary16 scale per cell);
+# the int8 form has scale binary16(max|key| / 127) and codes rint(key / s).
+
+def pin_float_to_half(o) -> None:
+    """The oracle's binary32 -> binary16 rounding against numpy's, on
+    normals, subnormals, exact ties and the largest finite values."""
+    r = _rng(201)
+    x = (r.standard_normal(30000) * 10.0 ** r.integers(-9, 5, 30000)).astype(np.float32)
+    ties = np.array([1 + 2 ** -11, 1 + 3 * 2 ** -11, 2 ** -24 * 0.5, 2 ** -24 * 1.5, 2 ** -24 * 2.5,
+                     65504.0, 65519.0, 2 ** -14, 2 ** -14 * (1 - 2 ** -11), 0.0, -0.0, -(1 + 2 ** -11)],
+                    dtype=np.float32)
+    for v in np.concatenate([x, ties, -ties]):
+        assert o.float_to_half(v) == int(np.float16(v).view(np.uint16)), float(v)
+
+
+def _summary_cells(rows, scales):
+    return np.asarray(rows, dtype=np.int8), _half_bits(scales)
+
+
+def pin_summary_exact_means(o) -> None:
+    """Cells whose sums are exact in fp32 (small integers, power-of-two
+    scales): the key is the exact mean over the present cells (4, 2 or 1 of
+    them), and a block with no present cell is zero."""
+    from fractions import Fraction
+    r = _rng(202)
+    rows = r.integers(-100, 101, (11, D))
+    scales = 2.0 ** r.integers(-6, 2, 11)
+    kq, ks = _summary_cells(rows, scales)
+    key, _, _ = o.block_summary(kq, ks, 0, 4)           # blocks of 4, 4, 3 cells and none
+    for b, n in ((0, 4), (1, 4)):
+        for d in range(D):
+            want = sum(Fraction(int(rows[4 * b + t, d])) * Fraction(float(scales[4 * b + t])) for t in range(n)) / n
+            assert Fraction(float(key[b, d])) == want, (b, d)
+    k2, _, _ = o.block_summary(kq[:10], ks[:10], 2, 3)  # block 2 holds cells 8, 9
+    for d in range(D):
+        want = (Fraction(int(rows[8, d])) * Fraction(float(scales[8])) +
+                Fraction(int(rows[9, d])) * Fraction(float(scales[9]))) / 2
+        assert Fraction(float(k2[0, d])) == want, d
+    k1, _, _ = o.block_summary(kq[:9], ks[:9], 2, 3)    # block 2 holds cell 8 only
+    assert np.array_equal(k1[0], rows[8].astype(np.float32) * np.float32(scales[8]))
+    assert np.all(key[3] == 0.0)
+
+
+def pin_summary_codes(o) -> None:
+    """int8 form: the scale is numpy's binary16 of max|key| / 127, every code
+    is within half a step of the key, the largest |key| gets |code| 127, and
+    a zero block gets scale 0 and zero codes."""
+    r = _rng(203)
+    kq = r.integers(-127, 128, (64, D)).astype(np.int8)
+    ks = _half_bits(np.exp(r.uniform(np.log(1e-3), np.log(1e-1), 64)))
+    kq[40:44] = 0
+    key, q8, sc = o.block_summary(kq, ks, 0, 16)
+    for b in range(16):
+        top = np.float32(np.abs(key[b]).max())
+        assert sc[b] == int(np.float16(top / np.float32(127.0)).view(np.uint16)), b
+        s = float(np.uint16(sc[b]).view(np.float16))
+        if top == 0:
+            assert s == 0 and np.all(q8[b] == 0)
+            continue
+        assert np.all(np.abs(q8[b].astype(np.float64) * s - key[b]) <= 0.5 * s * (1 + 2 ** -20)), b
+        assert abs(int(q8[b][np.argmax(np.abs(key[b]))])) == 127
+    assert np.all(q8[10] == 0) and sc[10] == 0          # cells 40..43 are zero
+
+
+def pin_summary_padding(o) -> None:
+    """A block's key depends only on its own present cells: the same block
+    from a longer or a cut pool, and blocks past the cells are zero."""
+    kq, _, ks, _ = _attn_case(23, 204)
+    a = o.block_summary(kq, ks, 0, 8)
+    b = o.block_summary(kq[:20], ks[:20], 0, 8)
+    for x, y in zip(a, b):
+        assert np.array_equal(x[:5], y[:5])               # blocks 0..4 whole in both
+    assert not np.array_equal(a[0][5], b[0][5])           # block 5: cells 20..22 against none
+    assert np.all(b[0][5:] == 0) and np.all(b[1][5:] == 0) and np.all(b[2][5:] == 0)
+    c = o.block_summary(kq, ks, 3, 6)
+    for x, y in zip(a, c):
+        assert np.array_equal(x[3:6], y)                  # a sub-range gives the same rows
+
+
 ALL_PINS = [
     pin_brute_force_topk,
+    pin_float_to_half,
+    pin_summary_exact_means,
+    pin_summary_codes,
+    pin_summary_padding,
     pin_attn_single_cell,
     pin_attn_uniform_weights,
     pin_attn_two_cells_logistic,

@@ -38,6 +38,13 @@ MUTANTS = {
     "attn_head_stride": ("((size_t)i * QSA_H + (size_t)h) * QSA_D", "((size_t)i * QSA_H) * QSA_D"),
     "attn_unnormalised": ("const double p = w[t] / total;", "const double p = w[t];"),
     "attn_exponent_sign": ("w[t] = exp(w[t] - top);", "w[t] = exp(top - w[t]);"),
+    "summary_divide_by_4": ("mean[d] = n > 0 ? sum / (float)n : 0.0f;", "mean[d] = n > 0 ? sum / 4.0f : 0.0f;"),
+    "summary_scale_255": ("float_to_half_rne(top / 127.0f)", "float_to_half_rne(top / 255.0f)"),
+    "summary_truncated_codes": ("rintf(mean[d] / s)", "truncf(mean[d] / s)"),
+    "summary_cell_stride": ("const long c = 4 * b + t;", "const long c = 2 * b + t;"),
+    "summary_scale_dropped": ("(float)kq[(size_t)c * QSA_D + d] * (float)qsa_oracle_half_to_double(ks[c])",
+                              "(float)kq[(size_t)c * QSA_D + d]"),
+    "half_no_rounding": ("if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u;", ""),
 }
 
 
