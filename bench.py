@@ -366,6 +366,59 @@ def attention_side_measurement(dev, stream):
     return out
 
 
+def summary_side_measurement(dev, stream):
+    """qsa_block_summary: every summary key (fp32 and int8 forms) of a
+    262,144-cell pool rebuilt (65,536 blocks, L2 flushed before each call),
+    and the one-block refresh after a decode append (per call of a CUDA graph
+    of 20 calls)."""
+    import torch
+    import sparse_attention_kv_qsa_gb300 as qsa
+    from sparse_attention_kv_qsa_gb300 import workloads as w
+    A = w.attn_case(1, 262144, 1)
+    kc = torch.from_numpy(np.ascontiguousarray(A.kc)).to(dev)
+    ks = torch.from_numpy(A.ks.view(np.int16)).to(dev)
+    nb = 65536
+    key = torch.empty((nb, 128), dtype=torch.float32, device=dev)
+    q8 = torch.empty((nb, 128), dtype=torch.int8, device=dev)
+    sc = torch.empty((nb,), dtype=torch.int16, device=dev)
+    full = lambda: qsa.block_summary(kc, ks, 0, nb, kblk=key, kblk_q8=q8, kblk_scale_f16=sc)
+    one = lambda: qsa.block_summary(kc, ks, nb - 1, nb, kblk=key, kblk_q8=q8, kblk_scale_f16=sc)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    for _ in range(5):
+        full()
+    torch.cuda.synchronize()
+    ts = []
+    for i in range(30):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        full()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(1e3 * e0.elapsed_time(e1))
+    us = statistics.median(ts)
+    bytes_ = 262144 * (128 + 2) + nb * (128 * 4 + 128 + 2)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        one()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(20):
+                one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return {"workload": "block summary keys (fp32 + int8 forms) of a 262,144-cell int8 pool", "unit": "us",
+            "rebuild_65536_blocks_us_p50": us, "algorithmic_bytes": bytes_, "hbm_gbs": bytes_ / us / 1e3,
+            "append_one_block_graph_us": 1e3 * e0.elapsed_time(e1) / 20}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -385,6 +438,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped side measurement")
     ap.add_argument("--no-ksweep", action="store_true", help="skip the k sweep (64, 256, 1024) side measurement")
     ap.add_argument("--no-attn", action="store_true", help="skip the attention side measurement")
+    ap.add_argument("--no-summary", action="store_true", help="skip the summary-key side measurement")
     ap.add_argument("--attn-launches", type=int, default=0,
                     help="only launch qsa_sparse_attn this many times on 256 queries x k=512 over 262,144 "
                          "cells (a short run for a profiler to capture), then exit")
@@ -618,6 +672,8 @@ def main():
         line["decode"] = decode_side_measurement(dev, stream)
     if rank == 0 and not args.no_attn:
         line["attention"] = attention_side_measurement(dev, stream)
+    if rank == 0 and not args.no_summary:
+        line["summary"] = summary_side_measurement(dev, stream)
 
     if rank == 0 and not args.no_ksweep and path == "gmax":
         # The headline workload's k sweep, same calls and flushes, 200 steps

@@ -232,6 +232,32 @@ qsa_status qsa_sparse_attn(const float *q, const int8_t *k_cells, const uint16_t
                            int nq, int k, float *out, cudaStream_t stream);
 
 /*
+ * Block summary keys from int8 KV cells, for blocks block_begin ..
+ * block_end-1 (after an append: block_begin = old ncells / 4, block_end =
+ * ceil(new ncells / 4)):
+ *   kblk[b][d]    = (sum over the present cells c = 4b .. 4b+3 (< ncells) of
+ *                    k_cells[c][d] * k_scale[c]) / (number of present cells)
+ *   kblk_scale[b] = binary16(max_d |kblk[b][d]| / 127), round to nearest even
+ *   kblk_q8[b][d] = rint(kblk[b][d] / kblk_scale[b])  (0 when the scale is 0)
+ * computed in fp32 in that order (IEEE single operations), so the int8 form
+ * is reproducible bit for bit; a block with no present cell gets zeros.
+ * k_cells  int8 [ncells][128], 16-byte aligned; k_scale_f16 binary16 [ncells],
+ *          2-byte aligned (both may be NULL when ncells == 0).
+ * kblk     fp32 [>= block_end][128] (row b written), 16-byte aligned, or NULL.
+ * kblk_q8  int8 [>= block_end][128] and kblk_scale_f16 binary16 [>= block_end]
+ *          (the qsa_block_scores_q8 key layout), both or neither.
+ * ncells < 0, block_begin < 0, block_end < block_begin, or no output returns
+ * QSA_ERR_INVALID; an empty range is a no-op. Allocates nothing.
+ * Passage: "#3108 optimize exact QSA block scoring and top-k selection on
+ * gfx12", the Microbenchmark & Parity Evidence table (the decode layer's
+ * "append" step). The pages do not define the summary function: the mean of
+ * the present cells and the int8 form are readings.
+ */
+qsa_status qsa_block_summary(const int8_t *k_cells, const uint16_t *k_scale_f16, int ncells, int block_begin,
+                             int block_end, float *kblk, int8_t *kblk_q8, uint16_t *kblk_scale_f16,
+                             cudaStream_t stream);
+
+/*
  * Reads and clears the current device's error word: nonzero when a kernel
  * of this library gave up a bounded wait (its outputs are then invalid).
  * Synchronises `stream`. *code receives the word.

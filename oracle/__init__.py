@@ -4,9 +4,12 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package. The product path never does: it runs
 the CUDA library or fails.
 
-The arithmetic lives in ``qsa_oracle.c`` (FP64 scores, full-sort top-k, see
-its header comment for the definition and the passages it follows). This
-module compiles it with the host C compiler and marshals numpy arrays.
+The arithmetic lives in ``qsa_oracle.c`` (FP64 scores, full-sort top-k, FP64
+attention over the selected blocks, fp32 block summary keys; see its header
+comment for the definitions and the passages they follow). The block summary
+keys are "parity unpinned" as to their definition (the pages define no
+summary function; the mean of the cells is a reading). This module compiles
+the C source with the host C compiler and marshals numpy arrays.
 """
 
 from __future__ import annotations

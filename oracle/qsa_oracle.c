@@ -31,6 +31,12 @@
  * ascending, and fill the remaining k - active slots (if any) with -1. A NaN
  * score counts as -infinity (so it ties with -inf and ranks below every
  * finite score); -0.0 and +0.0 compare equal (and so tie).
+ *
+ * Also here: the attention over the selected blocks' cells (FP64) and the
+ * block summary keys (an fp32 restatement). The summary keys are "parity
+ * unpinned" as to their definition: the pages time an append step but never
+ * define how a block's key is built from its cells, so the function below is
+ * a reading; its arithmetic is pinned, the definition is not.
  */
 #include "qsa_oracle.h"
 

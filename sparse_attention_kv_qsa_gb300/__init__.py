@@ -1,5 +1,5 @@
-"""Exact QSA block selection on GB300: block scoring, per-query top-k, and
-attention over the selected blocks.
+"""Exact QSA block selection on GB300: block scoring, per-query top-k,
+attention over the selected blocks, and block summary keys on append.
 
 The computation lives in ``libqsa.so`` (CUDA kernels for sm_103a behind the C
 ABI of ``include/qsa.h``); ``qsa`` is its Python binding and ``workloads``
@@ -17,6 +17,7 @@ from .qsa import (  # noqa: F401
     block_select,
     block_select_small,
     block_select_static,
+    block_summary,
     block_topk,
     block_topk_gmax,
     groups,

@@ -231,6 +231,23 @@ qsa_status qsa_sparse_attn(const float *q, const int8_t *k_cells, const uint16_t
                                              stream));
 }
 
+qsa_status qsa_block_summary(const int8_t *k_cells, const uint16_t *k_scale_f16, int ncells, int block_begin,
+                             int block_end, float *kblk, int8_t *kblk_q8, uint16_t *kblk_scale_f16,
+                             cudaStream_t stream) {
+    if (ncells < 0 || block_begin < 0 || block_end < block_begin) return QSA_ERR_INVALID;
+    if (kblk == nullptr && kblk_q8 == nullptr) return QSA_ERR_INVALID;
+    if ((kblk_q8 == nullptr) != (kblk_scale_f16 == nullptr)) return QSA_ERR_INVALID;
+    if (block_end == block_begin) return QSA_OK;
+    if (ncells > 0 && (k_cells == nullptr || k_scale_f16 == nullptr || !aligned16(k_cells) ||
+                       (reinterpret_cast<uintptr_t>(k_scale_f16) & 1u) != 0))
+        return QSA_ERR_INVALID;
+    if ((kblk != nullptr && !aligned16(kblk)) || (kblk_q8 != nullptr && !aligned16(kblk_q8)) ||
+        (kblk_scale_f16 != nullptr && (reinterpret_cast<uintptr_t>(kblk_scale_f16) & 1u) != 0))
+        return QSA_ERR_INVALID;
+    return from_cuda(qsa::launch_block_summary(k_cells, k_scale_f16, ncells, block_begin, block_end, kblk, kblk_q8,
+                                               kblk_scale_f16, stream));
+}
+
 qsa_status qsa_get_device_error(uint32_t *code, cudaStream_t stream) {
     if (code == nullptr) return QSA_ERR_INVALID;
     *code = 0;

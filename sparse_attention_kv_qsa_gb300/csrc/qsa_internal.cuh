@@ -56,6 +56,11 @@ cudaError_t launch_topk(const float *scores, const uint32_t *gmax, int nq, int a
 cudaError_t launch_select_decode(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,
                                  int nq, int active, int k, float *scores, int32_t *ids, cudaStream_t stream);
 
+// Summary keys of blocks b0 .. b1-1 from int8 cells (csrc/summary.cu); key
+// (fp32 rows) and kq8 + kscale (int8 rows, binary16 scales) may each be null.
+cudaError_t launch_block_summary(const int8_t *kc, const uint16_t *ks, int ncells, int b0, int b1, float *key,
+                                 int8_t *kq8, uint16_t *kscale, cudaStream_t stream);
+
 // Attention of each query's 4 heads over the int8 KV cells of its listed
 // blocks (csrc/attn.cu).
 cudaError_t launch_sparse_attn(const float *q, const int8_t *kc, const uint16_t *ks, const int8_t *vc,

@@ -1,0 +1,107 @@
+// Block summary keys, brought up to date when cells are appended.
+//
+//   key[b][d] = (sum over the present cells c = 4b .. 4b+3 (< ncells) of
+//                kq[c][d] * ks[c]) / n          (n = number of present cells)
+//   s[b]      = binary16(max_d |key[b][d]| / 127)   (round to nearest even)
+//   kq8[b][d] = rint(key[b][d] / s[b])              (0 when s[b] is 0)
+//
+// Passage: "#3108 optimize exact QSA block scoring and top-k selection on
+// gfx12", the Microbenchmark & Parity Evidence table (the decode layer times
+// "append + scores + topk + attn"). The pages do not define the summary
+// function; the mean of the block's present cells is the reading taken, and
+// the int8 form (one binary16 scale per block) is the decode scorer's key
+// format. The integer codes are decided by float arithmetic, so the sum,
+// the division by n, the scale and the code divisions are single IEEE
+// operations in one fixed order (each product of an int8 by a binary16 scale
+// is exact in fp32).
+//
+// GB300 mapping: an HBM-bound elementwise pass. One warp per block; lane l
+// owns d = 4l .. 4l+3, reads one 4-byte word of each present cell's row (a
+// 128-byte line per row and warp) and writes one 16-byte key word and one
+// 4-byte code word; the block's max |key| is a warp max over the float bit
+// patterns (non-negative floats order like their bits).
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "qsa_internal.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int SUM_WARPS = 8;
+
+__global__ void __launch_bounds__(SUM_WARPS * 32)
+    summary_kernel(const int8_t *__restrict__ kc, const __half *__restrict__ ks, long long ncells, long long b0,
+                   long long nblk, float *__restrict__ key, int8_t *__restrict__ kq8,
+                   __half *__restrict__ kscale) {
+    grid_dependency_wait();   // the cells may come from the previous grid (the append itself)
+    const int lane = threadIdx.x & 31;
+    const long long j = static_cast<long long>(blockIdx.x) * SUM_WARPS + (threadIdx.x >> 5);
+    if (j >= nblk) return;   // the whole warp
+    const long long b = b0 + j;
+    long long n = ncells - 4 * b;
+    n = n > 4 ? 4 : (n < 0 ? 0 : n);
+
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        if (t < n) {
+            w[t] = __ldg(reinterpret_cast<const uint32_t *>(kc + (4 * b + t) * D) + lane);
+            sc[t] = __half2float(ks[4 * b + t]);
+        }
+    }
+    float m[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            if (t < n)
+                sum = __fadd_rn(sum, __fmul_rn(static_cast<float>(static_cast<int8_t>((w[t] >> (8 * e)) & 0xFFu)),
+                                               sc[t]));
+        m[e] = n > 0 ? __fdiv_rn(sum, static_cast<float>(n)) : 0.0f;
+    }
+    if (key != nullptr)
+        *reinterpret_cast<float4 *>(key + b * D + 4 * lane) = make_float4(m[0], m[1], m[2], m[3]);
+    if (kq8 != nullptr) {
+        float top = fmaxf(fmaxf(fabsf(m[0]), fabsf(m[1])), fmaxf(fabsf(m[2]), fabsf(m[3])));
+        top = __uint_as_float(__reduce_max_sync(FULL_MASK, __float_as_uint(top)));
+        const __half sh = __float2half_rn(__fdiv_rn(top, 127.0f));
+        const float s = __half2float(sh);
+        uint32_t codes = 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            int c = s > 0.0f ? __float2int_rn(__fdiv_rn(m[e], s)) : 0;
+            c = c > 127 ? 127 : (c < -127 ? -127 : c);
+            codes |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * e);
+        }
+        *reinterpret_cast<uint32_t *>(kq8 + b * D + 4 * lane) = codes;
+        if (lane == 0) kscale[b] = sh;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_block_summary(const int8_t *kc, const uint16_t *ks, int ncells, int b0, int b1, float *key,
+                                 int8_t *kq8, uint16_t *kscale, cudaStream_t stream) {
+    const long long nblk = static_cast<long long>(b1) - b0;
+    if (nblk <= 0) return cudaSuccess;
+    const long long grid = (nblk + SUM_WARPS - 1) / SUM_WARPS;
+    if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(SUM_WARPS * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, summary_kernel, kc, reinterpret_cast<const __half *>(ks),
+                              static_cast<long long>(ncells), static_cast<long long>(b0), nblk, key, kq8,
+                              reinterpret_cast<__half *>(kscale));
+}
+
+}  // namespace qsa

@@ -25,8 +25,8 @@ QSA_OK, QSA_ERR_INVALID, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
 
 EXPORTED = ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
             "qsa_block_scores_gmax", "qsa_block_scores_q8_gmax", "qsa_block_group_max", "qsa_block_topk_gmax",
-            "qsa_block_select_static", "qsa_block_select_small", "qsa_sparse_attn", "qsa_get_device_error",
-            "qsa_status_string")
+            "qsa_block_select_static", "qsa_block_select_small", "qsa_sparse_attn", "qsa_block_summary",
+            "qsa_get_device_error", "qsa_status_string")
 
 
 class QSAError(RuntimeError):
@@ -63,13 +63,14 @@ def lib() -> ctypes.CDLL:
         L.qsa_block_select_static.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
         L.qsa_block_select_small.argtypes = [vp, vp, vp, vp, i, i, i, i, vp, vp, vp]
         L.qsa_sparse_attn.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, vp, vp]
+        L.qsa_block_summary.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp]
         L.qsa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
         L.qsa_status_string.argtypes = [i]
         L.qsa_status_string.restype = ctypes.c_char_p
         for f in ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
                   "qsa_block_scores_gmax", "qsa_block_scores_q8_gmax", "qsa_block_topk_gmax",
                   "qsa_block_group_max", "qsa_block_select_static", "qsa_block_select_small",
-                  "qsa_sparse_attn", "qsa_get_device_error"):
+                  "qsa_sparse_attn", "qsa_block_summary", "qsa_get_device_error"):
             getattr(L, f).restype = i
         _lib = L
     return _lib
@@ -355,6 +356,35 @@ def sparse_attn(q: torch.Tensor, k_cells: torch.Tensor, k_scale_f16: torch.Tenso
     _check(lib().qsa_sparse_attn(_ptr(q), _ptr(k_cells), _ptr(k_scale_f16), _ptr(v_cells), _ptr(v_scale_f16),
                                  ncells, _ptr(ids), nq, k, _ptr(out), _stream(q)), "qsa_sparse_attn")
     return out
+
+
+def block_summary(k_cells: torch.Tensor, k_scale_f16: torch.Tensor, block_begin: int, block_end: int,
+                  kblk: torch.Tensor | None = None, kblk_q8: torch.Tensor | None = None,
+                  kblk_scale_f16: torch.Tensor | None = None) -> None:
+    """``qsa_block_summary``: rewrites rows ``block_begin .. block_end-1`` of the
+    summary keys from the int8 cells (``k_cells [ncells, 128]``, binary16
+    scales ``[ncells]``): fp32 ``kblk`` and/or int8 ``kblk_q8`` with binary16
+    ``kblk_scale_f16`` (capacity buffers with at least ``block_end`` rows)."""
+    _need(k_cells, "k_cells", torch.int8, 2)
+    ncells = k_cells.shape[0]
+    if k_cells.shape[1] != 128:
+        raise ValueError("k_cells must be [ncells, 128]")
+    if (not k_scale_f16.is_cuda or k_scale_f16.dim() != 1 or k_scale_f16.shape[0] != ncells
+            or k_scale_f16.element_size() != 2 or not k_scale_f16.is_contiguous()):
+        raise ValueError(f"k_scale_f16 must be a 1-d CUDA tensor of {ncells} binary16 values")
+    if kblk is not None:
+        _need(kblk, "kblk", torch.float32, 2)
+        if kblk.shape[1] != 128 or kblk.shape[0] < block_end:
+            raise ValueError(f"kblk must be [>= {block_end}, 128]")
+    if kblk_q8 is not None:
+        _need(kblk_q8, "kblk_q8", torch.int8, 2)
+        if kblk_q8.shape[1] != 128 or kblk_q8.shape[0] < block_end:
+            raise ValueError(f"kblk_q8 must be [>= {block_end}, 128]")
+        if (kblk_scale_f16 is None or not kblk_scale_f16.is_cuda or kblk_scale_f16.dim() != 1
+                or kblk_scale_f16.shape[0] < block_end or kblk_scale_f16.element_size() != 2):
+            raise ValueError(f"kblk_scale_f16 must be a 1-d CUDA tensor of >= {block_end} binary16 values")
+    _check(lib().qsa_block_summary(_ptr(k_cells), _ptr(k_scale_f16), ncells, block_begin, block_end, _ptr(kblk),
+                                   _ptr(kblk_q8), _ptr(kblk_scale_f16), _stream(k_cells)), "qsa_block_summary")
 
 
 def device_error(device: torch.device | None = None) -> int:
