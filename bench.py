@@ -439,6 +439,9 @@ def main():
     ap.add_argument("--no-ksweep", action="store_true", help="skip the k sweep (64, 256, 1024) side measurement")
     ap.add_argument("--no-attn", action="store_true", help="skip the attention side measurement")
     ap.add_argument("--no-summary", action="store_true", help="skip the summary-key side measurement")
+    ap.add_argument("--summary-launches", type=int, default=0,
+                    help="only launch qsa_block_summary this many times over a 262,144-cell pool (65,536 "
+                         "blocks, both key forms; a short run for a profiler to capture), then exit")
     ap.add_argument("--attn-launches", type=int, default=0,
                     help="only launch qsa_sparse_attn this many times on 256 queries x k=512 over 262,144 "
                          "cells (a short run for a profiler to capture), then exit")
@@ -460,6 +463,18 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.summary_launches > 0:
+        A = workloads.attn_case(1, 262144, 1)
+        kc = torch.from_numpy(np.ascontiguousarray(A.kc)).to(dev)
+        ks = torch.from_numpy(A.ks.view(np.int16)).to(dev)
+        key = torch.empty((65536, 128), dtype=torch.float32, device=dev)
+        q8 = torch.empty((65536, 128), dtype=torch.int8, device=dev)
+        sc = torch.empty((65536,), dtype=torch.int16, device=dev)
+        for _ in range(args.summary_launches):
+            qsa.block_summary(kc, ks, 0, 65536, kblk=key, kblk_q8=q8, kblk_scale_f16=sc)
+        torch.cuda.synchronize()
+        print(json.dumps({"summary_launches": args.summary_launches, "workload": "262,144 cells"}), flush=True)
+        return
     if args.attn_launches > 0:
         A = workloads.attn_case(256, 262144, 512)
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
