@@ -127,10 +127,7 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst_smem, const void *src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Release store / acquire load of a global word at GPU scope.
-__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
+// Acquire load of a global word at GPU scope.
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -144,15 +141,15 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v
     return old;
 }
 
-// Waits (bounded by WAIT_LIMIT_NS) until the word at p differs from `old`,
+// Waits (bounded by WAIT_LIMIT_NS) until the word at p is at least `target`,
 // with acquire semantics at GPU scope. Returns false if it gave up.
-__device__ __forceinline__ bool wait_word_changes(const uint32_t *p, uint32_t old) {
-    if (ld_acquire_gpu(p) != old) return true;
+__device__ __forceinline__ bool wait_word_reaches(const uint32_t *p, uint32_t target) {
+    if (ld_acquire_gpu(p) >= target) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
-            if (ld_acquire_gpu(p) != old) return true;
+            if (ld_acquire_gpu(p) >= target) return true;
         if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
     }
 }

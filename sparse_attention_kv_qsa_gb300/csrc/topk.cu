@@ -779,15 +779,17 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
 
 // Fused decode select (nq <= 4): one cooperative launch scores every key row
 // (and the group maxima) across the whole grid, then its first nq CTAs each
-// take one row's top-k. The CTAs release their scores through an arrival
-// counter; the last to arrive resets the counter and advances a generation
-// word that the top-k CTAs wait on (bounded; a cooperative launch keeps every
-// CTA resident, so all of them arrive). Each CTA reads the generation before
-// it arrives, and it cannot advance before every CTA has arrived, so all of
-// them see the same value; the words need no clearing between launches. The
+// take one row's top-k. Each CTA releases its scores with an acquire-release
+// atomic increment of an arrival counter, and the top-k CTAs wait (bounded; a
+// cooperative launch keeps every CTA resident, so all of them arrive) until
+// they read the full count with an acquire load. Two counters alternate by
+// the parity of a generation word: each CTA reads the generation before it
+// arrives, and only the last arrival advances it, so all of them use the
+// same counter; the last arrival also clears the other counter, the one the
+// next launch uses (this launch's counter keeps its count until then). The
 // group maxima live in a fixed device array, so the call allocates nothing.
 // Launches of this kernel on one device therefore run one at a time.
-__device__ uint32_t g_decode_sync[2];   // arrivals, generation
+__device__ uint32_t g_decode_sync[3];   // arrivals (two, by generation parity), generation
 static __device__ __align__(256) uint32_t g_decode_gmax[SMALL_NQ_MAX * (MAX_ACTIVE / GROUP_BLOCKS)];
 
 template <int NQ, bool kInt8>
@@ -801,7 +803,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
     grid_dependency_wait();   // q and the keys may come from the previous grid
     grid_launch_dependents();
     uint32_t gen = 0u;
-    if (threadIdx.x == 0) gen = ld_acquire_gpu(&g_decode_sync[1]);
+    if (threadIdx.x == 0) gen = ld_acquire_gpu(&g_decode_sync[2]);
     dec_build_queries<NQ, ROW_THREADS>(q, nq, qs);
     __syncthreads();
     const long long nchunks = (static_cast<long long>(active) + ROWS - 1) / ROWS;
@@ -809,17 +811,16 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         dec_score_chunk<NQ, kInt8, ROW_THREADS>(qs, c, kblk, kq8, kscale, nq, active, scores, g_decode_gmax, gk);
     if (threadIdx.x == 0) {
         // The arrival releases this CTA's scores and group maxima (ordered
-        // before it by the CTA barrier that ends the scoring); the last one
-        // also acquires every other CTA's through the counter, publishes them
-        // with the generation's release store, and then resets the counter
-        // (read again only by the next launch, after this grid completes).
-        if (atom_add_acq_rel_gpu(&g_decode_sync[0], 1u) == gridDim.x - 1) {
-            st_release_gpu(&g_decode_sync[1], gen + 1u);
-            g_decode_sync[0] = 0u;
+        // before it by the CTA barrier that ends the scoring); a top-k CTA's
+        // acquire load that reads the full count synchronises with every
+        // arrival.
+        if (atom_add_acq_rel_gpu(&g_decode_sync[gen & 1u], 1u) == gridDim.x - 1) {
+            g_decode_sync[(gen + 1u) & 1u] = 0u;   // read by the next launch only, after this grid completes
+            g_decode_sync[2] = gen + 1u;
         }
     }
     if (blockIdx.x >= static_cast<unsigned>(nq)) return;   // the whole CTA
-    if (threadIdx.x == 0 && !wait_word_changes(&g_decode_sync[1], gen)) atomicOr(&g_topk_error, 2u);
+    if (threadIdx.x == 0 && !wait_word_reaches(&g_decode_sync[gen & 1u], gridDim.x)) atomicOr(&g_topk_error, 2u);
     __syncthreads();
     topk_row<true>(scores, g_decode_gmax, active, k, ids, blockIdx.x);
 }
