@@ -31,24 +31,26 @@ namespace {
 constexpr int SUM_WARPS = 8;
 
 __global__ void __launch_bounds__(SUM_WARPS * 32)
-    summary_kernel(const int8_t *__restrict__ kc, const __half *__restrict__ ks, long long ncells, long long b0,
-                   long long nblk, float *__restrict__ key, int8_t *__restrict__ kq8,
-                   __half *__restrict__ kscale) {
+    summary_kernel(const int8_t *__restrict__ kc, const __half *__restrict__ ks, int ncells, int b0, int nblk,
+                   float *__restrict__ key, int8_t *__restrict__ kq8, __half *__restrict__ kscale) {
     grid_dependency_wait();   // the cells may come from the previous grid (the append itself)
     const int lane = threadIdx.x & 31;
-    const long long j = static_cast<long long>(blockIdx.x) * SUM_WARPS + (threadIdx.x >> 5);
+    const int j = static_cast<int>(blockIdx.x) * SUM_WARPS + (threadIdx.x >> 5);
     if (j >= nblk) return;   // the whole warp
-    const long long b = b0 + j;
-    long long n = ncells - 4 * b;
+    const int b = b0 + j;
+    int n = ncells - 4 * b;   // present cells (ncells and 4b + 4 fit in int: checked by the host)
     n = n > 4 ? 4 : (n < 0 ? 0 : n);
 
+    // One 64-bit base per block; the 4 rows and scales sit at fixed offsets.
+    const uint32_t *rows = reinterpret_cast<const uint32_t *>(kc + static_cast<size_t>(b) * (4 * D)) + lane;
+    const __half *scl = ks + static_cast<size_t>(b) * 4;
     uint32_t w[4] = {0u, 0u, 0u, 0u};
     float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
         if (t < n) {
-            w[t] = __ldg(reinterpret_cast<const uint32_t *>(kc + (4 * b + t) * D) + lane);
-            sc[t] = __half2float(ks[4 * b + t]);
+            w[t] = __ldg(rows + t * (D / 4));
+            sc[t] = __half2float(scl[t]);
         }
     }
     float m[4];
@@ -62,8 +64,8 @@ __global__ void __launch_bounds__(SUM_WARPS * 32)
                                                sc[t]));
         m[e] = n > 0 ? __fdiv_rn(sum, static_cast<float>(n)) : 0.0f;
     }
-    if (key != nullptr)
-        *reinterpret_cast<float4 *>(key + b * D + 4 * lane) = make_float4(m[0], m[1], m[2], m[3]);
+    const size_t out = static_cast<size_t>(b) * D + 4 * lane;
+    if (key != nullptr) *reinterpret_cast<float4 *>(key + out) = make_float4(m[0], m[1], m[2], m[3]);
     if (kq8 != nullptr) {
         float top = fmaxf(fmaxf(fabsf(m[0]), fabsf(m[1])), fmaxf(fabsf(m[2]), fabsf(m[3])));
         top = __uint_as_float(__reduce_max_sync(FULL_MASK, __float_as_uint(top)));
@@ -76,7 +78,7 @@ __global__ void __launch_bounds__(SUM_WARPS * 32)
             c = c > 127 ? 127 : (c < -127 ? -127 : c);
             codes |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * e);
         }
-        *reinterpret_cast<uint32_t *>(kq8 + b * D + 4 * lane) = codes;
+        *reinterpret_cast<uint32_t *>(kq8 + out) = codes;
         if (lane == 0) kscale[b] = sh;
     }
 }
@@ -87,6 +89,7 @@ cudaError_t launch_block_summary(const int8_t *kc, const uint16_t *ks, int ncell
                                  int8_t *kq8, uint16_t *kscale, cudaStream_t stream) {
     const long long nblk = static_cast<long long>(b1) - b0;
     if (nblk <= 0) return cudaSuccess;
+    if (4LL * b1 + 4 > 0x7FFFFFFFLL) return cudaErrorInvalidValue;   // cell indices stay in int
     const long long grid = (nblk + SUM_WARPS - 1) / SUM_WARPS;
     if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -100,7 +103,7 @@ cudaError_t launch_block_summary(const int8_t *kc, const uint16_t *ks, int ncell
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, summary_kernel, kc, reinterpret_cast<const __half *>(ks),
-                              static_cast<long long>(ncells), static_cast<long long>(b0), nblk, key, kq8,
+                              ncells, b0, static_cast<int>(nblk), key, kq8,
                               reinterpret_cast<__half *>(kscale));
 }
 
