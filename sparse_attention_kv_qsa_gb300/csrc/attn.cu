@@ -90,8 +90,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     __shared__ AttnShared sh;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t rank = csize > 1 ? cluster_ctarank() : 0u;
-    const long long i = blockIdx.x / csize;   // query
-    const int32_t *ids_i = ids + i * k;
+    const int i = static_cast<int>(blockIdx.x) / csize;   // query
+    const int32_t *ids_i = ids + static_cast<size_t>(i) * k;
     const int nblocks = (ncells + 3) / 4;
 
     grid_dependency_wait();   // q, the cells and the ids may come from the previous grid
@@ -99,35 +99,41 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     float qv[HEADS][4];       // this lane's slice d = 4 lane .. +3 of each head's query
 #pragma unroll
     for (int h = 0; h < HEADS; ++h) {
-        const float4 t = __ldg(reinterpret_cast<const float4 *>(q + (i * HEADS + h) * D) + lane);
+        const float4 t = __ldg(reinterpret_cast<const float4 *>(q + (static_cast<size_t>(i) * HEADS + h) * D) + lane);
         qv[h][0] = t.x, qv[h][1] = t.y, qv[h][2] = t.z, qv[h][3] = t.w;
     }
 
-    const long long nsteps = (static_cast<long long>(k) + STEP_IDS - 1) / STEP_IDS;
-    const long long wg = static_cast<long long>(rank) * AT_WARPS + warp;
-    const long long nw = static_cast<long long>(csize) * AT_WARPS;
+    const int nsteps = (k - 1) / STEP_IDS + 1;   // k >= 1
+    const int wg = static_cast<int>(rank) * AT_WARPS + warp;
+    const int nw = csize * AT_WARPS;
 
     // A step's data: its two listed blocks (-1 when past k, padding or past
     // the last block) and word `lane` of each of their cells' K and V rows
-    // (0 for dead cells).
+    // (0 for dead cells). Block and cell indices are 32-bit (the host keeps
+    // ncells + 4 within int); each block's rows are addressed from one base.
     struct Step {
         int b[STEP_IDS];
         uint32_t kw[STEP_CELLS], vw[STEP_CELLS];
     };
-    auto load_step = [&](long long st, Step &s) {
+    auto load_step = [&](int st, Step &s) {
 #pragma unroll
         for (int j = 0; j < STEP_IDS; ++j) {
-            const long long slot = STEP_IDS * st + j;
+            const int slot = STEP_IDS * st + j;
             const int b = st < nsteps && slot < k ? __ldg(ids_i + slot) : -1;
             s.b[j] = b >= 0 && b < nblocks ? b : -1;
         }
 #pragma unroll
-        for (int c = 0; c < STEP_CELLS; ++c) {
-            const int b = s.b[c >> 2];
-            const long long cell = 4LL * b + (c & 3);
-            const bool live = b >= 0 && cell < ncells;
-            s.kw[c] = live ? __ldg(reinterpret_cast<const uint32_t *>(kc + cell * D) + lane) : 0u;
-            s.vw[c] = live ? __ldg(reinterpret_cast<const uint32_t *>(vc + cell * D) + lane) : 0u;
+        for (int j = 0; j < STEP_IDS; ++j) {
+            const int b = s.b[j];
+            const size_t base = static_cast<size_t>(b < 0 ? 0 : b) * (4 * D);
+            const uint32_t *krow = reinterpret_cast<const uint32_t *>(kc + base) + lane;
+            const uint32_t *vrow = reinterpret_cast<const uint32_t *>(vc + base) + lane;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const bool live = b >= 0 && 4 * b + t < ncells;
+                s.kw[4 * j + t] = live ? __ldg(krow + t * (D / 4)) : 0u;
+                s.vw[4 * j + t] = live ? __ldg(vrow + t * (D / 4)) : 0u;
+            }
         }
     };
 
@@ -151,7 +157,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
         const float dot = reduce_scatter32(v, lane);
         const int b = (mc >> 2) != 0 ? s.b[1] : s.b[0];
-        const long long cell = 4LL * b + (mc & 3);
+        const int cell = 4 * b + (mc & 3);
         const bool live = b >= 0 && cell < ncells;
         const float logit = live ? dot * __half2float(ks[cell]) * TEMPERATURE : -INFINITY;
 
@@ -190,7 +196,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
     // Two step buffers in turn: the next step's rows load while this one runs.
     Step s0, s1;
-    long long st = wg;
+    int st = wg;
     load_step(st, s0);
     while (st < nsteps) {   // warp-uniform
         load_step(st + nw, s1);
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             }
         }
     }
-    float *o = out + (i * HEADS + h) * D + d;
+    float *o = out + (static_cast<size_t>(i) * HEADS + h) * D + d;
     if (csize == 1) {
         *o = L > 0.0f ? A / L : 0.0f;
         return;
@@ -283,7 +289,7 @@ cudaError_t launch_sparse_attn(const float *q, const int8_t *kc, const uint16_t 
         }
     }
     const long long grid = static_cast<long long>(nq) * csize;
-    if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    if (grid > 0x7FFFFFFFLL || ncells > 0x7FFFFFFF - 4) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(AT_THREADS);
