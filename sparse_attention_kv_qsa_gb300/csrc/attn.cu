@@ -14,7 +14,7 @@
 // attention and MMVQ row reuse on gfx12", item D5 (decode attention in
 // chunks of cells whose partial results merge in sequential order).
 //
-// GB300 mapping. One CTA of 16 warps per query, or a cluster of up to 8 CTAs
+// GB300 mapping. One CTA of 16 warps per query, or a cluster of up to 4 CTAs
 // per query when there are few queries (decode), so that the cells of one
 // query stream through several SMs. A warp step covers two listed blocks
 // (8 cells): every lane loads its 4 bytes (d = 4 lane .. +3) of each cell's
@@ -40,7 +40,7 @@ constexpr int AT_THREADS = AT_WARPS * 32;
 constexpr int STEP_IDS = 2;                              // listed blocks per warp step
 constexpr int STEP_CELLS = STEP_IDS * 4;                 // 8 cells
 constexpr float TEMPERATURE = 0.08838834764831845f;      // 1 / sqrt(128) = 2^-3.5, exact in fp32
-constexpr int MAX_CLUSTER = 8;
+constexpr int MAX_CLUSTER = 4;
 
 struct AttnShared {
     alignas(16) float p[AT_WARPS][32];          // a step's weights times the value scales, per warp

@@ -87,7 +87,7 @@ def _check(W, out):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("nq,ncells,k,pad", [(1, 262144, 128, 0),      # decode: clusters of 8
+@pytest.mark.parametrize("nq,ncells,k,pad", [(1, 262144, 128, 0),      # decode: clusters of 4
                                              (4, 262144, 128, 0),
                                              (30, 65536, 256, 3),       # clusters of 4
                                              (60, 16384, 64, 0),        # pairs
