@@ -439,6 +439,9 @@ def main():
     ap.add_argument("--no-ksweep", action="store_true", help="skip the k sweep (64, 256, 1024) side measurement")
     ap.add_argument("--no-attn", action="store_true", help="skip the attention side measurement")
     ap.add_argument("--no-summary", action="store_true", help="skip the summary-key side measurement")
+    ap.add_argument("--decode-launches", type=int, default=0,
+                    help="only launch qsa_block_select_small this many times on the decode workload (4 queries, "
+                         "int8 keys, 262,144 cells, k=128; a short run for a profiler to capture), then exit")
     ap.add_argument("--summary-launches", type=int, default=0,
                     help="only launch qsa_block_summary this many times over a 262,144-cell pool (65,536 "
                          "blocks, both key forms; a short run for a profiler to capture), then exit")
@@ -463,6 +466,18 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.decode_launches > 0:
+        Wd = workloads.decode(4, 262144)
+        qd = torch.from_numpy(Wd.q).to(dev)
+        kqd = torch.from_numpy(Wd.kq8).to(dev)
+        ksd = torch.from_numpy(Wd.kscale.view(np.int16)).to(dev)
+        sd = torch.empty((4, Wd.active), dtype=torch.float32, device=dev)
+        idd = torch.empty((4, Wd.k), dtype=torch.int32, device=dev)
+        for _ in range(args.decode_launches):
+            qsa.block_select_small(qd, Wd.active, Wd.k, kblk_q8=kqd, kscale_f16=ksd, scores_out=sd, ids_out=idd)
+        torch.cuda.synchronize()
+        print(json.dumps({"decode_launches": args.decode_launches, "workload": Wd.name}), flush=True)
+        return
     if args.summary_launches > 0:
         A = workloads.attn_case(1, 262144, 1)
         kc = torch.from_numpy(np.ascontiguousarray(A.kc)).to(dev)
