@@ -217,8 +217,9 @@ qsa_status qsa_block_select_small(const float *q, const float *kblk, const int8_
  *          (may be NULL when ncells == 0).
  * ids      int32 [nq][k] (e.g. qsa_block_topk's output), 16-byte aligned.
  * out      fp32 [nq][4][128], written, 16-byte aligned.
- * nq < 0, k < 1 or ncells < 0 returns QSA_ERR_INVALID; nq == 0 is a no-op.
- * Allocates nothing and keeps no state.
+ * nq < 0, k < 1 or ncells < 0 returns QSA_ERR_INVALID; nq == 0 is a no-op;
+ * ncells > INT_MAX - 4 returns QSA_ERR_UNSUPPORTED. Allocates nothing and
+ * keeps no state.
  * Passages: "#3224 [Engine] perf(hip): tune RDNA4 QSA prompt WMMA path
  * (STRATA_HIP_WMMA stays opt-in)", Summary and Evidence section 2 (int8-KV
  * QSA attention with binary16 k/v scales, gated against FP64); "#3102
@@ -247,7 +248,8 @@ qsa_status qsa_sparse_attn(const float *q, const int8_t *k_cells, const uint16_t
  * kblk_q8  int8 [>= block_end][128] and kblk_scale_f16 binary16 [>= block_end]
  *          (the qsa_block_scores_q8 key layout), both or neither.
  * ncells < 0, block_begin < 0, block_end < block_begin, or no output returns
- * QSA_ERR_INVALID; an empty range is a no-op. Allocates nothing.
+ * QSA_ERR_INVALID; an empty range is a no-op; 4 * block_end + 4 > INT_MAX
+ * returns QSA_ERR_UNSUPPORTED. Allocates nothing.
  * Passage: "#3108 optimize exact QSA block scoring and top-k selection on
  * gfx12", the Microbenchmark & Parity Evidence table (the decode layer's
  * "append" step). The pages do not define the summary function: the mean of

@@ -220,6 +220,7 @@ qsa_status qsa_sparse_attn(const float *q, const int8_t *k_cells, const uint16_t
                            int nq, int k, float *out, cudaStream_t stream) {
     if (nq < 0 || k < 1 || ncells < 0) return QSA_ERR_INVALID;
     if (nq == 0) return QSA_OK;
+    if (ncells > 0x7FFFFFFF - 4) return QSA_ERR_UNSUPPORTED;   // cell indices stay in int
     if (q == nullptr || ids == nullptr || out == nullptr || !aligned16(q) || !aligned16(ids) || !aligned16(out))
         return QSA_ERR_INVALID;
     if (ncells > 0 && (k_cells == nullptr || v_cells == nullptr || k_scale_f16 == nullptr ||
@@ -238,6 +239,7 @@ qsa_status qsa_block_summary(const int8_t *k_cells, const uint16_t *k_scale_f16,
     if (kblk == nullptr && kblk_q8 == nullptr) return QSA_ERR_INVALID;
     if ((kblk_q8 == nullptr) != (kblk_scale_f16 == nullptr)) return QSA_ERR_INVALID;
     if (block_end == block_begin) return QSA_OK;
+    if (static_cast<long long>(block_end) * 4 + 4 > 0x7FFFFFFFLL) return QSA_ERR_UNSUPPORTED;   // cell indices in int
     if (ncells > 0 && (k_cells == nullptr || k_scale_f16 == nullptr || !aligned16(k_cells) ||
                        (reinterpret_cast<uintptr_t>(k_scale_f16) & 1u) != 0))
         return QSA_ERR_INVALID;

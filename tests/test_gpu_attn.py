@@ -46,6 +46,7 @@ def test_sparse_attn_argument_errors(lib):
     assert f(A, B, B + 1, B, B, 100, A, 2, 4, A, None) == INVALID    # odd key-scale address
     assert f(A, B, B, B, None, 100, A, 2, 4, A, None) == INVALID     # no value scales
     assert f(None, None, None, None, None, 0, None, 0, 4, None, None) == OK   # no queries
+    assert f(A, B, B, B, B, 2 ** 31 - 2, A, 2, 4, A, None) == qsa.QSA_ERR_UNSUPPORTED   # cell indices past int
 
 
 def tolerance(q, kc, ks, vc, vs, ids) -> np.ndarray:

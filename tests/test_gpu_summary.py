@@ -34,6 +34,7 @@ def test_block_summary_argument_errors(lib):
     assert f(A, B, 16, 0, 4, None, A, B + 1, None) == INVALID       # odd block-scale address
     assert f(None, None, 16, 0, 4, A, None, None, None) == INVALID  # cells missing
     assert f(A, B, 16, 3, 3, A, None, None, None) == OK             # empty range
+    assert f(A, B, 16, 0, 2 ** 29, A, None, None, None) == qsa.QSA_ERR_UNSUPPORTED   # cell indices past int
 
 
 def _pool(ncells, seed_index=11):
