@@ -62,7 +62,18 @@ __global__ void __launch_bounds__(SUM_WARPS * 32)
             if (t < n)
                 sum = __fadd_rn(sum, __fmul_rn(static_cast<float>(static_cast<int8_t>((w[t] >> (8 * e)) & 0xFFu)),
                                                sc[t]));
-        m[e] = n > 0 ? __fdiv_rn(sum, static_cast<float>(n)) : 0.0f;
+        m[e] = sum;
+    }
+    // The mean: dividing by 4, 2 or 1 is multiplying by 0.25, 0.5 or 1 (one
+    // rounding either way); only a block of 3 present cells divides (n is
+    // the same across the warp, so this branch does not diverge).
+    if (n == 3) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) m[e] = __fdiv_rn(m[e], 3.0f);
+    } else {
+        const float inv = n == 4 ? 0.25f : (n == 2 ? 0.5f : 1.0f);   // n == 0 leaves the zero sums
+#pragma unroll
+        for (int e = 0; e < 4; ++e) m[e] = __fmul_rn(m[e], inv);
     }
     const size_t out = static_cast<size_t>(b) * D + 4 * lane;
     if (key != nullptr) *reinterpret_cast<float4 *>(key + out) = make_float4(m[0], m[1], m[2], m[3]);
@@ -71,12 +82,25 @@ __global__ void __launch_bounds__(SUM_WARPS * 32)
         top = __uint_as_float(__reduce_max_sync(FULL_MASK, __float_as_uint(top)));
         const __half sh = __float2half_rn(__fdiv_rn(top, 127.0f));
         const float s = __half2float(sh);
+        // rint(m / s) without a division per code: q0 = rint(m * (1/s)) is
+        // within one of it, and the residual r = m - q0 * s is exact in fp32
+        // (q0 * s has at most 19 significant bits and |r| is about s / 2 or
+        // less), so comparing |r| with s / 2 (exact) settles the nearest
+        // integer, ties to even.
         uint32_t codes = 0u;
+        if (s > 0.0f) {
+            const float rs = __frcp_rn(s), hs = 0.5f * s;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            int c = s > 0.0f ? __float2int_rn(__fdiv_rn(m[e], s)) : 0;
-            c = c > 127 ? 127 : (c < -127 ? -127 : c);
-            codes |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * e);
+            for (int e = 0; e < 4; ++e) {
+                float q = rintf(__fmul_rn(m[e], rs));
+                const float r = __fmaf_rn(-q, s, m[e]);
+                const float ar = fabsf(r);
+                const float step = r > 0.0f ? 1.0f : -1.0f;
+                if (ar > hs || (ar == hs && fmodf(q, 2.0f) != 0.0f)) q += step;
+                int c = static_cast<int>(q);
+                c = c > 127 ? 127 : (c < -127 ? -127 : c);
+                codes |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * e);
+            }
         }
         *reinterpret_cast<uint32_t *>(kq8 + out) = codes;
         if (lane == 0) kscale[b] = sh;
