@@ -39,7 +39,10 @@ constexpr int AT_WARPS = 16;
 constexpr int AT_THREADS = AT_WARPS * 32;
 constexpr int STEP_IDS = 2;                              // listed blocks per warp step
 constexpr int STEP_CELLS = STEP_IDS * 4;                 // 8 cells
-constexpr float TEMPERATURE = 0.08838834764831845f;      // 1 / sqrt(128) = 2^-3.5, exact in fp32
+// Logits are kept in base-2 units: (q . k) * ks / sqrt(128) * log2(e), so the
+// softmax weights are 2^(logit - max) (the same weights as e^ of the natural
+// logits); log2(e) / sqrt(128), rounded to fp32.
+constexpr float LOGIT2_SCALE = 0.12751743082459868f;
 constexpr int MAX_CLUSTER = 4;
 
 struct AttnShared {
@@ -159,7 +162,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const int b = (mc >> 2) != 0 ? s.b[1] : s.b[0];
         const int cell = 4 * b + (mc & 3);
         const bool live = b >= 0 && cell < ncells;
-        const float logit = live ? dot * __half2float(ks[cell]) * TEMPERATURE : -INFINITY;
+        const float logit = live ? dot * __half2float(ks[cell]) * LOGIT2_SCALE : -INFINITY;
 
         // Online softmax of head lane % 4 over this step's cells (the lanes with that head).
         float bm = logit;
@@ -167,19 +170,23 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 8));
         bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 16));
         const float mn = fmaxf(m, bm);
-        const float alpha = mn == -INFINITY ? 1.0f : expf(m - mn);
-        const float p = live ? expf(logit - mn) : 0.0f;
+        const float alpha = mn == -INFINITY ? 1.0f : exp2f(m - mn);
+        const float p = live ? exp2f(logit - mn) : 0.0f;
         m = mn;
         lsum = fmaf(lsum, alpha, p);
         sh.p[warp][lane] = live ? p * __half2float(vs[cell]) : 0.0f;
-        float al[HEADS];
-#pragma unroll
-        for (int h = 0; h < HEADS; ++h) al[h] = __shfl_sync(FULL_MASK, alpha, h);
         __syncwarp();
+        // Rescale the outputs only when some head's running maximum moved
+        // (alpha is exactly 1 otherwise; the test is warp-uniform).
+        if (__any_sync(FULL_MASK, alpha != 1.0f)) {
+            float al[HEADS];
 #pragma unroll
-        for (int h = 0; h < HEADS; ++h)
+            for (int h = 0; h < HEADS; ++h) al[h] = __shfl_sync(FULL_MASK, alpha, h);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[h][e] *= al[h];
+            for (int h = 0; h < HEADS; ++h)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[h][e] *= al[h];
+        }
 #pragma unroll
         for (int c = 0; c < STEP_CELLS; ++c) {
             const float4 pc = *reinterpret_cast<const float4 *>(&sh.p[warp][4 * c]);   // heads 0..3
@@ -232,7 +239,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         for (int w = 0; w < AT_WARPS; ++w) {
             const float mw = sh.m[w][h];
             if (mw != -INFINITY) {
-                const float f = expf(mw - M);
+                const float f = exp2f(mw - M);
                 A = fmaf(sh.acc[w][h][d], f, A);
                 L = fmaf(sh.l[w][h], f, L);
             }
@@ -263,7 +270,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
             for (int r = 0; r < MAX_CLUSTER; ++r) {
                 if (r < csize && mr[r] != -INFINITY) {
-                    const float f = expf(mr[r] - Mc);
+                    const float f = exp2f(mr[r] - Mc);
                     Ac = fmaf(ld_shared_cluster_f32(map_shared_rank(smem_u32(&sh.cacc[h][d]), r)), f, Ac);
                     Lc = fmaf(ld_shared_cluster_f32(map_shared_rank(smem_u32(&sh.cl[h]), r)), f, Lc);
                 }
