@@ -48,3 +48,25 @@ def test_deterministic():
     a, b = w.tiny(), w.tiny()
     assert np.array_equal(a.q, b.q) and np.array_equal(a.kblk, b.kblk)
     assert not np.array_equal(w.tiny(0).q, w.tiny(5).q)
+
+
+def test_attention_case():
+    """The attention recipe: deterministic, k - pad distinct ascending block
+    ids in range then -1 padding, int8 cells on [-127, 127], binary16 scales
+    positive, finite and within [1e-3, 1e-1] after rounding."""
+    A = w.attn_case(5, 4099 * 4 + 3, 60, pad=7)
+    B = w.attn_case(5, 4099 * 4 + 3, 60, pad=7)
+    for x, y in ((A.q, B.q), (A.kc, B.kc), (A.vc, B.vc), (A.ks, B.ks), (A.vs, B.vs), (A.ids, B.ids)):
+        assert np.array_equal(x, y)
+    nblocks = (A.ncells + 3) // 4
+    assert A.ids.shape == (5, 60) and np.all(A.ids[:, 53:] == -1)
+    for row in A.ids[:, :53]:
+        assert np.all(np.diff(row) > 0) and row.min() >= 0 and row.max() < nblocks
+    assert A.kc.shape == (A.ncells, 128) and A.kc.min() >= -127 and A.kc.max() <= 127
+    for sc in (A.ks, A.vs):
+        f = sc.view(np.float16).astype(np.float64)
+        assert np.all(np.isfinite(f)) and f.min() >= 0.999e-3 and f.max() <= 1.001e-1
+    assert not np.array_equal(A.kc, A.vc)            # K and V come from different streams
+    # all blocks of a small pool, in a seeded order, ascending
+    S = w.attn_case(2, 17, 5)
+    assert np.array_equal(S.ids, np.tile(np.arange(5, dtype=np.int32), (2, 1)))
