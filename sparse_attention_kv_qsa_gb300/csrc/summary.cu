@@ -56,12 +56,13 @@ __global__ void __launch_bounds__(SUM_WARPS * 32)
     float m[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
+        // Each int8 x binary16 product is exact in fp32, so one fused
+        // multiply-add rounds exactly like the multiply and the add in turn.
         float sum = 0.0f;
 #pragma unroll
         for (int t = 0; t < 4; ++t)
             if (t < n)
-                sum = __fadd_rn(sum, __fmul_rn(static_cast<float>(static_cast<int8_t>((w[t] >> (8 * e)) & 0xFFu)),
-                                               sc[t]));
+                sum = __fmaf_rn(static_cast<float>(static_cast<int8_t>((w[t] >> (8 * e)) & 0xFFu)), sc[t], sum);
         m[e] = sum;
     }
     // The mean: dividing by 4, 2 or 1 is multiplying by 0.25, 0.5 or 1 (one
