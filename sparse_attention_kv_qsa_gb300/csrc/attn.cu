@@ -22,7 +22,8 @@
 // dot products against its slice of the 4 head queries, and a butterfly
 // reduce-scatter (31 shuffles) leaves lane l with the full logit of cell
 // l / 4 for head l % 4. Each warp keeps an online softmax per head (running
-// maximum, normaliser, and the head's 128 output values, 4 per lane); the
+// maximum, normaliser, and the head's 128 output values, 4 per lane), in
+// base 2, rescaling the outputs only in steps where a maximum moved; the
 // next step's rows are loaded before the current step is used. Partial
 // results merge in a fixed order: the CTA's warps in warp order, then the
 // cluster's CTAs in rank order through distributed shared memory, so the

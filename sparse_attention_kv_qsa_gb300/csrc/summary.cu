@@ -10,12 +10,16 @@
 // "append + scores + topk + attn"). The pages do not define the summary
 // function; the mean of the block's present cells is the reading taken, and
 // the int8 form (one binary16 scale per block) is the decode scorer's key
-// format. The integer codes are decided by float arithmetic, so the sum,
-// the division by n, the scale and the code divisions are single IEEE
-// operations in one fixed order (each product of an int8 by a binary16 scale
-// is exact in fp32).
+// format. The integer codes are decided by float arithmetic, so every value
+// equals that of single IEEE operations in one fixed order: the sum adds the
+// cells in turn (each int8 x binary16 product is exact, so a fused
+// multiply-add rounds the same), the mean divides by n (a multiply by 1/4,
+// 1/2 or 1 rounds the same), and each code is rint of the rounded quotient
+// (computed from one reciprocal and an exact residual, which lands on the
+// same integer).
 //
-// GB300 mapping: an HBM-bound elementwise pass. One warp per block; lane l
+// GB300 mapping: an elementwise pass over the cells (bound by instruction
+// issue more than by HBM on this GPU). One warp per block; lane l
 // owns d = 4l .. 4l+3, reads one 4-byte word of each present cell's row (a
 // 128-byte line per row and warp) and writes one 16-byte key word and one
 // 4-byte code word; the block's max |key| is a warp max over the float bit
