@@ -21,6 +21,15 @@ pipelined over two input buffers, the copy of one step overlapping the
 kernels of the previous one); ``cpu_baseline`` times the CPU oracle on this
 machine's cores.
 
+Side measurements nested in the same line (rank 0): ``k_sweep`` (the
+headline workload at k = 64, 256, 1024), ``decode`` (nq = 1 and 4 decode
+steps: the one-launch qsa_block_select_small and the two-call forms),
+``attention`` (qsa_sparse_attn at decode shapes and at 256 queries x
+k = 512) and ``summary`` (qsa_block_summary over a 262,144-cell pool and a
+one-block append). ``--decode-launches``, ``--attn-launches`` and
+``--summary-launches`` only launch that call a few times and exit (short
+runs for a profiler).
+
 ``--impl reference`` times the CPU oracle itself as the reference arm.
 Under torchrun each rank runs an independent replica (no collective on the
 data path); timing is the max over ranks.
