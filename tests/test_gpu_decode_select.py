@@ -69,8 +69,9 @@ def test_select_small_matches_plain_calls_and_oracle(kind, nq, active, k):
 
 @pytest.mark.gpu
 def test_select_small_repeated_calls_and_ties():
-    """Back-to-back calls on one stream (the launch clears its sync words each
-    time), on integer keys whose scores tie heavily."""
+    """Back-to-back calls on one stream (each call's grid barrier uses the
+    counter its predecessor cleared, by generation parity), on integer keys
+    whose scores tie heavily."""
     import torch
     import oracle
     from sparse_attention_kv_qsa_gb300 import workloads as w
