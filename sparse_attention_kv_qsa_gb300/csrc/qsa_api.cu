@@ -178,6 +178,10 @@ qsa_status qsa_block_select_static(const float *q, const float *kblk, int nq, in
     if (active_blocks > 0 && (kblk == nullptr || !aligned16(kblk))) return QSA_ERR_INVALID;
     const long long groups = static_cast<long long>(nq) * ((active_blocks + qsa::GROUP_BLOCKS - 1) / qsa::GROUP_BLOCKS);
     if (groups > QSA_SELECT_STATIC_GROUPS_MAX) return QSA_ERR_UNSUPPORTED;
+    // The top-k's own size limits, before the scorer launches.
+    if (active_blocks > QSA_TOPK_MAX_ACTIVE) return QSA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(nq) * k > (1LL << 40)) return QSA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(nq) * 8 > 0x7FFFFFFFLL) return QSA_ERR_UNSUPPORTED;
     uint32_t *gm = select_scratch();
     if (gm == nullptr) return QSA_ERR_CUDA;
     if (active_blocks > 0) {

@@ -39,8 +39,11 @@
 //  they re-stream the row and filter by prefix instead).
 //  Each digit's histogram is built by all warps with shared-memory atomics and
 //  scanned by warp 0 alone (two block barriers per digit).
-// No CTA ever waits on another: no cluster, no grid-wide synchronisation, no
-// global scratch.
+// In topk_row_kernel no CTA ever waits on another: no cluster, no grid-wide
+// synchronisation, no global scratch. The fused decode select at the end of
+// this file is the exception: a cooperative launch whose CTAs meet at a
+// bounded grid-wide barrier, with its group maxima and arrival counters in
+// fixed device arrays (so its calls must be ordered on a device).
 #include "decode_rows.cuh"
 #include "ptx.cuh"
 #include "qsa_internal.cuh"

@@ -38,6 +38,10 @@ def test_static_select_argument_and_size_errors(lib):
     gmax = qsa.SELECT_STATIC_GROUPS_MAX
     assert f(A, B, 257, 40000, 32768, 5, A, B, None) == UNSUPPORTED
     assert f(A, B, 1, 10 ** 7, 32 * gmax + 1, 5, A, B, None) == UNSUPPORTED
+    # within the scratch bound but past the top-k's row limit: refused before
+    # the scorer launches (these fake pointers would fault a launched kernel)
+    assert f(A, B, 1, 10 ** 7, qsa.TOPK_MAX_ACTIVE + 1, 5, A, B, None) == UNSUPPORTED
+    assert f(A, B, 1, 10 ** 7, 400000, 5, A, B, None) == UNSUPPORTED
 
 
 @pytest.mark.gpu
