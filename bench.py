@@ -10,10 +10,11 @@ inputs are the seeded synthetic full-capacity workload: q and keys
 Student-t(3) at unit variance.
 
 Prints ONE JSON line (rank 0). ``value`` is query-blocks per second over all
-ranks; ``ms_per_step`` the device time of one step (one CUDA event pair
-around both calls on the launching stream, L2 flushed before every step and
-the flush untimed; every other step carries an extra event between the
-calls, which gives each kernel's duration);
+ranks; ``ms_per_step`` the mean device time of the K timed steps (one CUDA
+event pair around both calls of each step on the launching stream, L2
+flushed before every step and the flush untimed; p10/p50/p90 in
+``step_us``); each kernel's own duration (``kernels_us``, the roofline's)
+comes from a separate pass right after, with an event between the calls;
 ``roofline`` describes the dominant kernel; ``e2e`` repeats the measurement
 through the public API with host buffers (pinned H2D of q and the active
 keys, D2H of the ids, all inside the timed region; consecutive steps are
@@ -208,7 +209,13 @@ class ClockSampler:
             self.thread.start()
         except (OSError, ValueError):
             self.proc = None
-        time.sleep(0.3)
+            return
+        # nvidia-smi's start-up (driver and NVML initialisation) must be over
+        # before the timed steps begin: wait for its first sample (bounded).
+        t0 = time.monotonic()
+        while not self.lines and time.monotonic() - t0 < 5.0 and self.proc.poll() is None:
+            time.sleep(0.01)
+        time.sleep(0.2)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -314,12 +321,13 @@ def run_reference(args, world, rank):
             "gpu_launches": 0}
 
 
-def attention_side_measurement(dev, stream):
+def attention_side_measurement(dev, stream, sm_mhz: float):
     """qsa_sparse_attn over the selected blocks' int8 KV cells (262,144 cells,
     binary16 scales): decode shapes (nq = 1 and 4, k = 128) per call of a CUDA
     graph of 20 calls, and a prompt-like shape (256 queries, k = 512, L2
     flushed before each call) with its HBM and FP32 fractions. The FP32 peak
-    is 152 SMs x 128 lanes x 2 FLOP x the sampled SM clock's maximum."""
+    is the device's SM count x 128 lanes x 2 FLOP x `sm_mhz` (the SM clock
+    sampled during the timed steps)."""
     import torch
     import sparse_attention_kv_qsa_gb300 as qsa
     from sparse_attention_kv_qsa_gb300 import workloads as w
@@ -369,9 +377,11 @@ def attention_side_measurement(dev, stream):
         cells = nq * k * 4
         bytes_ = cells * 2 * (128 + 2) + nq * 4 * 128 * 4 * 2 + nq * k * 4
         flops = cells * 4 * 128 * 2 * 2
-        peak_fp32 = 152 * 128 * 2 * 2.07e9
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak_fp32 = sms * 128 * 2 * sm_mhz * 1e6
         out[name] = {"call_us_p50": us, "algorithmic_bytes": bytes_, "hbm_gbs": bytes_ / us / 1e3,
-                     "fp32_tflops": flops / us / 1e6, "fp32_frac_of_nominal": flops / (us * 1e-6) / peak_fp32}
+                     "fp32_tflops": flops / us / 1e6, "fp32_frac": flops / (us * 1e-6) / peak_fp32,
+                     "fp32_peak_note": f"{sms} SMs x 128 lanes x 2 FLOP x {sm_mhz:.0f} MHz (sampled)"}
     return out
 
 
@@ -536,45 +546,60 @@ def main():
                          lambda: qsa.block_topk_gmax(scores, gmax, W.k, out=ids))
 
     def timed_steps(score, topk, n):
-        """n flushed steps. Even steps: one event pair around both calls (the
-        step time; the top-k may launch under the scorer's tail). Odd steps:
-        an extra event between the calls gives each kernel's duration."""
+        """n flushed steps, each timed whole: one event pair on the launching
+        stream around both calls (the top-k may launch under the scorer's
+        tail, as it does in use)."""
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for i in range(n):
+            if not args.no_flush:
+                flush.fill_(float(i))
+            ev[i][0].record(stream)
+            score()
+            topk()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
+
+    def split_steps(score, topk, n):
+        """n flushed steps with an extra event between the calls: each
+        kernel's own duration. The middle event keeps the top-k from
+        launching under the scorer's tail, so these steps are not step times."""
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
         for i in range(n):
             if not args.no_flush:
                 flush.fill_(float(i))
             ev[i][0].record(stream)
             score()
-            if i & 1 or n == 1:
-                ev[i][1].record(stream)
+            ev[i][1].record(stream)
             topk()
             ev[i][2].record(stream)
         torch.cuda.synchronize()
-        split = [i for i in range(n) if i & 1 or n == 1]
-        whole = [i for i in range(n) if not i & 1]
-        return ([ev[i][0].elapsed_time(ev[i][1]) for i in split], [ev[i][1].elapsed_time(ev[i][2]) for i in split],
-                [ev[i][0].elapsed_time(ev[i][2]) for i in whole], len(split))
+        return [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)], [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
 
     score, topk = calls[path]
+    K_ = args.steps
+    # The clock sampler runs from before the warm-up to after the timed steps.
+    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    if sampler:
+        sampler.start()
     for i in range(args.warmup):
         if not args.no_flush:
             flush.fill_(float(i))
         score()
         topk()
     torch.cuda.synchronize()
-
-    K_ = args.steps
-    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
-    if sampler:
-        sampler.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    t_score, t_topk, t_step, n_split = timed_steps(score, topk, K_)
+    t_step = timed_steps(score, topk, K_)
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
     ids_headline = ids.clone()
+    # Each kernel's own duration (the roofline's), in a pass of its own right
+    # after the timed steps: same calls, same flushes.
+    n_split = max(K_, 200)
+    t_score, t_topk = split_steps(score, topk, n_split)
     other = None
     if len(calls) > 1:
         # The other path, for comparison (same ids), outside the timed region.
@@ -582,12 +607,13 @@ def main():
         for i in range(args.warmup):
             o_score()
             o_topk()
-        n_o = min(K_, 400)
-        os_, ot_, ostep, _ = timed_steps(o_score, o_topk, n_o)
+        n_o = min(max(K_, 200), 400)
+        ostep = timed_steps(o_score, o_topk, n_o)
+        os_, ot_ = split_steps(o_score, o_topk, n_o)
         assert torch.equal(ids, ids_headline), "the two paths disagree"
         other = {"path": "plain" if path == "gmax" else "gmax", "steps": n_o,
-                 "step_us": 1e3 * statistics.mean(ostep), "scores_us": 1e3 * statistics.mean(os_),
-                 "topk_us": 1e3 * statistics.mean(ot_)}
+                 "step_us": 1e3 * statistics.mean(ostep), "step_p50_us": 1e3 * pct(ostep, 50),
+                 "scores_us": 1e3 * statistics.mean(os_), "topk_us": 1e3 * statistics.mean(ot_)}
     step_ms_local = statistics.mean(t_step)
     step_ms = max_over_ranks(step_ms_local, world, dev)
     if qsa.device_error(dev) != 0:
@@ -638,9 +664,11 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kernels_us": {"scores": score_us, "topk": topk_us,
                        "scores_p50": 1e3 * statistics.median(t_score), "topk_p50": 1e3 * statistics.median(t_topk),
-                       "steps_timed_split": n_split},
+                       "steps": n_split,
+                       "pass": "a split pass after the timed steps (an event between the two calls)"},
         "step_us": {"mean": 1e3 * step_ms_local, "p10": 1e3 * pct(t_step, 10), "p50": 1e3 * pct(t_step, 50),
-                    "p90": 1e3 * pct(t_step, 90), "steps": len(t_step)},
+                    "p90": 1e3 * pct(t_step, 90), "min": 1e3 * min(t_step), "max": 1e3 * max(t_step),
+                    "steps": len(t_step)},
         "roofline": roof,
         "step_roofline": {"floor_us": floor_us, "frac": floor_us / (step_ms * 1e3),
                           "note": "algorithmic step bytes at the HBM peak (the step's binding roof when "
@@ -710,7 +738,8 @@ def main():
     if rank == 0 and not args.no_decode:
         line["decode"] = decode_side_measurement(dev, stream)
     if rank == 0 and not args.no_attn:
-        line["attention"] = attention_side_measurement(dev, stream)
+        sm_mhz = (clocks or {}).get("sm_mhz") or peaks["sm_max_mhz"]
+        line["attention"] = attention_side_measurement(dev, stream, sm_mhz)
     if rank == 0 and not args.no_summary:
         line["summary"] = summary_side_measurement(dev, stream)
 
@@ -726,7 +755,8 @@ def main():
             for _ in range(args.warmup):
                 sc()
                 tk()
-            t_s, t_k, t_st, _ = timed_steps(sc, tk, 200)
+            t_st = timed_steps(sc, tk, 200)
+            t_s, t_k = split_steps(sc, tk, 200)
             qsa.block_topk(scores, ks, out=ids_p)
             torch.cuda.synchronize()
             assert torch.equal(ids_k, ids_p), f"k={ks}: the two top-k paths disagree"
