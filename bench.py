@@ -99,21 +99,22 @@ def source_sha(fname: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def decode_side_measurement(dev, stream):
-    """Decode-shaped calls (int8 keys, k=128, 262,144 cells = 65,536 blocks;
-    nq = 1 and 4): launch- and latency-bound, so reported in microseconds per
-    score + top-k step, once with a CUDA-event pair per step (L2 flushed
-    first) and once per step of a CUDA graph of 20 back-to-back steps; for
-    the one-launch call (fused: qsa_block_select_small), the group-maximum
-    calls (gmax) and the plain ones."""
+def decode_side_measurement(dev, stream, cells_list=(2048, 16384, 65536, 262144)):
+    """Decode-shaped calls (int8 keys, k=128, nq = 1 and 4, the decode sweep's
+    contexts of 2,048 to 262,144 cells = 512 to 65,536 blocks): launch- and
+    latency-bound, so reported in microseconds per score + top-k step, once
+    with a CUDA-event pair per step (L2 flushed first) and once per step of a
+    CUDA graph of 20 back-to-back steps; for the one-launch call (fused:
+    qsa_block_select_small), the group-maximum calls (gmax) and the plain
+    ones. Rows of at most 16,384 blocks take the register-resident top-k."""
     import torch
     import sparse_attention_kv_qsa_gb300 as qsa
     from sparse_attention_kv_qsa_gb300 import workloads as w
-    out = {"workload": "decode: int8 keys + binary16 scales, 262,144 cells (65,536 blocks), k=128", "unit": "us"}
+    out = {"workload": "decode: int8 keys + binary16 scales, k=128; keys nq{1,4}_c<cells>", "unit": "us"}
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
-    for nq in (1, 4):
-        W = w.decode(nq, 262144)
+    for nq, cells in [(nq, c) for c in cells_list for nq in (1, 4)]:
+        W = w.decode(nq, cells)
         q = torch.from_numpy(W.q).to(dev)
         kq = torch.from_numpy(W.kq8).to(dev)
         ks = torch.from_numpy(W.kscale.view(np.int16)).to(dev)
@@ -163,7 +164,7 @@ def decode_side_measurement(dev, stream):
             torch.cuda.synchronize()
             res[name] = {"step_p50": pct(ts, 50), "step_p10": pct(ts, 10), "step_p90": pct(ts, 90),
                          "graph_step": 1e3 * e0.elapsed_time(e1) / 20}
-        out[f"nq{nq}"] = res
+        out[f"nq{nq}_c{cells}"] = res
     return out
 
 
@@ -545,11 +546,19 @@ def main():
         calls["gmax"] = (lambda: qsa.block_scores_gmax(q, kblk, W.active, out=scores, gmax_out=gmax),
                          lambda: qsa.block_topk_gmax(scores, gmax, W.k, out=ids))
 
+    def queue_ahead():
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(2_000_000)   # ~1 ms
+
     def timed_steps(score, topk, n):
         """n flushed steps, each timed whole: one event pair on the launching
         stream around both calls (the top-k may launch under the scorer's
-        tail, as it does in use)."""
+        tail, as it does in use). A short device-side sleep before the first
+        event lets the host queue the first steps while the GPU is still busy,
+        so no step's events also time a host launch gap; it is outside every
+        timed event pair."""
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        queue_ahead()
         for i in range(n):
             if not args.no_flush:
                 flush.fill_(float(i))
@@ -565,6 +574,7 @@ def main():
         kernel's own duration. The middle event keeps the top-k from
         launching under the scorer's tail, so these steps are not step times."""
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        queue_ahead()
         for i in range(n):
             if not args.no_flush:
                 flush.fill_(float(i))
@@ -668,6 +678,7 @@ def main():
                        "pass": "a split pass after the timed steps (an event between the two calls)"},
         "step_us": {"mean": 1e3 * step_ms_local, "p10": 1e3 * pct(t_step, 10), "p50": 1e3 * pct(t_step, 50),
                     "p90": 1e3 * pct(t_step, 90), "min": 1e3 * min(t_step), "max": 1e3 * max(t_step),
+                    "argmax": int(np.argmax(t_step)), "first3": [1e3 * x for x in t_step[:3]],
                     "steps": len(t_step)},
         "roofline": roof,
         "step_roofline": {"floor_us": floor_us, "frac": floor_us / (step_ms * 1e3),

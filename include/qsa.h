@@ -262,9 +262,29 @@ qsa_status qsa_block_summary(const int8_t *k_cells, const uint16_t *k_scale_f16,
 /*
  * Reads and clears the current device's error word: nonzero when a kernel
  * of this library gave up a bounded wait (its outputs are then invalid).
- * Synchronises `stream`. *code receives the word.
+ * Bit 0x100: a wait of the tensor-core scorer's pipeline ran out (the CTA
+ * then abandons its remaining waits at once, lets its own copies and MMAs
+ * in flight finish, and exits); bit 0x2: the fused decode select's grid
+ * barrier ran out. Synchronises `stream`. *code receives the word.
  */
 qsa_status qsa_get_device_error(uint32_t *code, cudaStream_t stream);
+
+/*
+ * Diagnostics for the bounded waits (not for production use; the pages have
+ * no counterpart). For the kernels launched after the call: every spin-wait
+ * gives up after wait_limit_ns (default 2,000,000,000), and `faults` plants
+ * a wait that cannot complete so that the time-out path runs:
+ *   bit 0: the tensor-core scorer's CTA 0 never loads its first key piece
+ *          (qsa_block_scores, _q8, _gmax and _select_static with nq > 4);
+ *   bit 1: the fused decode select's grid barrier waits for one arrival
+ *          more than its grid has (qsa_block_select_small).
+ * The outputs of such calls are invalid and qsa_get_device_error reports
+ * them; the device stays usable. Call qsa_debug_inject(0, 2000000000) to
+ * restore normal operation. Process-wide; not thread-safe against
+ * concurrent launches. faults with other bits, or wait_limit_ns == 0 or
+ * above 60 s, returns QSA_ERR_INVALID.
+ */
+qsa_status qsa_debug_inject(uint32_t faults, uint64_t wait_limit_ns);
 
 /* Static description of a status code. */
 const char *qsa_status_string(qsa_status status);

@@ -21,6 +21,7 @@ from .qsa import (  # noqa: F401
     block_topk,
     block_topk_gmax,
     groups,
+    debug_inject,
     default_scorer_kernel,
     device_error,
     sparse_attn,

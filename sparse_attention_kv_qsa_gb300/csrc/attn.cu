@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     float qv[HEADS][4];       // this lane's slice d = 4 lane .. +3 of each head's query
 #pragma unroll
     for (int h = 0; h < HEADS; ++h) {
-        const float4 t = __ldg(reinterpret_cast<const float4 *>(q + (static_cast<size_t>(i) * HEADS + h) * D) + lane);
+        const float4 t = ld_in(reinterpret_cast<const float4 *>(q + (static_cast<size_t>(i) * HEADS + h) * D) + lane);
         qv[h][0] = t.x, qv[h][1] = t.y, qv[h][2] = t.z, qv[h][3] = t.w;
     }
 
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < STEP_IDS; ++j) {
             const int slot = STEP_IDS * st + j;
-            const int b = st < nsteps && slot < k ? __ldg(ids_i + slot) : -1;
+            const int b = st < nsteps && slot < k ? ld_in(ids_i + slot) : -1;
             s.b[j] = b >= 0 && b < nblocks ? b : -1;
         }
 #pragma unroll
@@ -135,8 +135,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 const bool live = b >= 0 && 4 * b + t < ncells;
-                s.kw[4 * j + t] = live ? __ldg(krow + t * (D / 4)) : 0u;
-                s.vw[4 * j + t] = live ? __ldg(vrow + t * (D / 4)) : 0u;
+                s.kw[4 * j + t] = live ? ld_in(krow + t * (D / 4)) : 0u;
+                s.vw[4 * j + t] = live ? ld_in(vrow + t * (D / 4)) : 0u;
             }
         }
     };
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const int b = (mc >> 2) != 0 ? s.b[1] : s.b[0];
         const int cell = 4 * b + (mc & 3);
         const bool live = b >= 0 && cell < ncells;
-        const float logit = live ? dot * __half2float(ks[cell]) * LOGIT2_SCALE : -INFINITY;
+        const float logit = live ? dot * __half2float(__ushort_as_half(ld_in_u16(ks + cell))) * LOGIT2_SCALE : -INFINITY;
 
         // Online softmax of head lane % 4 over this step's cells (the lanes with that head).
         float bm = logit;
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const float p = live ? exp2f(logit - mn) : 0.0f;
         m = mn;
         lsum = fmaf(lsum, alpha, p);
-        sh.p[warp][lane] = live ? p * __half2float(vs[cell]) : 0.0f;
+        sh.p[warp][lane] = live ? p * __half2float(__ushort_as_half(ld_in_u16(vs + cell))) : 0.0f;
         __syncwarp();
         // Rescale the outputs only when some head's running maximum moved
         // (alpha is exactly 1 otherwise; the test is warp-uniform).

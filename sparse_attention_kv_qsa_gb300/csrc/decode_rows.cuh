@@ -42,7 +42,7 @@ __device__ __forceinline__ void dec_build_queries(const float *__restrict__ q, i
         float v = 0.0f;
         if (r < nq) {
             const float *p = q + static_cast<size_t>(r) * (HEADS * D) + d;
-            v = __fadd_rn(__fadd_rn(__fadd_rn(__ldg(p), __ldg(p + D)), __ldg(p + 2 * D)), __ldg(p + 3 * D));
+            v = __fadd_rn(__fadd_rn(__fadd_rn(ld_in(p), ld_in(p + D)), ld_in(p + 2 * D)), ld_in(p + 3 * D));
         }
         qs[r][dec_qidx(d)] = v;
     }
@@ -74,7 +74,7 @@ __device__ __forceinline__ void dec_score_chunk(const float (*qs)[DEC_QROW], lon
             const float4 *row = reinterpret_cast<const float4 *>(kblk + b * D + part * PER);
             float4 kv[PER / 4];
 #pragma unroll
-            for (int c = 0; c < PER / 4; ++c) kv[c] = __ldg(row + c);
+            for (int c = 0; c < PER / 4; ++c) kv[c] = ld_in(row + c);
 #pragma unroll
             for (int c = 0; c < PER / 4; ++c) {
 #pragma unroll
@@ -90,7 +90,7 @@ __device__ __forceinline__ void dec_score_chunk(const float (*qs)[DEC_QROW], lon
             const uint4 *row = reinterpret_cast<const uint4 *>(kq8 + b * D + part * PER);
             uint4 kv[PER / 16];
 #pragma unroll
-            for (int c = 0; c < PER / 16; ++c) kv[c] = __ldg(row + c);
+            for (int c = 0; c < PER / 16; ++c) kv[c] = ld_in(row + c);
 #pragma unroll
             for (int c = 0; c < PER / 16; ++c) {
                 const uint32_t w4[4] = {kv[c].x, kv[c].y, kv[c].z, kv[c].w};
@@ -120,7 +120,7 @@ __device__ __forceinline__ void dec_score_chunk(const float (*qs)[DEC_QROW], lon
         for (int o = 1; o < TPR; o <<= 1) acc[r] = __fadd_rn(acc[r], __shfl_xor_sync(FULL_MASK, acc[r], o));
     }
     if (live && part == 0) {
-        const float scale = kInt8 ? __half2float(kscale[b]) : 1.0f;
+        const float scale = kInt8 ? __half2float(__ushort_as_half(ld_in_u16(kscale + b))) : 1.0f;
 #pragma unroll
         for (int r = 0; r < NQ; ++r) {
             if (kInt8) acc[r] = __fmul_rn(acc[r], scale);

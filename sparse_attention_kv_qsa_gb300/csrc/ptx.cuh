@@ -62,15 +62,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Waits for the phase with the given parity to complete; false after
+// limit_ns, or as soon as *abort (when given) is non-zero.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = WAIT_LIMIT_NS,
+                                          const volatile uint32_t *abort = nullptr) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+        if (abort != nullptr && *abort != 0u) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -110,6 +113,13 @@ __device__ __forceinline__ void st_async_v4(uint32_t raddr, uint32_t rbar, uint3
                  : "memory");
 }
 
+// 8-byte store into another CTA's shared memory, as st_async_v4.
+__device__ __forceinline__ void st_async_v2(uint32_t raddr, uint32_t rbar, uint32_t a, uint32_t b) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(raddr),
+                 "r"(a), "r"(b), "r"(rbar)
+                 : "memory");
+}
+
 // Programmatic dependent launch. wait: blocks until the grids this one depends
 // on have completed and their memory is visible (a no-op without such a
 // dependency). launch_dependents: lets the next grid on the stream start
@@ -119,13 +129,23 @@ __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Asynchronous copy of one 4-byte word from global to shared memory: the
-// value passes through no register, so the issuing thread does not stall on
-// it. The same thread's cp_async_wait_all() waits for all its copies.
-__device__ __forceinline__ void cp_async_4(uint32_t dst_smem, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst_smem), "l"(src) : "memory");
+// Loads of kernel inputs. Every kernel here is launched as a programmatic
+// dependent of the previous grid on its stream, so it can start while that
+// grid still writes the buffers it will read (it reads them only after
+// griddepcontrol.wait). Such data must come neither through the read-only
+// (non-coherent) path nor from an L1 line that an earlier kernel left on this
+// SM: measured on GB300, a top-k launched this way read stale scores through
+// the read-only path. These loads (ld.global.cg through the __ldcg intrinsic,
+// which the compiler schedules as ordinary loads) are cached in L2 only.
+__device__ __forceinline__ uint32_t ld_in(const uint32_t *p) { return __ldcg(p); }
+__device__ __forceinline__ int32_t ld_in(const int32_t *p) { return __ldcg(p); }
+__device__ __forceinline__ float ld_in(const float *p) { return __ldcg(p); }
+__device__ __forceinline__ uint4 ld_in(const uint4 *p) { return __ldcg(p); }
+__device__ __forceinline__ float4 ld_in(const float4 *p) { return __ldcg(p); }
+// One binary16 value (its bits), L2 only.
+__device__ __forceinline__ uint16_t ld_in_u16(const void *p) {
+    return __ldcg(reinterpret_cast<const unsigned short *>(p));
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Acquire load of a global word at GPU scope.
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
@@ -141,18 +161,20 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v
     return old;
 }
 
-// Waits (bounded by WAIT_LIMIT_NS) until the word at p is at least `target`,
+// Waits (bounded by limit_ns) until the word at p is at least `target`,
 // with acquire semantics at GPU scope. Returns false if it gave up.
-__device__ __forceinline__ bool wait_word_reaches(const uint32_t *p, uint32_t target) {
+__device__ __forceinline__ bool wait_word_reaches(const uint32_t *p, uint32_t target,
+                                                  uint64_t limit_ns = WAIT_LIMIT_NS) {
     if (ld_acquire_gpu(p) >= target) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (ld_acquire_gpu(p) >= target) return true;
-        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }
+
 
 // Asks the TMA unit to bring [src, src + bytes) into L2 (no destination, no
 // completion to wait for). src 16-byte aligned; bytes % 16 == 0.

@@ -1,5 +1,6 @@
 // C ABI of the QSA selection library: argument checks, then launches on the
 // caller's stream. Declarations and the contract: include/qsa.h.
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 #include <vector>
@@ -8,6 +9,14 @@
 #include "qsa_internal.cuh"
 
 namespace qsa {
+
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<uint32_t> g_inject{0u};
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+uint32_t debug_inject() { return g_inject.load(std::memory_order_relaxed); }
 
 int device_sm_count() {
     static std::mutex mu;
@@ -262,6 +271,13 @@ qsa_status qsa_get_device_error(uint32_t *code, cudaStream_t stream) {
     if (e == cudaSuccess) e = qsa::tc_error_read_clear(&b, stream);
     *code = a | (b << 8);
     return from_cuda(e);
+}
+
+qsa_status qsa_debug_inject(uint32_t faults, uint64_t wait_limit_ns) {
+    if ((faults & ~3u) != 0u || wait_limit_ns == 0 || wait_limit_ns > 60000000000ull) return QSA_ERR_INVALID;
+    qsa::g_inject.store(faults, std::memory_order_relaxed);
+    qsa::g_wait_limit_ns.store(wait_limit_ns, std::memory_order_relaxed);
+    return QSA_OK;
 }
 
 const char *qsa_status_string(qsa_status status) {

@@ -72,6 +72,11 @@ cudaError_t launch_topk_all(int nq, int active, int k, int32_t *ids, cudaStream_
 
 // Error words of the kernels (bounded waits that gave up); read and clear.
 cudaError_t topk_error_read_clear(uint32_t *word, cudaStream_t stream);
+// Upper bound (ns) of every spin-wait in the kernels launched from now on:
+// 2 s, unless qsa_debug_inject changed it.
+uint64_t wait_limit_ns();
+// qsa_debug_inject's fault bits for the kernels launched from now on (0 in use).
+uint32_t debug_inject();
 cudaError_t tc_error_read_clear(uint32_t *word, cudaStream_t stream);
 
 }  // namespace qsa

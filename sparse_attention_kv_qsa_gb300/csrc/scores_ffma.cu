@@ -17,6 +17,7 @@
 // scale is applied once per score in the epilogue.
 #include <cuda_fp16.h>
 
+#include "ptx.cuh"
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(FTHREADS, 2)
             float v = 0.f;
             if (q0 + j < nq) {
                 const float *qp = q + static_cast<size_t>(q0 + j) * (HEADS * D) + d;
-                v = ((qp[0] + qp[D]) + qp[2 * D]) + qp[3 * D];
+                v = ((ld_in(qp) + ld_in(qp + D)) + ld_in(qp + 2 * D)) + ld_in(qp + 3 * D);
             }
             s_t[d * SPAD + j] = v;
         }
@@ -81,16 +82,17 @@ __global__ void __launch_bounds__(FTHREADS, 2)
                             reinterpret_cast<const float4 *>(kblk + static_cast<size_t>(b) * D + dc + h * 16);
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            const float4 f = src[u];
+                            const float4 f = ld_in(src + u);
                             v[4 * u] = f.x;
                             v[4 * u + 1] = f.y;
                             v[4 * u + 2] = f.z;
                             v[4 * u + 3] = f.w;
                         }
                     } else {
-                        const int4 raw =
-                            *reinterpret_cast<const int4 *>(kq8 + static_cast<size_t>(b) * D + dc + h * 16);
-                        const int w[4] = {raw.x, raw.y, raw.z, raw.w};
+                        const uint4 raw =
+                            ld_in(reinterpret_cast<const uint4 *>(kq8 + static_cast<size_t>(b) * D + dc + h * 16));
+                        const int w[4] = {static_cast<int>(raw.x), static_cast<int>(raw.y), static_cast<int>(raw.z),
+                                          static_cast<int>(raw.w)};
 #pragma unroll
                         for (int u = 0; u < 4; ++u)
 #pragma unroll
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(FTHREADS, 2)
             if constexpr (kInt8) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    if (bb + e < active) sc[e] = __half2float(kscale[bb + e]);
+                    if (bb + e < active) sc[e] = __half2float(__ushort_as_half(ld_in_u16(kscale + bb + e)));
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {

@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(ROWS_THREADS)
     const int r = static_cast<int>(w / ngr), g = static_cast<int>(w % ngr);
     const int b = g * GROUP_BLOCKS + lane;
     uint32_t key = 0u;
-    if (b < active) key = score_key(__ldg(scores + static_cast<size_t>(r) * active + b));
+    if (b < active) key = score_key(ld_in(scores + static_cast<size_t>(r) * active + b));
     key = __reduce_max_sync(FULL_MASK, key);
     if (lane == 0) gmax[w] = key;
 }

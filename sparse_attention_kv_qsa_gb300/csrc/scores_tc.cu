@@ -101,7 +101,9 @@ struct TcBarriers {
     uint64_t acc_empty[2];          // epilogue -> MMA: accumulator 0 / 1 read out
     uint64_t a_ready;               // query slices in TMEM
     uint64_t q_peer;                // CTA pairs: the peer's half of the query slices landed
+    uint64_t mma_drain;             // MMA thread: every MMA it issued has completed
     uint32_t tmem_base;
+    uint32_t abort;                 // set by the first timed-out wait: later waits return at once
 };
 
 static_assert(sizeof(TcBarriers) <= 256, "barriers fit their slot");
@@ -132,8 +134,19 @@ __device__ __forceinline__ uint32_t qs_off(int s, int r, int c) {
     return QS_OFF + s * QS_SLICE_BYTES + r * 256 + ((c ^ (r & 15)) << 4);
 }
 
-__device__ __forceinline__ void wait_or_flag(uint64_t *bar, uint32_t parity) {
-    if (!mbar_wait(bar, parity)) atomicOr(&g_tc_error, 1u);
+// A bounded wait of the pipeline. The first one that runs out sets the
+// error word and the CTA's abort word; from then on every wait of the CTA
+// returns false at once, so the roles leave their loops (each first waits,
+// bounded, for its own asynchronous operations in flight) instead of each
+// running out in turn.
+__device__ __forceinline__ bool wait_or_flag(uint64_t *bar, uint32_t parity, uint32_t *abort, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;   // the common case reads no abort word
+    volatile uint32_t *ab = abort;
+    if (*ab != 0u) return false;
+    if (mbar_wait(bar, parity, limit_ns, ab)) return true;
+    *ab = 1u;
+    atomicOr(&g_tc_error, 1u);
+    return false;
 }
 
 // x = hi + mid + lo, each an fp32 bit pattern whose low 16 bits are zero
@@ -158,7 +171,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     scores_tc_kernel(const float *__restrict__ q, const __half *__restrict__ kscale, int nq, int active,
                      int ntiles, int ctas_per_group, float *__restrict__ scores, uint32_t *__restrict__ gmax,
                      const __grid_constant__ CUtensorMap key_map, const __grid_constant__ CUtensorMap out_map,
-                     int use_tma, int pair) {
+                     int use_tma, int pair, uint64_t wait_ns, uint32_t inject) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -189,6 +202,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         mbar_init(&bars->a_ready, EPI_THREADS);
         mbar_init(&bars->q_peer, 1);
+        mbar_init(&bars->mma_drain, 1);
+        bars->abort = 0u;
         if (pair) mbar_arrive_expect_tx(&bars->q_peer, QS_PEER_BYTES);
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -202,13 +217,36 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (pair) cluster_sync_all();  // ... in both CTAs of the pair
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
+    uint32_t *abort = &bars->abort;
+    // The pipeline's waits: bounded by wait_ns, abandoned once the CTA aborts.
+    auto wait = [&](uint64_t *bar, uint32_t parity) { return wait_or_flag(bar, parity, abort, wait_ns); };
     // Inputs may come from the previous grid on the stream; the next grid (the
     // top-k) may launch now and waits for this one's scores itself.
     grid_dependency_wait();
     grid_launch_dependents();
 
-    // Head-summed query slices: every warp but the producer builds them (one
-    // 8-d chunk of one query per task, coalesced loads) into shared memory.
+    const int npieces = 4 * nlocal;
+    // Diagnostics only (qsa_debug_inject): CTA 0 never loads its first piece,
+    // so a wait of the pipeline runs out.
+    const bool skip_first = (inject & 1u) != 0u && blockIdx.x == 0;
+    auto issue_piece = [&](int p) {   // piece p: tile p / 4, K-half (p / 2) % 2, rows 64 * (p % 2) .. +63
+        const int slot = p % RAW_SLOTS;
+        const int row0 = tile_b0(p >> 2) + (p & 1) * PIECE_ROWS;
+        if (p == 0 && skip_first) return;
+        if (row0 < active) {
+            mbar_arrive_expect_tx(&bars->raw_full[slot], PIECE_BYTES);
+            tma_load_2d(base + RAW_OFF + slot * RAW_SLOT_BYTES, &key_map, ((p >> 1) & 1) * KHALF, row0,
+                        &bars->raw_full[slot]);
+        } else {
+            mbar_arrive(&bars->raw_full[slot]);
+        }
+    };
+
+    // Head-summed query slices: every warp but the producer (which is already
+    // streaming keys) builds them into shared memory, one task per 4 d of one
+    // query: a warp's 32 tasks read 512 contiguous bytes of one head row per
+    // load, so every L2 sector is fetched once; each thread has the loads of
+    // four tasks in flight at a time.
     // CTA pairs (a cluster of two in the same query group) split the rows:
     // each builds 64 and also writes them into its peer's staging with
     // asynchronous cluster stores that count on the peer's q_peer barrier, so
@@ -218,46 +256,55 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp != PRODUCER_WARP) {
         const uint32_t rank = pair ? cluster_ctarank() : 0u;
         const int rows0 = pair ? static_cast<int>(rank) * (QGROUP / 2) : 0;
-        const int ntask = (pair ? QGROUP / 2 : QGROUP) * (D / 8);   // a power of two
+        const int ntask = (pair ? QGROUP / 2 : QGROUP) * (D / 4);   // a power of two
         const uint32_t peer_bar = pair ? map_shared_rank(smem_u32(&bars->q_peer), rank ^ 1u) : 0u;
         const uint32_t peer_base = pair ? map_shared_rank(base, rank ^ 1u) : 0u;
-        const int rot = (j0 * 37 * 16) & (ntask - 1);
-#pragma unroll 2
-        for (int t0 = tid - 32; t0 < ntask; t0 += TC_THREADS - 32) {
-            const int t = (t0 + rot) & (ntask - 1);
-            const int r = rows0 + (t >> 4), c = t & 15;
-            float x[8];
-            if (r < qn) {
-                const float4 *p =
-                    reinterpret_cast<const float4 *>(q + static_cast<size_t>(q0 + r) * (HEADS * D) + 8 * c);
-                float4 a[4][2];
+        const int rot = (j0 * 37 * 32) & (ntask - 1);   // a multiple of 32: warps keep whole rows
+        constexpr int BUILDERS = TC_THREADS - 32, TPT = 4;   // tasks per thread in flight
+#pragma unroll 1
+        for (int t0 = tid - 32; t0 < ntask; t0 += TPT * BUILDERS) {
+            // All loads of TPT tasks first (the stores below are volatile asm,
+            // which the compiler does not move loads across).
+            float4 a[TPT][4];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    a[h][0] = __ldg(p + h * (D / 4));
-                    a[h][1] = __ldg(p + h * (D / 4) + 1);
+            for (int u = 0; u < TPT; ++u) {
+                const int tu = t0 + u * BUILDERS;
+                const int t = (tu + rot) & (ntask - 1);
+                const int r = rows0 + (t >> 5), c4 = t & 31;
+                if (tu < ntask && r < qn) {
+                    const float4 *p =
+                        reinterpret_cast<const float4 *>(q + static_cast<size_t>(q0 + r) * (HEADS * D)) + c4;
+#pragma unroll
+                    for (int hh = 0; hh < 4; ++hh) a[u][hh] = ld_in(p + hh * (D / 4));
+                } else {
+#pragma unroll
+                    for (int hh = 0; hh < 4; ++hh) a[u][hh] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float v0 = e < 4 ? (&a[0][0].x)[e] : (&a[0][1].x)[e - 4];
-                    const float v1 = e < 4 ? (&a[1][0].x)[e] : (&a[1][1].x)[e - 4];
-                    const float v2 = e < 4 ? (&a[2][0].x)[e] : (&a[2][1].x)[e - 4];
-                    const float v3 = e < 4 ? (&a[3][0].x)[e] : (&a[3][1].x)[e - 4];
-                    x[e] = __fadd_rn(__fadd_rn(__fadd_rn(v0, v1), v2), v3);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = 0.f;
             }
-            uint32_t h[8], m[8], l[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) split3(x[e], h[e], m[e], l[e]);
-            const uint32_t w[3][4] = {{pack2(h[0], h[1]), pack2(h[2], h[3]), pack2(h[4], h[5]), pack2(h[6], h[7])},
-                                      {pack2(m[0], m[1]), pack2(m[2], m[3]), pack2(m[4], m[5]), pack2(m[6], m[7])},
-                                      {pack2(l[0], l[1]), pack2(l[2], l[3]), pack2(l[4], l[5]), pack2(l[6], l[7])}};
+            for (int u = 0; u < TPT; ++u) {
+                const int tu = t0 + u * BUILDERS;
+                if (tu >= ntask) break;
+                const int t = (tu + rot) & (ntask - 1);
+                const int r = rows0 + (t >> 5), c4 = t & 31;
+                const float x[4] = {
+                    __fadd_rn(__fadd_rn(__fadd_rn(a[u][0].x, a[u][1].x), a[u][2].x), a[u][3].x),
+                    __fadd_rn(__fadd_rn(__fadd_rn(a[u][0].y, a[u][1].y), a[u][2].y), a[u][3].y),
+                    __fadd_rn(__fadd_rn(__fadd_rn(a[u][0].z, a[u][1].z), a[u][2].z), a[u][3].z),
+                    __fadd_rn(__fadd_rn(__fadd_rn(a[u][0].w, a[u][1].w), a[u][2].w), a[u][3].w)};
+                uint32_t h[4], m[4], l[4];
 #pragma unroll
-            for (int sl = 0; sl < 3; ++sl) {
-                st_shared_v4(base + qs_off(sl, r, c), w[sl][0], w[sl][1], w[sl][2], w[sl][3]);
-                if (pair) st_async_v4(peer_base + qs_off(sl, r, c), peer_bar, w[sl][0], w[sl][1], w[sl][2], w[sl][3]);
+                for (int e = 0; e < 4; ++e) split3(x[e], h[e], m[e], l[e]);
+                const uint32_t w[3][2] = {{pack2(h[0], h[1]), pack2(h[2], h[3])},
+                                          {pack2(m[0], m[1]), pack2(m[2], m[3])},
+                                          {pack2(l[0], l[1]), pack2(l[2], l[3])}};
+                // 8 bytes: half (c4 % 2) of the 16-byte chunk c4 / 2 of row r.
+#pragma unroll
+                for (int sl = 0; sl < 3; ++sl) {
+                    const uint32_t off = qs_off(sl, r, c4 >> 1) + 8u * (c4 & 1);
+                    st_shared_v2(base + off, w[sl][0], w[sl][1]);
+                    if (pair) st_async_v2(peer_base + off, peer_bar, w[sl][0], w[sl][1]);
+                }
             }
         }
         sync_non_producer();
@@ -267,19 +314,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ---- raw key pieces -> ring (2-D tensor copies) ------------------------
         // Piece p: tile p / 4, K-half (p / 2) % 2, rows 64 * (p % 2) .. +63.
         if (lane == 0) {
-            const int npieces = 4 * nlocal;
-            for (int p = 0; p < npieces; ++p) {
-                const int slot = p % RAW_SLOTS;
-                wait_or_flag(&bars->raw_empty[slot], ((p / RAW_SLOTS) & 1) ^ 1);
-                const int row0 = tile_b0(p >> 2) + (p & 1) * PIECE_ROWS;
-                if (row0 < active) {
-                    mbar_arrive_expect_tx(&bars->raw_full[slot], PIECE_BYTES);
-                    tma_load_2d(base + RAW_OFF + slot * RAW_SLOT_BYTES, &key_map, ((p >> 1) & 1) * KHALF, row0,
-                                &bars->raw_full[slot]);
-                } else {
-                    mbar_arrive(&bars->raw_full[slot]);
-                }
+            int p = 0;
+            for (; p < npieces; ++p) {
+                if (!wait(&bars->raw_empty[p % RAW_SLOTS], ((p / RAW_SLOTS) & 1) ^ 1)) break;
+                issue_piece(p);
             }
+            // The copies started here must have landed before the CTA leaves:
+            // the last RAW_SLOTS pieces (earlier ones were consumed). Without an
+            // abort these waits return at once.
+            for (int d = p > RAW_SLOTS ? p - RAW_SLOTS : 0; d < p; ++d)
+                if (!(d == 0 && skip_first)) mbar_wait(&bars->raw_full[d % RAW_SLOTS], (d / RAW_SLOTS) & 1, wait_ns);
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
@@ -292,13 +336,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(QGROUP, TILE_N);
             const uint32_t d0 = tmem + ACC0_COL, d1 = tmem + ACC1_COL;
-            wait_or_flag(&bars->a_ready, 0);
+            bool ok = wait(&bars->a_ready, 0);
             tc_fence_after_sync();
-            for (int li = 0; li < nlocal; ++li) {
+            for (int li = 0; ok && li < nlocal; ++li) {
                 for (int kh = 0; kh < 2; ++kh) {
                     const int t = 2 * li + kh, ks = t % KS_STAGES;
-                    wait_or_flag(&bars->ks_full[ks], (t / KS_STAGES) & 1);
-                    if (kh == 0) wait_or_flag(&bars->acc_empty[0], (li & 1) ^ 1);
+                    ok = wait(&bars->ks_full[ks], (t / KS_STAGES) & 1);
+                    if (ok && kh == 0) ok = wait(&bars->acc_empty[0], (li & 1) ^ 1);
+                    if (!ok) break;
                     tc_fence_after_sync();
                     // Slice s of this K-half at stage + s * KS_SUB_BYTES; +32 B per K-step.
                     const uint64_t kdesc = sw128_kmajor_desc(base + KS_OFF + ks * KS_STAGE_BYTES);
@@ -308,7 +353,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                        idesc, (kh | kk) != 0 ? 1u : 0u);
                     if (kh == 1) tc_commit(&bars->acc_full[0]);
                     if (kh == 0) {
-                        wait_or_flag(&bars->acc_empty[1], (li & 1) ^ 1);
+                        ok = wait(&bars->acc_empty[1], (li & 1) ^ 1);
+                        if (!ok) break;
                         tc_fence_after_sync();
                     }
 #pragma unroll
@@ -326,8 +372,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     tc_commit(&bars->ks_empty[ks]);
                 }
-                tc_commit(&bars->acc_full[1]);
+                if (ok) tc_commit(&bars->acc_full[1]);
             }
+            // Every MMA issued here has completed before TMEM is freed (at
+            // once without an abort: the epilogue has read the last tile).
+            tc_commit(&bars->mma_drain);
+            mbar_wait(&bars->mma_drain, 0, wait_ns);
         }
         __syncwarp();
     } else if (warp < EPI_WARP0 + EPI_WARPS) {
@@ -336,7 +386,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int team = (warp - EPI_WARP0) >> 2;           // column half of a tile: 0 or 1
         const int row = 32 * quarter + lane;                // query row within the group
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
-        if (pair) wait_or_flag(&bars->q_peer, 0);   // the peer's 64 rows have landed
+        // The epilogue's waits are not acted on: after an abort they return at
+        // once, and the remaining tiles read (garbage) TMEM and store garbage
+        // scores -- invalid outputs, reported by the error word -- with the
+        // same barrier pattern, so no warp is left waiting at a barrier.
+        if (pair) wait(&bars->q_peer, 0);   // the peer's 64 rows have landed
         // This warp's 32 query rows, half of the 16-byte chunks: staged slices -> TMEM.
         for (int c = 8 * team; c < 8 * team + 8; ++c) {
 #pragma unroll
@@ -363,7 +417,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int nb = min(TILE_N, active - b0);
             // hi*hi first (final early), then the corrections.
             float v[TILE_N / 2];
-            wait_or_flag(&bars->acc_full[0], li & 1);
+            wait(&bars->acc_full[0], li & 1);
             tc_fence_after_sync();
             {
                 uint32_t x0[32], x1[32];
@@ -378,7 +432,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             tc_fence_before_sync();
             mbar_arrive(&bars->acc_empty[0]);
-            wait_or_flag(&bars->acc_full[1], li & 1);
+            wait(&bars->acc_full[1], li & 1);
             tc_fence_after_sync();
             {
                 uint32_t x0[32], x1[32];
@@ -396,7 +450,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if constexpr (kInt8) {
 #pragma unroll
                 for (int j = 0; j < TILE_N / 2; ++j)
-                    if (col0 + j < nb) v[j] = __fmul_rn(v[j], __half2float(kscale[b0 + col0 + j]));
+                    if (col0 + j < nb)
+                        v[j] = __fmul_rn(v[j], __half2float(__ushort_as_half(ld_in_u16(kscale + b0 + col0 + j))));
             }
             // Group maxima: this thread's 64 columns are two 32-block groups.
             // fmaxf skips NaN (an all-NaN group stays NaN, whose key is that of
@@ -502,15 +557,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int cw = converter_index(warp);
         const int sub = lane & 15, rsel = lane >> 4;
         const int c = sub >> 1, part = sub & 1;
-        wait_or_flag(&bars->a_ready, 0);   // query staging has left the key stages
-        for (int t = 0; t < 2 * nlocal; ++t) {             // K-half stage t: tile t / 2, K-half t % 2
+        const int nstage = wait(&bars->a_ready, 0) ? 2 * nlocal : 0;   // query staging has left the key stages
+        for (int t = 0; t < nstage; ++t) {             // K-half stage t: tile t / 2, K-half t % 2
             const int ks = t % KS_STAGES;
             const uint32_t kbase = base + KS_OFF + ks * KS_STAGE_BYTES;
-            wait_or_flag(&bars->ks_empty[ks], ((t / KS_STAGES) & 1) ^ 1);
+            if (!wait(&bars->ks_empty[ks], ((t / KS_STAGES) & 1) ^ 1)) break;
+            bool ok = true;
             for (int rh = 0; rh < 2; ++rh) {
                 const int p = 2 * t + rh;
                 const int slot = p % RAW_SLOTS;
-                wait_or_flag(&bars->raw_full[slot], (p / RAW_SLOTS) & 1);
+                if (!wait(&bars->raw_full[slot], (p / RAW_SLOTS) & 1)) {
+                    ok = false;
+                    break;
+                }
                 const int row0 = tile_b0(t >> 1) + rh * PIECE_ROWS;
                 const uint32_t src = base + RAW_OFF + slot * RAW_SLOT_BYTES;
                 // A warp's row pairs are i = cw + CONV_WARPS j; all of its reads
@@ -564,6 +623,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 mbar_arrive(&bars->raw_empty[slot]);
             }
+            if (!ok) break;
             fence_proxy_async_smem();
             mbar_arrive(&bars->ks_full[ks]);
         }
@@ -675,9 +735,11 @@ cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq
         return cudaErrorNotSupported;
     if (int8)
         return cudaLaunchKernelEx(&cfg, scores_tc_kernel<true>, q, reinterpret_cast<const __half *>(kscale), nq,
-                                  active, ntiles, per, scores, gmax, key_map, out_map, use_tma, pair);
+                                  active, ntiles, per, scores, gmax, key_map, out_map, use_tma, pair,
+                                  wait_limit_ns(), debug_inject());
     return cudaLaunchKernelEx(&cfg, scores_tc_kernel<false>, q, static_cast<const __half *>(nullptr), nq, active,
-                              ntiles, per, scores, gmax, key_map, out_map, use_tma, pair);
+                              ntiles, per, scores, gmax, key_map, out_map, use_tma, pair, wait_limit_ns(),
+                              debug_inject());
 }
 
 cudaError_t tc_error_read_clear(uint32_t *word, cudaStream_t stream) {

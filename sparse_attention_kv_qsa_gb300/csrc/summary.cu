@@ -53,8 +53,8 @@ __global__ void __launch_bounds__(SUM_WARPS * 32)
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
         if (t < n) {
-            w[t] = __ldg(rows + t * (D / 4));
-            sc[t] = __half2float(scl[t]);
+            w[t] = ld_in(rows + t * (D / 4));
+            sc[t] = __half2float(__ushort_as_half(ld_in_u16(scl + t)));
         }
     }
     float m[4];

@@ -31,6 +31,8 @@
 //  the threshold, and the digits below run on that list alone. A list shorter than k or longer
 //  than its capacity sends the row to the exact passes, so the result is
 //  exact either way.
+//  Rows of at most 8,192 scores are read once into registers (up to 16 per
+//  thread) and the whole digit search runs on them (topk_reg_row).
 //  Exact passes: pass A reads the row and builds the 11-bit histogram in
 //  shared memory; pass B streams the row again -- from L2, where pass A just
 //  left it -- and marks keys above the leading bin in a shared-memory
@@ -96,10 +98,11 @@ __device__ __forceinline__ uint32_t float_bits_to_key(uint32_t bits) {
     return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
 
-// Score and group-maximum loads. The top-k kernel reads data that no thread
-// of its grid writes, through the read-only path (kCoherent false); the fused
-// decode kernel reads scores its own grid wrote before a grid-wide release,
-// so it uses coherent global loads (kCoherent true).
+// Score and group-maximum loads. The top-k kernels read data that the
+// previous grid on the stream wrote, cached in L2 only (ld_in: the grid may
+// have started before that grid finished); the fused decode kernel reads
+// scores its own grid wrote before a grid-wide release, through coherent
+// GPU-scope loads (kCoherent true).
 template <bool kCoherent>
 __device__ __forceinline__ uint32_t ld_word(const uint32_t *p) {
     if constexpr (kCoherent) {
@@ -107,7 +110,7 @@ __device__ __forceinline__ uint32_t ld_word(const uint32_t *p) {
         asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
         return v;
     } else {
-        return __ldg(p);
+        return ld_in(p);
     }
 }
 template <bool kCoherent>
@@ -120,7 +123,7 @@ __device__ __forceinline__ uint4 ld_quad(const uint4 *p) {
                      : "memory");
         return v;
     } else {
-        return __ldg(p);
+        return ld_in(p);
     }
 }
 
@@ -245,6 +248,67 @@ __device__ __forceinline__ void stream_row(const uint32_t *g, int n, int head, i
     __syncthreads();
 }
 
+// The end of one row's selection, shared by every path: selbits marks the
+// selected ids; when `ties` is set, the first kk ids marked in tiebits (in id
+// order) join them. Writes the row's k ids in ascending order to out.
+__device__ __forceinline__ void finish_row(uint32_t *selbits, const uint32_t *tiebits, int nwords, bool ties,
+                                           uint32_t kk, int k, int32_t *__restrict__ out, RowShared &sh, int tid,
+                                           int lane, int warp) {
+    // Each thread owns a contiguous run of bitmap words, so ids stay ordered.
+    const int wpt = (nwords + ROW_THREADS - 1) / ROW_THREADS;
+    const int wb = min(nwords, tid * wpt), we = min(nwords, wb + wpt);
+    if (ties) {  // uniform: the first kk ties in id order join the selection
+        uint32_t c = 0u;
+        for (int wd = wb; wd < we; ++wd) c += __popc(tiebits[wd]);
+        uint32_t run = block_excl_scan(c, sh.scan_tot, lane, warp);
+        for (int wd = wb; wd < we && run < kk; ++wd) {
+            uint32_t bits = tiebits[wd], add = 0u;
+            while (bits != 0u && run < kk) {
+                add |= bits & (~bits + 1u);
+                bits &= bits - 1u;
+                ++run;
+            }
+            selbits[wd] |= add;
+        }
+        __syncthreads();
+    }
+    if (wpt == 4) {
+        // Up to 65,536 scores (nwords <= 2,048): a thread's four words as one
+        // conflict-free 16-byte load, kept in registers for both passes.
+        uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
+        if (wb < nwords) w4 = *reinterpret_cast<const uint4 *>(selbits + wb);
+        // Words past nwords (the last thread, when nwords % 4 != 0) belong to
+        // the tie bitmap that follows: drop them.
+        const uint32_t wv[4] = {w4.x, wb + 1 < nwords ? w4.y : 0u, wb + 2 < nwords ? w4.z : 0u,
+                                wb + 3 < nwords ? w4.w : 0u};
+        uint32_t pos = block_excl_scan(__popc(wv[0]) + __popc(wv[1]) + __popc(wv[2]) + __popc(wv[3]), sh.scan_tot,
+                                       lane, warp);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            uint32_t bits = wv[e];
+            while (bits != 0u) {
+                const int b = __ffs(bits) - 1;
+                bits &= bits - 1u;
+                if (pos < static_cast<uint32_t>(k)) out[pos] = (wb + e) * 32 + b;  // always, for consistent counts
+                ++pos;
+            }
+        }
+    } else {
+        uint32_t c = 0u;
+        for (int wd = wb; wd < we; ++wd) c += __popc(selbits[wd]);
+        uint32_t pos = block_excl_scan(c, sh.scan_tot, lane, warp);
+        for (int wd = wb; wd < we; ++wd) {
+            uint32_t bits = selbits[wd];
+            while (bits != 0u) {
+                const int b = __ffs(bits) - 1;
+                bits &= bits - 1u;
+                if (pos < static_cast<uint32_t>(k)) out[pos] = wd * 32 + b;  // always, for consistent counts
+                ++pos;
+            }
+        }
+    }
+}
+
 // One row's exact top-k by one 512-thread CTA (the whole of topk_row_kernel;
 // also the second phase of the fused decode kernel). Dynamic shared memory:
 // row_smem_bytes(active).
@@ -290,6 +354,22 @@ __device__ __forceinline__ void topk_row(const float *__restrict__ scores, const
     const bool use_gmax = gmax != nullptr && 2 * k <= ngr && ngr <= 4 * ROW_THREADS;
     const bool try_list = use_gmax || (n >= FAST_MIN_ACTIVE && r_target <= nsamp / 2);
 
+    // Shared memory is cleared before the wait below (it does not depend on
+    // the previous grid).
+    if (tid == 0) {
+        sh.cand_n = 0u;
+        sh.glist_n = 0u;
+    }
+    if (!try_list || use_gmax) {   // the exact path's histogram, or the group-maximum bins
+        static_assert(HIST_A == 4 * ROW_THREADS, "one 16-byte store per thread clears histA");
+        reinterpret_cast<uint4 *>(sh.histA)[tid] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int i = tid; i < BINS_R; i += ROW_THREADS) sh.histR[i] = 0u;
+    for (int i = tid; i < nwords; i += ROW_THREADS) {
+        selbits[i] = 0u;
+        tiebits[i] = 0u;
+    }
+
     // The scores may come from the previous grid on the stream (launched as
     // its programmatic dependent); nothing global is read before this.
     grid_dependency_wait();
@@ -318,19 +398,6 @@ __device__ __forceinline__ void topk_row(const float *__restrict__ scores, const
         }
     }
 
-    if (tid == 0) {
-        sh.cand_n = 0u;
-        sh.glist_n = 0u;
-    }
-    if (!try_list || use_gmax) {   // the exact path's histogram, or the group-maximum bins
-        static_assert(HIST_A == 4 * ROW_THREADS, "one 16-byte store per thread clears histA");
-        reinterpret_cast<uint4 *>(sh.histA)[tid] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    for (int i = tid; i < BINS_R; i += ROW_THREADS) sh.histR[i] = 0u;
-    for (int i = tid; i < nwords; i += ROW_THREADS) {
-        selbits[i] = 0u;
-        tiebits[i] = 0u;
-    }
     if (use_gmax) {   // the group maxima's warp maxima ride on the same barrier
         uint32_t m = 0u;
 #pragma unroll
@@ -439,10 +506,10 @@ __device__ __forceinline__ void topk_row(const float *__restrict__ scores, const
         // each stalled on an L2 round trip).
         if (tg > NEG_INF_KEY) {
             const float ft = __uint_as_float(tg >= 0x80000000u ? (tg ^ 0x80000000u) : ~tg);
-            const uint32_t key_base = smem_u32(sh.cand_key);
             // Slots for one 32-score step's hits: bit j of `hits` is the score
-            // at index idx(j), which reaches its slot by an asynchronous 4-byte
-            // copy (the registers that held it are reused by then).
+            // at index idx(j); the slot records the index, and the listed
+            // scores are gathered after the pass (the registers that held
+            // them are reused by then).
             auto book = [&](uint32_t hits, auto idx) {
                 const uint32_t c = __popc(hits);
                 const uint32_t incl = warp_incl_scan(c, lane);
@@ -454,11 +521,7 @@ __device__ __forceinline__ void topk_row(const float *__restrict__ scores, const
                     while (hits != 0u) {
                         const int j = __ffs(hits) - 1;
                         hits &= hits - 1u;
-                        if (slot < static_cast<uint32_t>(CAND_MAX)) {
-                            const int i = idx(j);
-                            sh.cand_idx[slot] = static_cast<uint32_t>(i);
-                            cp_async_4(key_base + 4u * slot, g + i);
-                        }
+                        if (slot < static_cast<uint32_t>(CAND_MAX)) sh.cand_idx[slot] = static_cast<uint32_t>(idx(j));
                         ++slot;
                     }
                 }
@@ -534,10 +597,7 @@ __device__ __forceinline__ void topk_row(const float *__restrict__ scores, const
                 auto list_scalar = [&](int i) {
                     if (__uint_as_float(ld_word<kCoherent>(g + i)) >= ft) {
                         const uint32_t slot = atomicAdd(&sh.cand_n, 1u);
-                        if (slot < static_cast<uint32_t>(CAND_MAX)) {
-                            sh.cand_idx[slot] = static_cast<uint32_t>(i);
-                            cp_async_4(key_base + 4u * slot, g + i);
-                        }
+                        if (slot < static_cast<uint32_t>(CAND_MAX)) sh.cand_idx[slot] = static_cast<uint32_t>(i);
                     }
                 };
                 for (int i = tid; i < head; i += ROW_THREADS) list_scalar(i);
@@ -572,22 +632,22 @@ __device__ __forceinline__ void topk_row(const float *__restrict__ scores, const
         } else if (tid == 0) {
             sh.cand_n = static_cast<uint32_t>(CAND_MAX) + 1u;  // would list the whole row
         }
-        cp_async_wait_all();  // this thread's copies of listed scores have landed
         __syncthreads();
         const uint32_t nc = sh.cand_n;
         listed = nc >= kk && nc <= static_cast<uint32_t>(CAND_MAX);
         if (listed && use_gmax) {
-            // The listed scores become keys in place (their maximum, the row's,
-            // is known from the group maxima).
+            // The listed scores are gathered (one L2 round trip for the whole
+            // list) as keys (their maximum, the row's, is known from the group
+            // maxima).
 #pragma unroll 4
             for (int j = tid; j < static_cast<int>(nc); j += ROW_THREADS)
-                sh.cand_key[j] = float_bits_to_key(sh.cand_key[j]);
+                sh.cand_key[j] = float_bits_to_key(ld_word<kCoherent>(g + sh.cand_idx[j]));
             __syncthreads();
         } else if (listed) {
-            // The listed scores become keys in place; the largest is kept.
+            // The listed scores are gathered as keys; the largest is kept.
 #pragma unroll 4
             for (int j = tid; j < static_cast<int>(nc); j += ROW_THREADS) {
-                const uint32_t key = float_bits_to_key(sh.cand_key[j]);
+                const uint32_t key = float_bits_to_key(ld_word<kCoherent>(g + sh.cand_idx[j]));
                 sh.cand_key[j] = key;
                 kmax = max(kmax, key);
             }
@@ -718,66 +778,115 @@ __device__ __forceinline__ void topk_row(const float *__restrict__ scores, const
         }
     }
 
-    // Each thread owns a contiguous run of bitmap words, so ids stay ordered.
-    const int wpt = (nwords + ROW_THREADS - 1) / ROW_THREADS;
-    const int wb = min(nwords, tid * wpt), we = min(nwords, wb + wpt);
-    if (!doneA && !done) {  // uniform: the first kk ties in id order join the selection
-        uint32_t c = 0u;
-        for (int wd = wb; wd < we; ++wd) c += __popc(tiebits[wd]);
-        uint32_t run = block_excl_scan(c, sh.scan_tot, lane, warp);
-        for (int wd = wb; wd < we && run < kk; ++wd) {
-            uint32_t bits = tiebits[wd], add = 0u;
-            while (bits != 0u && run < kk) {
-                add |= bits & (~bits + 1u);
-                bits &= bits - 1u;
-                ++run;
-            }
-            selbits[wd] |= add;
-        }
-        __syncthreads();
-    }
-    int32_t *out = ids + row * static_cast<size_t>(k);
-    if (wpt == 4) {
-        // Up to 65,536 scores (nwords <= 2,048): a thread's four words as one
-        // conflict-free 16-byte load, kept in registers for both passes.
-        uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
-        if (wb < nwords) w4 = *reinterpret_cast<const uint4 *>(selbits + wb);
-        // Words past nwords (the last thread, when nwords % 4 != 0) belong to
-        // the tie bitmap that follows: drop them.
-        const uint32_t wv[4] = {w4.x, wb + 1 < nwords ? w4.y : 0u, wb + 2 < nwords ? w4.z : 0u,
-                                wb + 3 < nwords ? w4.w : 0u};
-        uint32_t pos = block_excl_scan(__popc(wv[0]) + __popc(wv[1]) + __popc(wv[2]) + __popc(wv[3]), sh.scan_tot,
-                                       lane, warp);
+    finish_row(selbits, tiebits, nwords, !doneA && !done, kk, k, ids + row * static_cast<size_t>(k), sh, tid,
+               lane, warp);
+}
+
+// Register-resident exact top-k of a short row (n <= PER * 512 scores,
+// k < n): every score is read once, into registers (thread t holds scores
+// t, t + 512, ...), and the digit search runs on those registers: the 11-bit
+// leading digit, then 8, 8 and 5 bits over the keys that match the prefix,
+// each a shared-memory histogram scanned from the top (the same digits and
+// tie rule as topk_row). The selection and tie bitmaps are built by warp
+// ballots: with this layout one warp's 32 scores of step j are exactly one
+// bitmap word.
+template <int PER, bool kCoherent>
+__device__ __forceinline__ void topk_reg_row(const float *__restrict__ scores, int n, int k,
+                                             int32_t *__restrict__ ids, size_t row) {
+    static_assert(PER >= 1 && PER <= 32, "one validity bit per register");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwords = (n + 31) >> 5;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    RowShared &sh = *reinterpret_cast<RowShared *>(smem_raw);
+    uint32_t *selbits = reinterpret_cast<uint32_t *>(smem_raw + SHARED_BYTES);
+    uint32_t *tiebits = selbits + nwords;
+    const uint32_t *g = reinterpret_cast<const uint32_t *>(scores + row * static_cast<size_t>(n));
+
+    static_assert(HIST_A == 4 * ROW_THREADS && BINS_R <= ROW_THREADS, "one clearing store per thread");
+    reinterpret_cast<uint4 *>(sh.histA)[tid] = make_uint4(0u, 0u, 0u, 0u);   // before the wait: no global data
+    if (tid < BINS_R) sh.histR[tid] = 0u;
+    grid_dependency_wait();   // the scores may come from the previous grid
+    uint32_t key[PER];
+    uint32_t valid = 0u;      // bit j: score j * 512 + tid exists
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            uint32_t bits = wv[e];
-            while (bits != 0u) {
-                const int b = __ffs(bits) - 1;
-                bits &= bits - 1u;
-                if (pos < static_cast<uint32_t>(k)) out[pos] = (wb + e) * 32 + b;  // always, for consistent counts
-                ++pos;
-            }
-        }
-    } else {
-        uint32_t c = 0u;
-        for (int wd = wb; wd < we; ++wd) c += __popc(selbits[wd]);
-        uint32_t pos = block_excl_scan(c, sh.scan_tot, lane, warp);
-        for (int wd = wb; wd < we; ++wd) {
-            uint32_t bits = selbits[wd];
-            while (bits != 0u) {
-                const int b = __ffs(bits) - 1;
-                bits &= bits - 1u;
-                if (pos < static_cast<uint32_t>(k)) out[pos] = wd * 32 + b;  // always, for consistent counts
-                ++pos;
-            }
+    for (int j = 0; j < PER; ++j) {
+        const int i = j * ROW_THREADS + tid;
+        key[j] = 0u;
+        if (i < n) {
+            key[j] = ld_word<kCoherent>(g + i);
+            valid |= 1u << j;
         }
     }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        key[j] = float_bits_to_key(key[j]);
+        if (valid >> j & 1u) atomicAdd(&sh.histA[key[j] >> 21], 1u);
+    }
+    __syncthreads();
+    if (tid < HIST_A / GROUP) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(&sh.histA[GROUP * tid]);
+        const uint4 b = *reinterpret_cast<const uint4 *>(&sh.histA[GROUP * tid + 4]);
+        sh.groupA[tid] = a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w;
+    }
+    __syncthreads();
+    uint32_t kk = static_cast<uint32_t>(k);
+    if (warp == 0) warp_select_2048(kk, sh, lane);
+    __syncthreads();
+    kk -= sh.sel_above;
+    bool done = sh.sel_cnt == kk;
+    uint32_t prefix = sh.sel_bin << 21, mask = 0xFFE00000u;
+    int shift = 21;
+#pragma unroll 1
+    while (!done && shift > 0) {
+        const int width = min(8, shift);
+        shift -= width;
+        const uint32_t dmask = (1u << width) - 1u;
+#pragma unroll
+        for (int j = 0; j < PER; ++j)
+            if ((valid >> j & 1u) && (key[j] & mask) == prefix) atomicAdd(&sh.histR[(key[j] >> shift) & dmask], 1u);
+        __syncthreads();
+        if (warp == 0) warp_select_256(sh.histR, kk, sh, lane);   // also clears histR
+        __syncthreads();
+        kk -= sh.sel_above;
+        prefix |= sh.sel_bin << shift;
+        mask |= dmask << shift;
+        done = sh.sel_cnt == kk;
+    }
+    // Keys above the prefix are selected; keys equal to it are selected too
+    // when the search ended on a bin taken whole, else they are ties.
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const uint32_t km = key[j] & mask;
+        const bool ok = (valid >> j & 1u) != 0u;
+        const uint32_t sel = __ballot_sync(FULL_MASK, ok && (km > prefix || (done && km == prefix)));
+        const uint32_t tie = __ballot_sync(FULL_MASK, ok && !done && km == prefix);
+        const int wd = j * ROW_WARPS + warp;
+        if (lane == 0 && wd < nwords) {
+            selbits[wd] = sel;
+            tiebits[wd] = tie;
+        }
+    }
+    __syncthreads();
+    finish_row(selbits, tiebits, nwords, !done, kk, k, ids + row * static_cast<size_t>(k), sh, tid, lane, warp);
 }
 
 __global__ void __launch_bounds__(ROW_THREADS, 2)
     topk_row_kernel(const float *__restrict__ scores, const uint32_t *__restrict__ gmax, int active, int k,
                     int32_t *__restrict__ ids) {
     topk_row<false>(scores, gmax, active, k, ids, blockIdx.x);
+}
+
+// Rows of at most REG_MAX_ACTIVE scores take the register-resident path; PER
+// is the smallest of 4, 8, 16 that holds the row. (At 16,384 scores, 32 per
+// thread, the full-row histogram's shared-memory atomics crowd into a few
+// exponent bins and the sampled listing path is faster.)
+constexpr int REG_MAX_ACTIVE = 16 * ROW_THREADS;   // 8,192
+
+template <int PER>
+__global__ void __launch_bounds__(ROW_THREADS, 2)
+    topk_reg_kernel(const float *__restrict__ scores, int active, int k, int32_t *__restrict__ ids) {
+    topk_reg_row<PER, false>(scores, active, k, ids, blockIdx.x);
 }
 
 // Fused decode select (nq <= 4): one cooperative launch scores every key row
@@ -799,7 +908,8 @@ template <int NQ, bool kInt8>
 __global__ void __launch_bounds__(ROW_THREADS, 2)
     select_decode_kernel(const float *__restrict__ q, const float *__restrict__ kblk,
                          const int8_t *__restrict__ kq8, const __half *__restrict__ kscale, int nq, int active,
-                         int k, float *__restrict__ scores, int32_t *__restrict__ ids) {
+                         int k, float *__restrict__ scores, int32_t *__restrict__ ids, uint64_t wait_ns,
+                         uint32_t inject) {
     constexpr int ROWS = ROW_THREADS / dec_tpr<kInt8>();
     __shared__ __align__(16) float qs[NQ][DEC_QROW];   // head-summed queries, zero past nq
     __shared__ uint32_t gk[NQ][ROWS];
@@ -823,9 +933,21 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         }
     }
     if (blockIdx.x >= static_cast<unsigned>(nq)) return;   // the whole CTA
-    if (threadIdx.x == 0 && !wait_word_reaches(&g_decode_sync[gen & 1u], gridDim.x)) atomicOr(&g_topk_error, 2u);
+    // (Diagnostics only, qsa_debug_inject: wait for one arrival more than the
+    // grid has, so the wait runs out.)
+    const uint32_t target = gridDim.x + ((inject & 2u) != 0u ? 1u : 0u);
+    if (threadIdx.x == 0 && !wait_word_reaches(&g_decode_sync[gen & 1u], target, wait_ns))
+        atomicOr(&g_topk_error, 2u);
     __syncthreads();
-    topk_row<true>(scores, g_decode_gmax, active, k, ids, blockIdx.x);
+    // Short rows take the register-resident path.
+    if (active <= 4 * ROW_THREADS)
+        topk_reg_row<4, true>(scores, active, k, ids, blockIdx.x);
+    else if (active <= 8 * ROW_THREADS)
+        topk_reg_row<8, true>(scores, active, k, ids, blockIdx.x);
+    else if (active <= REG_MAX_ACTIVE)
+        topk_reg_row<16, true>(scores, active, k, ids, blockIdx.x);
+    else
+        topk_row<true>(scores, g_decode_gmax, active, k, ids, blockIdx.x);
 }
 
 __global__ void topk_all_kernel(int active, int k, size_t total, int32_t *__restrict__ ids) {
@@ -860,6 +982,11 @@ cudaError_t launch_topk(const float *scores, const uint32_t *gmax, int nq, int a
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (active <= REG_MAX_ACTIVE) {
+        if (active <= 4 * ROW_THREADS) return cudaLaunchKernelEx(&cfg, topk_reg_kernel<4>, scores, active, k, ids);
+        if (active <= 8 * ROW_THREADS) return cudaLaunchKernelEx(&cfg, topk_reg_kernel<8>, scores, active, k, ids);
+        return cudaLaunchKernelEx(&cfg, topk_reg_kernel<16>, scores, active, k, ids);
+    }
     return cudaLaunchKernelEx(&cfg, topk_row_kernel, scores, gmax, active, k, ids);
 }
 
@@ -899,7 +1026,7 @@ cudaError_t launch_decode_nq(const float *q, const float *kblk, const int8_t *kq
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kernel, q, kblk, kq8, reinterpret_cast<const __half *>(kscale), nq, active, k,
-                              scores, ids);
+                              scores, ids, wait_limit_ns(), debug_inject());
 }
 
 cudaError_t launch_select_decode(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,

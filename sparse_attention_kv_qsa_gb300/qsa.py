@@ -26,7 +26,7 @@ QSA_OK, QSA_ERR_INVALID, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
 EXPORTED = ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
             "qsa_block_scores_gmax", "qsa_block_scores_q8_gmax", "qsa_block_group_max", "qsa_block_topk_gmax",
             "qsa_block_select_static", "qsa_block_select_small", "qsa_sparse_attn", "qsa_block_summary",
-            "qsa_get_device_error", "qsa_status_string")
+            "qsa_get_device_error", "qsa_debug_inject", "qsa_status_string")
 
 
 class QSAError(RuntimeError):
@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.qsa_sparse_attn.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, vp, vp]
         L.qsa_block_summary.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp]
         L.qsa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+        L.qsa_debug_inject.argtypes = [ctypes.c_uint32, ctypes.c_uint64]
+        L.qsa_debug_inject.restype = i
         L.qsa_status_string.argtypes = [i]
         L.qsa_status_string.restype = ctypes.c_char_p
         for f in ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
@@ -393,6 +395,19 @@ def device_error(device: torch.device | None = None) -> int:
     stream = torch.cuda.current_stream(device).cuda_stream
     _check(lib().qsa_get_device_error(ctypes.byref(code), stream), "qsa_get_device_error")
     return int(code.value)
+
+
+WAIT_LIMIT_DEFAULT_NS = 2_000_000_000
+INJECT_SCORER_STALL = 1    # the tensor-core scorer's CTA 0 never loads its first key piece
+INJECT_DECODE_BARRIER = 2  # the fused decode select's grid barrier waits for one arrival too many
+
+
+def debug_inject(faults: int, wait_limit_ns: int = WAIT_LIMIT_DEFAULT_NS) -> None:
+    """``qsa_debug_inject``: diagnostics for the bounded waits. Kernels
+    launched afterwards give up every spin-wait after ``wait_limit_ns`` and
+    carry the planted faults (bits above); ``debug_inject(0)`` restores normal
+    operation."""
+    _check(lib().qsa_debug_inject(int(faults), int(wait_limit_ns)), "qsa_debug_inject")
 
 
 def default_scorer_kernel() -> tuple[str, str]:

@@ -44,6 +44,14 @@ def test_every_declared_symbol_is_exported(lib):
         getattr(lib, "qsa_oracle_scores")
 
 
+def test_debug_inject_arguments(lib):
+    f = lib.qsa_debug_inject
+    assert f(4, 10 ** 6) == INVALID                 # unknown fault bit
+    assert f(0, 0) == INVALID                       # zero limit
+    assert f(0, 61 * 10 ** 9) == INVALID            # above 60 s
+    assert f(0, qsa.WAIT_LIMIT_DEFAULT_NS) == OK    # normal operation (nothing launched)
+
+
 def test_status_strings(lib):
     for s in (OK, INVALID, UNSUPPORTED, qsa.QSA_ERR_CUDA):
         assert qsa.status_string(s).startswith("QSA_")

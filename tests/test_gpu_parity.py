@@ -83,7 +83,8 @@ def test_tiny_planted_ties(dev, o, scorer):
 
 @pytest.mark.parametrize("scorer", SCORERS)
 @pytest.mark.parametrize("nq,active,max_blocks", [
-    (8, 1024, 1024), (5, 1003, 1100), (1, 17, 17), (130, 4099, 4101), (256, 8192, 65538), (3, 65536, 65538)])
+    (8, 1024, 1024), (5, 1003, 1100), (1, 17, 17), (130, 4099, 4101), (256, 8192, 65538), (3, 65536, 65538),
+    (200, 5003, 5003), (255, 129, 130)])
 def test_integer_inputs_bit_exact(dev, o, scorer, nq, active, max_blocks):
     W = w.integer_valued(nq, active, max_blocks)
     S_gpu = gpu_scores(W, dev, scorer).cpu().numpy()
@@ -122,7 +123,7 @@ def test_decode_int8_keys(dev, o, scorer, nq, cells):
 
 
 @pytest.mark.parametrize("scorer", SCORERS)
-@pytest.mark.parametrize("nq,active,k", [(3, 4099, 100), (129, 777, 5), (2, 131, 130)])
+@pytest.mark.parametrize("nq,active,k", [(3, 4099, 100), (129, 777, 5), (2, 131, 130), (200, 20000, 300)])
 def test_int8_ragged(dev, o, scorer, nq, active, k):
     W = w.int8_case(nq, active, k, max_blocks=active + 3)
     check_select(o, W, gpu_scores(W, dev, scorer))
@@ -161,6 +162,30 @@ def test_topk_exact_on_given_scores(dev, o, nq, active, k):
     ids = qsa.block_topk(to_dev(S, dev), k).cpu().numpy()
     assert np.array_equal(ids, o.topk_f32(S, k))
     parity.check_ids_valid(ids, active, k)
+
+
+@pytest.mark.parametrize("active", [2, 511, 512, 513, 2048, 2049, 4096, 4097, 8191, 8192, 8193, 16384])
+@pytest.mark.parametrize("kind", ["ties", "signed", "smooth"])
+def test_topk_register_path_rows(dev, o, active, kind):
+    """Rows of at most 8,192 scores take the register-resident path: every
+    register width (4, 8, 16 scores per thread) and its boundaries (and the
+    first rows past it), with
+    tie-heavy rows, rows mixing +-0, +-inf and NaN, and smooth rows; k from 1
+    to active - 1, and the decode k = 128."""
+    nq = 3
+    if kind == "ties":
+        S = _tie_heavy(nq, active, seed=active + 5)
+    elif kind == "signed":
+        u = w.u32(active + 7, 3, nq * active).reshape(nq, active)
+        vals = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1.0, -1.0, 2.5], dtype=np.float32)
+        S = vals[u % 8]
+    else:
+        S = w.normal32(active + 9, 2, nq * active).reshape(nq, active)
+    S = np.ascontiguousarray(S)
+    for k in sorted({1, min(128, active - 1), active // 2, active - 1} - {0}):
+        ids = qsa.block_topk(to_dev(S, dev), k).cpu().numpy()
+        assert np.array_equal(ids, o.topk_f32(S, k)), (active, kind, k)
+        parity.check_ids_valid(ids, active, k)
 
 
 @pytest.mark.parametrize("m", [4095, 4096, 4097, 8000])
@@ -270,7 +295,7 @@ def test_topk_k_at_least_active(dev, o, active, k):
     assert np.array_equal(ids, o.topk_f32(S, k))
 
 
-@pytest.mark.parametrize("nq", [37, 3])
+@pytest.mark.parametrize("nq", [37, 3, 200])
 def test_outputs_stay_in_bounds(dev, o, nq):
     """Canary words after the scores and ids must survive; capacity rows
     (NaN) must not be read."""
@@ -285,6 +310,14 @@ def test_outputs_stay_in_bounds(dev, o, nq):
     qsa.block_topk(s, W.k, out=ids)
     assert torch.all(buf_s[n_s:] == 12345.0) and torch.all(buf_i[n_i:] == 777)
     check_select(o, W, s)
+
+
+@pytest.mark.parametrize("nq,active,k", [(160, 70001, 200), (256, 33, 8), (140, 38912, 1000)])
+def test_two_query_groups_ragged(dev, o, nq, active, k):
+    """Two query groups (the scorer's clusters then share each key tile's
+    conversion): a partial second group, ragged tile tails, few tiles."""
+    W = w.normal_case(nq=nq, active=active, k=k, max_blocks=active + 3)
+    check_select(o, W, gpu_scores(W, dev))
 
 
 def test_side_stream(dev, o):
