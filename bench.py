@@ -624,6 +624,31 @@ def main():
         other = {"path": "plain" if path == "gmax" else "gmax", "steps": n_o,
                  "step_us": 1e3 * statistics.mean(ostep), "step_p50_us": 1e3 * pct(ostep, 50),
                  "scores_us": 1e3 * statistics.mean(os_), "topk_us": 1e3 * statistics.mean(ot_)}
+    # The fused call (qsa_block_select: the same ids without storing the
+    # scores), same workload, flushes and step timing; its ids must equal the
+    # headline's.
+    select = None
+    peaks = load_peaks()
+    units_per_step = W.nq * W.active
+    if args.scorer == "default":
+        ids_f = torch.empty_like(ids)
+        scratch = torch.empty((qsa.select_scratch_bytes(W.nq),), dtype=torch.uint8, device=dev)
+        sel = lambda: qsa.block_select(q, kblk, W.active, W.k, ids_out=ids_f, scores_buf=scores, scratch=scratch)
+        for i in range(args.warmup):
+            sel()
+        n_f = min(max(K_, 200), 1000)
+        t_sel = timed_steps(sel, lambda: None, n_f)
+        torch.cuda.synchronize()
+        assert torch.equal(ids_f, ids_headline), "qsa_block_select disagrees with the two calls"
+        f_us = 1e3 * statistics.mean(t_sel)
+        f_alg = 1e6 * (W.nq * 128 * 4 * 4 + W.active * 128 * 4 + W.nq * W.k * 4) / (peaks["hbm_gbs"] * 1e9)
+        f_tc = 1e6 * 1024.0 * W.nq * W.active / (peaks["bf16_tflops"] * 1e12)
+        select = {"call": "qsa_block_select (five launches; scores not stored)", "steps": n_f,
+                  "step_us": f_us, "step_p50_us": 1e3 * pct(t_sel, 50), "value": units_per_step / (f_us * 1e-6),
+                  "roofline": {"hbm_floor_us": f_alg, "tensor_floor_us": f_tc, "floor_us": max(f_alg, f_tc),
+                               "frac": max(f_alg, f_tc) / f_us,
+                               "note": "q + keys + ids at the HBM copy peak; 1,024 FLOP per query-block (the 4-head "
+                                       "definition) at the bf16 tensor peak; the slower of the two"}}
     step_ms_local = statistics.mean(t_step)
     step_ms = max_over_ranks(step_ms_local, world, dev)
     if qsa.device_error(dev) != 0:
@@ -686,6 +711,7 @@ def main():
                                   "scoring runs on tensor cores)"},
         "gpu_launches": 2 * K_,
         "other_path": other,
+        "select": select,
         "clocks": clocks,
         "pages_context": {"r9700_score_plus_topk_ms": 2.8, "r9700_qblocks_per_s": 6.0e9,
                           "note": "AMD R9700 (gfx1201) numbers from the pages; context only"},

@@ -35,6 +35,7 @@
 #ifndef QSA_H
 #define QSA_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -258,6 +259,40 @@ qsa_status qsa_sparse_attn(const float *q, const int8_t *k_cells, const uint16_t
 qsa_status qsa_block_summary(const int8_t *k_cells, const uint16_t *k_scale_f16, int ncells, int block_begin,
                              int block_end, float *kblk, int8_t *kblk_q8, uint16_t *kblk_scale_f16,
                              cudaStream_t stream);
+
+/*
+ * qsa_block_select: the ids of qsa_block_topk(qsa_block_scores(...)) --
+ * exactly the same ids -- without writing the scores in the common case
+ * (fp32 keys; q, kblk, ids as qsa_block_scores / qsa_block_topk).
+ * Method: per query row, a threshold from a strided sample of 1,024 blocks
+ * (CUDA cores), chosen so that about 1.8 k scores reach it; the tensor-core
+ * scorer then appends every score at or above its row's threshold, with its
+ * block id, to the row's list (at most QSA_SELECT_LIST_CAP entries) instead
+ * of storing the scores; a row whose list holds at least k entries (and did
+ * not overflow) holds its whole top-k and is selected from the list exactly.
+ * The other rows' query groups (128 rows each) are scored into `scores` and
+ * their rows selected by qsa_block_topk's kernel. When nq <= 4, active_blocks
+ * <= QSA_SELECT_LIST_MIN_ACTIVE or k > QSA_SELECT_LIST_K_MAX, it runs the two
+ * plain calls (scores written). k >= active_blocks: ids as qsa_block_topk.
+ * scores: [nq][active_blocks] fp32, caller-owned; its contents afterwards are
+ * unspecified (written only where the fallback ran).
+ * scratch: device memory of at least qsa_block_select_scratch_bytes(nq)
+ * bytes, 16-byte aligned, caller-owned (thresholds, list counts, failure
+ * flags, lists; no contents need survive between calls). Five launches on
+ * `stream`; allocates nothing.
+ * Errors: as qsa_block_scores and qsa_block_topk, plus QSA_ERR_INVALID for a
+ * missing, misaligned or too small scratch.
+ * Passages: "#3108 optimize exact QSA block scoring and top-k selection on
+ * gfx12", Microbenchmark & Parity Evidence section 2 (selection inside the
+ * decode layer, where the scores are only an intermediate); "#337 gfx12 QSA
+ * select", What item 1 (scores, then top-k over the active blocks).
+ */
+#define QSA_SELECT_LIST_CAP 4096
+#define QSA_SELECT_LIST_MIN_ACTIVE 8192
+#define QSA_SELECT_LIST_K_MAX 1024
+size_t qsa_block_select_scratch_bytes(int nq);
+qsa_status qsa_block_select(const float *q, const float *kblk, int nq, int max_blocks, int active_blocks, int k,
+                            float *scores, int32_t *ids, void *scratch, size_t scratch_bytes, cudaStream_t stream);
 
 /*
  * Reads and clears the current device's error word: nonzero when a kernel

@@ -15,12 +15,14 @@ from .qsa import (  # noqa: F401
     block_scores_q8,
     block_scores_q8_gmax,
     block_select,
+    block_select_gmax,
     block_select_small,
     block_select_static,
     block_summary,
     block_topk,
     block_topk_gmax,
     groups,
+    select_scratch_bytes,
     debug_inject,
     default_scorer_kernel,
     device_error,

@@ -116,6 +116,34 @@ uint32_t *select_scratch() {
     return cache[dev];
 }
 
+// The fused select's scratch: per row a threshold, a list count, a failure
+// flag and a list of LIST_CAP (key, id) pairs; per query group a flag.
+struct SelectScratch {
+    float *thr;
+    uint32_t *cnt, *fail, *gfail;
+    uint2 *cand;
+    size_t bytes;
+};
+size_t round16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+SelectScratch select_layout(void *base, int nq) {
+    char *b = static_cast<char *>(base);
+    const size_t n = static_cast<size_t>(nq), ngroups = (n + 127) / 128;
+    SelectScratch s;
+    size_t off = 0;
+    s.thr = reinterpret_cast<float *>(b + off);
+    off = round16(off + 4 * n);
+    s.cnt = reinterpret_cast<uint32_t *>(b + off);
+    off = round16(off + 4 * n);
+    s.fail = reinterpret_cast<uint32_t *>(b + off);
+    off = round16(off + 4 * n);
+    s.gfail = reinterpret_cast<uint32_t *>(b + off);
+    off = round16(off + 4 * ngroups);
+    s.cand = reinterpret_cast<uint2 *>(b + off);
+    off += sizeof(uint2) * static_cast<size_t>(qsa::LIST_CAP) * n;
+    s.bytes = off;
+    return s;
+}
+
 }  // namespace
 
 extern "C" {
@@ -198,6 +226,51 @@ qsa_status qsa_block_select_static(const float *q, const float *kblk, int nq, in
         if (s != QSA_OK) return s;
     }
     return topk(scores, gm, true, nq, active_blocks, k, ids, stream);
+}
+
+static_assert(QSA_SELECT_LIST_CAP == qsa::LIST_CAP, "one list capacity");
+
+size_t qsa_block_select_scratch_bytes(int nq) { return nq > 0 ? select_layout(nullptr, nq).bytes : 0; }
+
+qsa_status qsa_block_select(const float *q, const float *kblk, int nq, int max_blocks, int active_blocks, int k,
+                            float *scores, int32_t *ids, void *scratch, size_t scratch_bytes, cudaStream_t stream) {
+    qsa_status s = check_score_args(q, nq, max_blocks, active_blocks, scores);
+    if (s != QSA_OK) return s;
+    if (k < 1) return QSA_ERR_INVALID;
+    if (nq == 0) return QSA_OK;
+    if (ids == nullptr || !aligned16(ids)) return QSA_ERR_INVALID;
+    if (active_blocks > 0 && (kblk == nullptr || !aligned16(kblk) || scores == nullptr)) return QSA_ERR_INVALID;
+    if (scratch == nullptr || !aligned16(scratch) || scratch_bytes < select_layout(nullptr, nq).bytes)
+        return QSA_ERR_INVALID;
+    if (active_blocks > QSA_TOPK_MAX_ACTIVE) return QSA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(nq) * k > (1LL << 40)) return QSA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(nq) * 8 > 0x7FFFFFFFLL) return QSA_ERR_UNSUPPORTED;
+    if (k >= active_blocks) return from_cuda(qsa::launch_topk_all(nq, active_blocks, k, ids, stream));
+    // The list path needs the tensor-core scorer (nq > 4), rows past the
+    // register-resident top-k's reach and k well inside a list's capacity;
+    // otherwise the two plain calls give the same ids.
+    if (nq <= qsa::SMALL_NQ_MAX || active_blocks <= QSA_SELECT_LIST_MIN_ACTIVE || k > QSA_SELECT_LIST_K_MAX) {
+        s = scores_f32(q, kblk, nq, max_blocks, active_blocks, scores, nullptr, false, stream);
+        if (s != QSA_OK) return s;
+        return topk(scores, nullptr, false, nq, active_blocks, k, ids, stream);
+    }
+    const SelectScratch x = select_layout(scratch, nq);
+    qsa::TcSelect list;
+    list.thr = x.thr;
+    list.cnt = x.cnt;
+    list.cand = x.cand;
+    qsa::TcSelect gated;
+    gated.gate = x.gfail;
+    cudaError_t e = qsa::launch_select_threshold(q, kblk, nq, active_blocks, k, x.thr, x.cnt, x.fail, x.gfail, stream);
+    if (e == cudaSuccess)
+        e = qsa::launch_scores_tc(q, kblk, nullptr, nullptr, nq, active_blocks, nullptr, nullptr, stream, list);
+    if (e == cudaSuccess) e = qsa::launch_select_list(x.cand, x.cnt, nq, active_blocks, k, ids, x.fail, x.gfail, stream);
+    // Rows whose list failed: their query groups' scores, then their top-k
+    // (both launches exit at once when no row failed).
+    if (e == cudaSuccess)
+        e = qsa::launch_scores_tc(q, kblk, nullptr, nullptr, nq, active_blocks, scores, nullptr, stream, gated);
+    if (e == cudaSuccess) e = qsa::launch_topk(scores, nullptr, nq, active_blocks, k, ids, stream, x.fail);
+    return from_cuda(e);
 }
 
 qsa_status qsa_block_select_small(const float *q, const float *kblk, const int8_t *kblk_q8,

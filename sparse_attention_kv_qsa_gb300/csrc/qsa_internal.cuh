@@ -29,11 +29,29 @@ cudaError_t launch_scores_ffma(const float *q, const float *kblk, const int8_t *
                                const uint16_t *kscale, int nq, int active, float *scores,
                                cudaStream_t stream);
 
+// The fused select's per-row candidate lists: LIST_CAP (key, block id) pairs.
+constexpr int LIST_CAP = 4096;
+
+// Extra modes of the tensor-core scorer for the fused select (fp32 keys):
+// list mode (thr set): no scores are stored; every score >= thr[row] is
+// appended to the row's list cand[row][0 .. LIST_CAP) as (key, id), counted
+// in cnt[row]; the scorer waits for the previous grid (which writes thr and
+// clears cnt) only before its first append. Gated mode (gate set): only the
+// CTAs of query groups g with gate[g] != 0 run (after waiting for the
+// previous grid), the others exit at once.
+struct TcSelect {
+    const float *thr = nullptr;
+    uint32_t *cnt = nullptr;
+    uint2 *cand = nullptr;
+    const uint32_t *gate = nullptr;
+};
+
 // Scores on the tensor cores (3-way bf16 split; int8 keys: one slice).
 // Exactly one of kblk / (kq8, kscale) is non-null. gmax (may be null):
 // [nq][ceil(active / GROUP_BLOCKS)] keys of each group's largest score.
 cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale,
-                             int nq, int active, float *scores, uint32_t *gmax, cudaStream_t stream);
+                             int nq, int active, float *scores, uint32_t *gmax, cudaStream_t stream,
+                             const TcSelect &sel = TcSelect());
 
 // gmax from packed scores (the decode scorer's companion).
 cudaError_t launch_group_max(const float *scores, int nq, int active, uint32_t *gmax, cudaStream_t stream);
@@ -48,7 +66,14 @@ cudaError_t launch_scores_rows(const float *q, const float *kblk, const int8_t *
 // group maxima of these scores, which let a row read only the groups that
 // can hold its top k.
 cudaError_t launch_topk(const float *scores, const uint32_t *gmax, int nq, int active, int k, int32_t *ids,
-                        cudaStream_t stream);
+                        cudaStream_t stream, const uint32_t *gate = nullptr);
+
+// Fused select (see topk.cu): the per-row thresholds (and the cleared list
+// counts and failure flags), and the exact selection from the lists.
+cudaError_t launch_select_threshold(const float *q, const float *kblk, int nq, int active, int k, float *thr,
+                                    uint32_t *cnt, uint32_t *fail, uint32_t *gfail, cudaStream_t stream);
+cudaError_t launch_select_list(const uint2 *cand, const uint32_t *cnt, int nq, int active, int k, int32_t *ids,
+                               uint32_t *fail, uint32_t *gfail, cudaStream_t stream);
 
 // Scores and top-k for nq <= 4 in one cooperative launch (k < active):
 // scores written, group maxima in a fixed device array; calls on one device

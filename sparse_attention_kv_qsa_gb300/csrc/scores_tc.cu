@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     scores_tc_kernel(const float *__restrict__ q, const __half *__restrict__ kscale, int nq, int active,
                      int ntiles, int ctas_per_group, float *__restrict__ scores, uint32_t *__restrict__ gmax,
                      const __grid_constant__ CUtensorMap key_map, const __grid_constant__ CUtensorMap out_map,
-                     int use_tma, int pair, uint64_t wait_ns, uint32_t inject) {
+                     int use_tma, int pair, uint64_t wait_ns, uint32_t inject, const TcSelect sel) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -184,6 +184,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int q0 = group * QGROUP;
     const int qn = min(QGROUP, nq - q0);
     const int nlocal = j0 < ntiles ? (ntiles - 1 - j0) / ctas_per_group + 1 : 0;
+    if (sel.gate != nullptr) {
+        // Gated (the fused select's fallback): only query groups with a
+        // flagged row; both CTAs of a pair belong to the same group.
+        grid_dependency_wait();
+        if (ld_in(sel.gate + group) == 0u) return;
+    }
+    const bool list_mode = !kInt8 && sel.thr != nullptr;
     constexpr uint32_t PIECE_BYTES = PIECE_ROWS * KHALF * (kInt8 ? 1 : 4);
     auto tile_b0 = [&](int li) { return (j0 + li * ctas_per_group) * TILE_N; };
 
@@ -221,8 +228,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // The pipeline's waits: bounded by wait_ns, abandoned once the CTA aborts.
     auto wait = [&](uint64_t *bar, uint32_t parity) { return wait_or_flag(bar, parity, abort, wait_ns); };
     // Inputs may come from the previous grid on the stream; the next grid (the
-    // top-k) may launch now and waits for this one's scores itself.
-    grid_dependency_wait();
+    // top-k) may launch now and waits for this one's scores itself. In list
+    // mode the previous grid (the thresholds) let this one start only after
+    // it had waited for its own predecessor, so q and the keys are final;
+    // the epilogue waits for the thresholds themselves.
+    if (!list_mode) grid_dependency_wait();
     grid_launch_dependents();
 
     const int npieces = 4 * nlocal;
@@ -412,6 +422,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int col0 = 64 * team;                         // first column of this thread's half
         const bool vec_ok = (active & 3) == 0;              // 16-byte aligned row segments
         const uint32_t stage0 = base + OUT_OFF + (warp - EPI_WARP0) * OUT_ROWS * OUT_ROW_BYTES;
+        float ft = 0.f;   // list mode: this row's threshold
+        if (list_mode) {
+            grid_dependency_wait();
+            if (row < qn) ft = ld_in(sel.thr + q0 + row);
+        }
         for (int li = 0; li < nlocal; ++li) {
             const int b0 = tile_b0(li);
             const int nb = min(TILE_N, active - b0);
@@ -452,6 +467,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int j = 0; j < TILE_N / 2; ++j)
                     if (col0 + j < nb)
                         v[j] = __fmul_rn(v[j], __half2float(__ushort_as_half(ld_in_u16(kscale + b0 + col0 + j))));
+            }
+            if (list_mode) {
+                // Append the scores at or above the threshold (x >= ft: NaN
+                // fails) to the row's list, as (key, block id); one atomic per
+                // thread and tile reserves the slots.
+                uint32_t h0 = 0u, h1 = 0u;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    h0 |= static_cast<uint32_t>(col0 + j < nb && v[j] >= ft) << j;
+                    h1 |= static_cast<uint32_t>(col0 + 32 + j < nb && v[32 + j] >= ft) << j;
+                }
+                const uint32_t c = __popc(h0) + __popc(h1);
+                if (c != 0u && row < qn) {
+                    uint32_t slot = atomicAdd(sel.cnt + q0 + row, c);
+                    uint2 *dst = sel.cand + static_cast<size_t>(q0 + row) * LIST_CAP;
+#pragma unroll
+                    for (int j = 0; j < TILE_N / 2; ++j) {
+                        if (((j < 32 ? h0 : h1) >> (j & 31)) & 1u) {
+                            if (slot < static_cast<uint32_t>(LIST_CAP))
+                                dst[slot] = make_uint2(score_key(v[j]), static_cast<uint32_t>(b0 + col0 + j));
+                            ++slot;
+                        }
+                    }
+                }
+                continue;
             }
             // Group maxima: this thread's 64 columns are two 32-block groups.
             // fmaxf skips NaN (an all-NaN group stays NaN, whose key is that of
@@ -687,7 +727,7 @@ bool encode_key_map(CUtensorMap *map, const void *keys, int active, bool int8) {
 }  // namespace
 
 cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq8, const uint16_t *kscale, int nq,
-                             int active, float *scores, uint32_t *gmax, cudaStream_t stream) {
+                             int active, float *scores, uint32_t *gmax, cudaStream_t stream, const TcSelect &sel) {
     static thread_local int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -728,7 +768,7 @@ cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq
     CUtensorMap out_map, key_map;
     memset(&out_map, 0, sizeof(out_map));
     memset(&key_map, 0, sizeof(key_map));
-    const int use_tma = encode_out_map(&out_map, scores, nq, active) ? 1 : 0;
+    const int use_tma = scores != nullptr && encode_out_map(&out_map, scores, nq, active) ? 1 : 0;
     const bool int8 = kq8 != nullptr;
     if (!encode_key_map(&key_map, int8 ? static_cast<const void *>(kq8) : static_cast<const void *>(kblk), active,
                         int8))
@@ -736,10 +776,10 @@ cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq
     if (int8)
         return cudaLaunchKernelEx(&cfg, scores_tc_kernel<true>, q, reinterpret_cast<const __half *>(kscale), nq,
                                   active, ntiles, per, scores, gmax, key_map, out_map, use_tma, pair,
-                                  wait_limit_ns(), debug_inject());
+                                  wait_limit_ns(), debug_inject(), TcSelect());
     return cudaLaunchKernelEx(&cfg, scores_tc_kernel<false>, q, static_cast<const __half *>(nullptr), nq, active,
                               ntiles, per, scores, gmax, key_map, out_map, use_tma, pair, wait_limit_ns(),
-                              debug_inject());
+                              debug_inject(), sel);
 }
 
 cudaError_t tc_error_read_clear(uint32_t *word, cudaStream_t stream) {

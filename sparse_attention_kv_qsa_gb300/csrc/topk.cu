@@ -790,6 +790,65 @@ __device__ __forceinline__ void topk_row(const float *__restrict__ scores, const
 // tie rule as topk_row). The selection and tie bitmaps are built by warp
 // ballots: with this layout one warp's 32 scores of step j are exactly one
 // bitmap word.
+// The digit search of a register-resident selection: key[j] for valid j
+// (bit j of `valid`) are this thread's keys; every thread of the CTA calls it.
+// Returns the final prefix and mask, the number kk still to take among keys
+// equal to the prefix, and whether the search ended on a bin taken whole
+// (done: every key matching the prefix is selected). histA and histR must be
+// clear, and a CTA barrier must separate their clearing from the call.
+struct DigitResult {
+    uint32_t prefix, mask, kk;
+    bool done;
+};
+template <int PER>
+__device__ __forceinline__ DigitResult reg_digit_search(const uint32_t (&key)[PER], uint32_t valid, int k,
+                                                        RowShared &sh, int tid, int lane, int warp) {
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+        if (valid >> j & 1u) atomicAdd(&sh.histA[key[j] >> 21], 1u);
+    __syncthreads();
+    if (tid < HIST_A / GROUP) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(&sh.histA[GROUP * tid]);
+        const uint4 b = *reinterpret_cast<const uint4 *>(&sh.histA[GROUP * tid + 4]);
+        sh.groupA[tid] = a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w;
+    }
+    __syncthreads();
+    DigitResult r;
+    r.kk = static_cast<uint32_t>(k);
+    if (warp == 0) warp_select_2048(r.kk, sh, lane);
+    __syncthreads();
+    r.kk -= sh.sel_above;
+    r.done = sh.sel_cnt == r.kk;
+    r.prefix = sh.sel_bin << 21;
+    r.mask = 0xFFE00000u;
+    int shift = 21;
+#pragma unroll 1
+    while (!r.done && shift > 0) {
+        const int width = min(8, shift);
+        shift -= width;
+        const uint32_t dmask = (1u << width) - 1u;
+#pragma unroll
+        for (int j = 0; j < PER; ++j)
+            if ((valid >> j & 1u) && (key[j] & r.mask) == r.prefix) atomicAdd(&sh.histR[(key[j] >> shift) & dmask], 1u);
+        __syncthreads();
+        if (warp == 0) warp_select_256(sh.histR, r.kk, sh, lane);   // also clears histR
+        __syncthreads();
+        r.kk -= sh.sel_above;
+        r.prefix |= sh.sel_bin << shift;
+        r.mask |= dmask << shift;
+        r.done = sh.sel_cnt == r.kk;
+    }
+    return r;
+}
+
+// Register-resident exact top-k of a short row (n <= PER * 512 scores,
+// k < n): every score is read once, into registers (thread t holds scores
+// t, t + 512, ...), and the digit search runs on those registers: the 11-bit
+// leading digit, then 8, 8 and 5 bits over the keys that match the prefix,
+// each a shared-memory histogram scanned from the top (the same digits and
+// tie rule as topk_row). The selection and tie bitmaps are built by warp
+// ballots: with this layout one warp's 32 scores of step j are exactly one
+// bitmap word.
 template <int PER, bool kCoherent>
 __device__ __forceinline__ void topk_reg_row(const float *__restrict__ scores, int n, int k,
                                              int32_t *__restrict__ ids, size_t row) {
@@ -817,50 +876,18 @@ __device__ __forceinline__ void topk_reg_row(const float *__restrict__ scores, i
             valid |= 1u << j;
         }
     }
-    __syncthreads();
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
-        key[j] = float_bits_to_key(key[j]);
-        if (valid >> j & 1u) atomicAdd(&sh.histA[key[j] >> 21], 1u);
-    }
+    for (int j = 0; j < PER; ++j) key[j] = float_bits_to_key(key[j]);
     __syncthreads();
-    if (tid < HIST_A / GROUP) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(&sh.histA[GROUP * tid]);
-        const uint4 b = *reinterpret_cast<const uint4 *>(&sh.histA[GROUP * tid + 4]);
-        sh.groupA[tid] = a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w;
-    }
-    __syncthreads();
-    uint32_t kk = static_cast<uint32_t>(k);
-    if (warp == 0) warp_select_2048(kk, sh, lane);
-    __syncthreads();
-    kk -= sh.sel_above;
-    bool done = sh.sel_cnt == kk;
-    uint32_t prefix = sh.sel_bin << 21, mask = 0xFFE00000u;
-    int shift = 21;
-#pragma unroll 1
-    while (!done && shift > 0) {
-        const int width = min(8, shift);
-        shift -= width;
-        const uint32_t dmask = (1u << width) - 1u;
-#pragma unroll
-        for (int j = 0; j < PER; ++j)
-            if ((valid >> j & 1u) && (key[j] & mask) == prefix) atomicAdd(&sh.histR[(key[j] >> shift) & dmask], 1u);
-        __syncthreads();
-        if (warp == 0) warp_select_256(sh.histR, kk, sh, lane);   // also clears histR
-        __syncthreads();
-        kk -= sh.sel_above;
-        prefix |= sh.sel_bin << shift;
-        mask |= dmask << shift;
-        done = sh.sel_cnt == kk;
-    }
+    const DigitResult r = reg_digit_search<PER>(key, valid, k, sh, tid, lane, warp);
     // Keys above the prefix are selected; keys equal to it are selected too
     // when the search ended on a bin taken whole, else they are ties.
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
-        const uint32_t km = key[j] & mask;
+        const uint32_t km = key[j] & r.mask;
         const bool ok = (valid >> j & 1u) != 0u;
-        const uint32_t sel = __ballot_sync(FULL_MASK, ok && (km > prefix || (done && km == prefix)));
-        const uint32_t tie = __ballot_sync(FULL_MASK, ok && !done && km == prefix);
+        const uint32_t sel = __ballot_sync(FULL_MASK, ok && (km > r.prefix || (r.done && km == r.prefix)));
+        const uint32_t tie = __ballot_sync(FULL_MASK, ok && !r.done && km == r.prefix);
         const int wd = j * ROW_WARPS + warp;
         if (lane == 0 && wd < nwords) {
             selbits[wd] = sel;
@@ -868,12 +895,16 @@ __device__ __forceinline__ void topk_reg_row(const float *__restrict__ scores, i
         }
     }
     __syncthreads();
-    finish_row(selbits, tiebits, nwords, !done, kk, k, ids + row * static_cast<size_t>(k), sh, tid, lane, warp);
+    finish_row(selbits, tiebits, nwords, !r.done, r.kk, k, ids + row * static_cast<size_t>(k), sh, tid, lane, warp);
 }
 
 __global__ void __launch_bounds__(ROW_THREADS, 2)
     topk_row_kernel(const float *__restrict__ scores, const uint32_t *__restrict__ gmax, int active, int k,
-                    int32_t *__restrict__ ids) {
+                    int32_t *__restrict__ ids, const uint32_t *__restrict__ gate) {
+    if (gate != nullptr) {   // the fused select's fallback: only rows whose list failed
+        grid_dependency_wait();
+        if (ld_in(gate + blockIdx.x) == 0u) return;
+    }
     topk_row<false>(scores, gmax, active, k, ids, blockIdx.x);
 }
 
@@ -885,7 +916,12 @@ constexpr int REG_MAX_ACTIVE = 16 * ROW_THREADS;   // 8,192
 
 template <int PER>
 __global__ void __launch_bounds__(ROW_THREADS, 2)
-    topk_reg_kernel(const float *__restrict__ scores, int active, int k, int32_t *__restrict__ ids) {
+    topk_reg_kernel(const float *__restrict__ scores, int active, int k, int32_t *__restrict__ ids,
+                    const uint32_t *__restrict__ gate) {
+    if (gate != nullptr) {
+        grid_dependency_wait();
+        if (ld_in(gate + blockIdx.x) == 0u) return;
+    }
     topk_reg_row<PER, false>(scores, active, k, ids, blockIdx.x);
 }
 
@@ -950,6 +986,154 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         topk_row<true>(scores, g_decode_gmax, active, k, ids, blockIdx.x);
 }
 
+// ---- fused select: scores and top-k without the scores ----------------------
+// Step 1 (select_threshold_kernel, one CTA per query row): a threshold that
+// about 1.8 k + 8 n / S of the row's n scores are expected to reach: the
+// r-th largest key, r = ceil(1.8 k S / n) + 8, of a strided sample of S =
+// LIST_SAMPLE blocks scored on CUDA cores (the same head-summed query and
+// fp32 FMA; its rounding only moves the threshold). Step 2 (the tensor-core
+// scorer in list mode) appends every score at or above its row's threshold,
+// as (key, block id), to the row's list instead of storing scores. Step 3
+// (select_list_kernel): when a row's list holds at least k entries and did
+// not overflow, it holds every score at or above the threshold and therefore
+// the whole top-k, ties included, and the exact digit search runs on it;
+// otherwise the row is flagged and its query group goes through the plain
+// scorer and top-k (steps 4 and 5). The result is exact either way.
+constexpr int LIST_SAMPLE = 1024;
+constexpr int LIST_PER = LIST_CAP / ROW_THREADS;   // list entries per thread in step 3
+static_assert(LIST_CAP % ROW_THREADS == 0 && LIST_PER <= 32, "list entries in registers");
+
+__global__ void __launch_bounds__(ROW_THREADS, 2)
+    select_threshold_kernel(const float *__restrict__ q, const float *__restrict__ kblk, int active, int k,
+                            float *__restrict__ thr, uint32_t *__restrict__ cnt, uint32_t *__restrict__ fail,
+                            uint32_t *__restrict__ gfail) {
+    __shared__ __align__(16) float qs[D];
+    __shared__ uint32_t keys[LIST_SAMPLE];
+    __shared__ __align__(16) uint32_t hist[BINS_R];
+    __shared__ uint32_t sel[3];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int row = blockIdx.x;
+    if (tid < BINS_R) hist[tid] = 0u;
+    // q and the keys may come from the previous grid; the scorer that follows
+    // may start once every CTA is past this wait (it reads q and the keys,
+    // not these thresholds, before waiting for this grid).
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (tid < D) {
+        const float *p = q + static_cast<size_t>(row) * (HEADS * D) + tid;
+        qs[tid] = __fadd_rn(__fadd_rn(__fadd_rn(ld_in(p), ld_in(p + D)), ld_in(p + 2 * D)), ld_in(p + 3 * D));
+    }
+    if (tid == 0) {
+        cnt[row] = 0u;
+        fail[row] = 0u;
+        if (row % 128 == 0) gfail[row / 128] = 0u;
+    }
+    __syncthreads();
+    // Sample block j: j * n / S (a warp per block: 16 bytes of the key row per lane).
+    const float4 qv = *reinterpret_cast<const float4 *>(qs + 4 * lane);
+#pragma unroll 4
+    for (int j = warp; j < LIST_SAMPLE; j += ROW_WARPS) {
+        const long long b = static_cast<long long>(j) * active / LIST_SAMPLE;
+        const float4 kv = ld_in(reinterpret_cast<const float4 *>(kblk + b * D) + lane);
+        float acc = fmaf(qv.w, kv.w, fmaf(qv.z, kv.z, fmaf(qv.y, kv.y, qv.x * kv.x)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, o);
+        if (lane == 0) keys[j] = score_key(acc);
+    }
+    __syncthreads();
+    // The r-th largest sample key, 8 bits at a time (two keys per thread).
+    static_assert(LIST_SAMPLE == 2 * ROW_THREADS, "two sample keys per thread");
+    const uint32_t k0 = keys[tid], k1 = keys[tid + ROW_THREADS];
+    uint32_t r = static_cast<uint32_t>((9ull * static_cast<uint64_t>(k) * LIST_SAMPLE + 5ull * active - 1) /
+                                       (5ull * active)) + 8u;
+    if (r > LIST_SAMPLE) r = LIST_SAMPLE;
+    uint32_t prefix = 0u, mask = 0u;
+#pragma unroll 1
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        if ((k0 & mask) == prefix) atomicAdd(&hist[(k0 >> shift) & 255u], 1u);
+        if ((k1 & mask) == prefix) atomicAdd(&hist[(k1 >> shift) & 255u], 1u);
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t bin, above, c;
+            warp_find_256(hist, r, true, lane, bin, above, c);
+            if (lane == 0) {
+                sel[0] = bin;
+                sel[1] = above;
+                sel[2] = c;
+            }
+        }
+        __syncthreads();
+        r -= sel[1];
+        prefix |= sel[0] << shift;
+        mask |= 255u << shift;
+        const bool whole = sel[2] == r;   // every key of the bin is among the r largest
+        __syncthreads();                   // sel read by all before the next digit rewrites it
+        if (whole) break;                  // (uniform) prefix is a key at least r sample keys reach
+    }
+    if (tid == 0) {
+        // x >= ft exactly when key(x) >= prefix (NaN, key of -inf, fails it).
+        thr[row] = __uint_as_float(prefix >= 0x80000000u ? (prefix ^ 0x80000000u) : ~prefix);
+    }
+}
+
+// Step 3: one CTA per row; the row's list (at most LIST_CAP (key, id) pairs,
+// LIST_PER per thread) is read into registers and selected exactly, the ids
+// marked in bitmaps over [0, active) and written ascending. A row whose list
+// is short or overflowed is flagged (and its query group), and left to the
+// fallback steps.
+__global__ void __launch_bounds__(ROW_THREADS, 2)
+    select_list_kernel(const uint2 *__restrict__ cand, const uint32_t *__restrict__ cnt, int active, int k,
+                       int32_t *__restrict__ ids, uint32_t *__restrict__ fail, uint32_t *__restrict__ gfail) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int row = blockIdx.x;
+    const int nwords = (active + 31) >> 5;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    RowShared &sh = *reinterpret_cast<RowShared *>(smem_raw);
+    uint32_t *selbits = reinterpret_cast<uint32_t *>(smem_raw + SHARED_BYTES);
+    uint32_t *tiebits = selbits + nwords;
+    reinterpret_cast<uint4 *>(sh.histA)[tid] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < BINS_R) sh.histR[tid] = 0u;
+    for (int i = tid; i < 2 * nwords; i += ROW_THREADS) selbits[i] = 0u;   // both bitmaps
+    grid_dependency_wait();   // the lists of the scorer before this grid
+    const uint32_t n = ld_in(cnt + row);
+    if (n < static_cast<uint32_t>(k) || n > static_cast<uint32_t>(LIST_CAP)) {   // uniform: the whole CTA
+        if (tid == 0) {
+            fail[row] = 1u;
+            atomicOr(&gfail[row / 128], 1u);
+        }
+        return;
+    }
+    const uint2 *c = cand + static_cast<size_t>(row) * LIST_CAP;
+    uint32_t key[LIST_PER], id[LIST_PER];
+    uint32_t valid = 0u;
+#pragma unroll
+    for (int j = 0; j < LIST_PER; ++j) {
+        const uint32_t e = static_cast<uint32_t>(j * ROW_THREADS + tid);
+        key[j] = 0u;
+        id[j] = 0u;
+        if (e < n) {
+            const uint2 v = __ldcg(c + e);
+            key[j] = v.x;
+            id[j] = v.y;
+            valid |= 1u << j;
+        }
+    }
+    __syncthreads();
+    const DigitResult r = reg_digit_search<LIST_PER>(key, valid, k, sh, tid, lane, warp);
+#pragma unroll
+    for (int j = 0; j < LIST_PER; ++j) {
+        if (!(valid >> j & 1u)) continue;
+        const uint32_t km = key[j] & r.mask;
+        const uint32_t b = id[j];
+        if (km > r.prefix || (r.done && km == r.prefix))
+            atomicOr(&selbits[b >> 5], 1u << (b & 31u));
+        else if (km == r.prefix)
+            atomicOr(&tiebits[b >> 5], 1u << (b & 31u));
+    }
+    __syncthreads();
+    finish_row(selbits, tiebits, nwords, !r.done, r.kk, k, ids + static_cast<size_t>(row) * k, sh, tid, lane, warp);
+}
+
 __global__ void topk_all_kernel(int active, int k, size_t total, int32_t *__restrict__ ids) {
     for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < total;
          t += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -961,7 +1145,7 @@ __global__ void topk_all_kernel(int active, int k, size_t total, int32_t *__rest
 }  // namespace
 
 cudaError_t launch_topk(const float *scores, const uint32_t *gmax, int nq, int active, int k, int32_t *ids,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const uint32_t *gate) {
     if (active > MAX_ACTIVE) return cudaErrorInvalidValue;
     static thread_local int configured_device = -1;
     int dev = 0;
@@ -983,11 +1167,13 @@ cudaError_t launch_topk(const float *scores, const uint32_t *gmax, int nq, int a
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (active <= REG_MAX_ACTIVE) {
-        if (active <= 4 * ROW_THREADS) return cudaLaunchKernelEx(&cfg, topk_reg_kernel<4>, scores, active, k, ids);
-        if (active <= 8 * ROW_THREADS) return cudaLaunchKernelEx(&cfg, topk_reg_kernel<8>, scores, active, k, ids);
-        return cudaLaunchKernelEx(&cfg, topk_reg_kernel<16>, scores, active, k, ids);
+        if (active <= 4 * ROW_THREADS)
+            return cudaLaunchKernelEx(&cfg, topk_reg_kernel<4>, scores, active, k, ids, gate);
+        if (active <= 8 * ROW_THREADS)
+            return cudaLaunchKernelEx(&cfg, topk_reg_kernel<8>, scores, active, k, ids, gate);
+        return cudaLaunchKernelEx(&cfg, topk_reg_kernel<16>, scores, active, k, ids, gate);
     }
-    return cudaLaunchKernelEx(&cfg, topk_row_kernel, scores, gmax, active, k, ids);
+    return cudaLaunchKernelEx(&cfg, topk_row_kernel, scores, gmax, active, k, ids, gate);
 }
 
 template <int NQ, bool kInt8>
@@ -1044,6 +1230,45 @@ cudaError_t launch_select_decode(const float *q, const float *kblk, const int8_t
             return i8 ? launch_decode_nq<4, true>(q, kblk, kq8, kscale, nq, active, k, scores, ids, stream)
                       : launch_decode_nq<4, false>(q, kblk, kq8, kscale, nq, active, k, scores, ids, stream);
     }
+}
+
+cudaError_t launch_select_threshold(const float *q, const float *kblk, int nq, int active, int k, float *thr,
+                                    uint32_t *cnt, uint32_t *fail, uint32_t *gfail, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nq));
+    cfg.blockDim = dim3(ROW_THREADS);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, select_threshold_kernel, q, kblk, active, k, thr, cnt, fail, gfail);
+}
+
+cudaError_t launch_select_list(const uint2 *cand, const uint32_t *cnt, int nq, int active, int k, int32_t *ids,
+                               uint32_t *fail, uint32_t *gfail, cudaStream_t stream) {
+    if (active > MAX_ACTIVE) return cudaErrorInvalidValue;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(select_list_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(row_smem_bytes(MAX_ACTIVE)));
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nq));
+    cfg.blockDim = dim3(ROW_THREADS);
+    cfg.dynamicSmemBytes = row_smem_bytes(active);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, select_list_kernel, cand, cnt, active, k, ids, fail, gfail);
 }
 
 cudaError_t launch_topk_all(int nq, int active, int k, int32_t *ids, cudaStream_t stream) {

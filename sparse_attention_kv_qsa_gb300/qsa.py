@@ -26,7 +26,8 @@ QSA_OK, QSA_ERR_INVALID, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
 EXPORTED = ("qsa_block_scores", "qsa_block_scores_q8", "qsa_block_scores_ffma", "qsa_block_topk",
             "qsa_block_scores_gmax", "qsa_block_scores_q8_gmax", "qsa_block_group_max", "qsa_block_topk_gmax",
             "qsa_block_select_static", "qsa_block_select_small", "qsa_sparse_attn", "qsa_block_summary",
-            "qsa_get_device_error", "qsa_debug_inject", "qsa_status_string")
+            "qsa_get_device_error", "qsa_debug_inject", "qsa_status_string", "qsa_block_select",
+            "qsa_block_select_scratch_bytes")
 
 
 class QSAError(RuntimeError):
@@ -65,6 +66,10 @@ def lib() -> ctypes.CDLL:
         L.qsa_sparse_attn.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, vp, vp]
         L.qsa_block_summary.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp]
         L.qsa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+        L.qsa_block_select.argtypes = [vp, vp, i, i, i, i, vp, vp, vp, ctypes.c_size_t, vp]
+        L.qsa_block_select.restype = i
+        L.qsa_block_select_scratch_bytes.argtypes = [i]
+        L.qsa_block_select_scratch_bytes.restype = ctypes.c_size_t
         L.qsa_debug_inject.argtypes = [ctypes.c_uint32, ctypes.c_uint64]
         L.qsa_debug_inject.restype = i
         L.qsa_status_string.argtypes = [i]
@@ -271,13 +276,48 @@ def block_topk_gmax(scores: torch.Tensor, gmax: torch.Tensor, k: int,
     return out
 
 
-def block_select(q: torch.Tensor, kblk: torch.Tensor, active_blocks: int, k: int,
-                 scores_out: torch.Tensor | None = None, ids_out: torch.Tensor | None = None,
-                 gmax_out: torch.Tensor | None = None):
+def block_select_gmax(q: torch.Tensor, kblk: torch.Tensor, active_blocks: int, k: int,
+                      scores_out: torch.Tensor | None = None, ids_out: torch.Tensor | None = None,
+                      gmax_out: torch.Tensor | None = None):
     """Scores (with group maxima) then top-k, both on the current stream:
     ``(scores, ids)``; the ids equal ``block_topk(block_scores(...), k)``."""
     s, gm = block_scores_gmax(q, kblk, active_blocks, scores_out, gmax_out)
     return s, block_topk_gmax(s, gm, k, ids_out)
+
+
+def select_scratch_bytes(nq: int) -> int:
+    """``qsa_block_select_scratch_bytes``: scratch bytes qsa_block_select needs."""
+    return int(lib().qsa_block_select_scratch_bytes(int(nq)))
+
+
+def block_select(q: torch.Tensor, kblk: torch.Tensor, active_blocks: int, k: int,
+                 ids_out: torch.Tensor | None = None, scores_buf: torch.Tensor | None = None,
+                 scratch: torch.Tensor | None = None) -> torch.Tensor:
+    """``qsa_block_select``: the ids of ``block_topk(block_scores(...), k)``
+    without writing the scores (fp32 keys). ``scores_buf`` ``[nq, active]``
+    fp32 is the fallback's buffer (contents unspecified afterwards) and
+    ``scratch`` a uint8 tensor of at least ``select_scratch_bytes(nq)``
+    bytes; both are allocated when not given."""
+    _check_q(q)
+    _need(kblk, "kblk", torch.float32, 2)
+    if kblk.shape[1] != D:
+        raise ValueError("kblk must be [max_blocks, 128]")
+    nq = q.shape[0]
+    scores_buf = _scores_out(q, active_blocks, scores_buf)
+    if ids_out is None:
+        ids_out = torch.empty((nq, k), dtype=torch.int32, device=q.device)
+    else:
+        _need(ids_out, "ids_out", torch.int32, 2)
+        if tuple(ids_out.shape) != (nq, k):
+            raise ValueError(f"ids_out must have shape {(nq, k)}")
+    need = select_scratch_bytes(nq)
+    if scratch is None:
+        scratch = torch.empty((max(need, 16),), dtype=torch.uint8, device=q.device)
+    elif scratch.dtype != torch.uint8 or not scratch.is_cuda or not scratch.is_contiguous():
+        raise ValueError("scratch must be a contiguous uint8 CUDA tensor")
+    _check(lib().qsa_block_select(_ptr(q), _ptr(kblk), nq, kblk.shape[0], active_blocks, k, _ptr(scores_buf),
+                                  _ptr(ids_out), _ptr(scratch), scratch.numel(), _stream(q)), "qsa_block_select")
+    return ids_out
 
 
 def block_select_static(q: torch.Tensor, kblk: torch.Tensor, active_blocks: int, k: int,

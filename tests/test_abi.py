@@ -52,6 +52,22 @@ def test_debug_inject_arguments(lib):
     assert f(0, qsa.WAIT_LIMIT_DEFAULT_NS) == OK    # normal operation (nothing launched)
 
 
+def test_select_scratch_and_argument_errors(lib):
+    f = lib.qsa_block_select
+    n = qsa.select_scratch_bytes(256)
+    assert n >= 256 * 4096 * 8 and qsa.select_scratch_bytes(0) == 0
+    assert qsa.select_scratch_bytes(257) > n
+    assert f(A, B, 8, 100, 50, 0, A, B, A, n, None) == INVALID            # k < 1
+    assert f(A, B, 8, 100, 50, 5, A, None, A, n, None) == INVALID         # null ids
+    assert f(A, B, 8, 100, 50, 5, A, B, None, n, None) == INVALID         # null scratch
+    assert f(A, B, 8, 100, 50, 5, A, B, MIS, n, None) == INVALID          # misaligned scratch
+    assert f(A, B, 8, 100, 50, 5, A, B, A, qsa.select_scratch_bytes(8) - 1, None) == INVALID   # too small
+    assert f(A, B, 8, 100, 50, 5, None, B, A, n, None) == INVALID         # null scores
+    assert f(A, B, 8, 100, 101, 5, A, B, A, n, None) == INVALID           # active > max_blocks
+    assert f(A, B, 1, 10 ** 7, 393217, 5, A, B, A, n, None) == UNSUPPORTED
+    assert f(None, None, 0, 100, 50, 5, None, None, None, 0, None) == OK  # no rows
+
+
 def test_status_strings(lib):
     for s in (OK, INVALID, UNSUPPORTED, qsa.QSA_ERR_CUDA):
         assert qsa.status_string(s).startswith("QSA_")

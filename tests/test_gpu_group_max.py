@@ -126,7 +126,7 @@ def test_select_full_headline_equals_plain_path(dev, o):
     block_topk, and the ids of 8 sampled rows equal the oracle's."""
     W = w.full(512)
     q, kb = to_dev(W.q, dev), to_dev(W.kblk, dev)
-    s, ids = qsa.block_select(q, kb, W.active, 512)
+    s, ids = qsa.block_select_gmax(q, kb, W.active, 512)
     s0 = qsa.block_scores(q, kb, W.active)
     ids0 = qsa.block_topk(s0, 512)
     torch.cuda.synchronize()

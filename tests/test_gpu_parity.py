@@ -326,7 +326,7 @@ def test_side_stream(dev, o):
     q, kb = to_dev(W.q, dev), to_dev(W.kblk, dev)
     torch.cuda.synchronize()
     with torch.cuda.stream(st):
-        s, ids = qsa.block_select(q, kb, W.active, W.k)
+        s, ids = qsa.block_select_gmax(q, kb, W.active, W.k)
     st.synchronize()
     check_select(o, W, s)
 

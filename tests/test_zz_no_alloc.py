@@ -56,7 +56,7 @@ def test_static_select_matches_two_calls_and_oracle(nq, active, k):
     q = torch.from_numpy(W.q).to(dev)
     kb = torch.from_numpy(np.ascontiguousarray(W.kblk)).to(dev)
     s, ids = qsa.block_select_static(q, kb, active, k)
-    s2, ids2 = qsa.block_select(q, kb, active, k)
+    s2, ids2 = qsa.block_select_gmax(q, kb, active, k)
     torch.cuda.synchronize()
     assert torch.equal(s, s2)
     assert torch.equal(ids, ids2)
