@@ -14,6 +14,9 @@
 // attention and MMVQ row reuse on gfx12", item D5 (decode attention in
 // chunks of cells whose partial results merge in sequential order).
 //
+// This file is the CUDA-core path, taken when there are fewer queries than
+// SMs; csrc/attn_tc.cu holds the tensor-core path for more.
+//
 // GB300 mapping. One CTA of 16 warps per query, or a cluster of up to 4 CTAs
 // per query when there are few queries (decode), so that the cells of one
 // query stream through several SMs. A warp step covers two listed blocks
@@ -287,8 +290,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 cudaError_t launch_sparse_attn(const float *q, const int8_t *kc, const uint16_t *ks, const int8_t *vc,
                                const uint16_t *vs, int ncells, const int32_t *ids, int nq, int k, float *out,
                                cudaStream_t stream) {
-    // Few queries: a cluster per query spreads its cells over several SMs.
+    // As many queries as SMs or more: the tensor-core kernel (csrc/attn_tc.cu),
+    // measured faster there; fewer: this one, whose cells per step are
+    // fewer instructions away from the softmax (lower latency per step).
     const int sms = device_sm_count();
+    if (nq >= sms) return launch_sparse_attn_tc(q, kc, ks, vc, vs, ncells, ids, nq, k, out, stream);
+    // Few queries: a cluster per query spreads its cells over several SMs.
     int csize = 1;
     for (int c = MAX_CLUSTER; c > 1; c >>= 1) {
         if (static_cast<long long>(nq) * c <= sms) {

@@ -87,10 +87,15 @@ cudaError_t launch_block_summary(const int8_t *kc, const uint16_t *ks, int ncell
                                  int8_t *kq8, uint16_t *kscale, cudaStream_t stream);
 
 // Attention of each query's 4 heads over the int8 KV cells of its listed
-// blocks (csrc/attn.cu).
+// blocks (csrc/attn.cu: CUDA cores for nq below the SM count, else the
+// tensor-core kernel of csrc/attn_tc.cu, which launch_sparse_attn_tc runs
+// for any nq >= 1).
 cudaError_t launch_sparse_attn(const float *q, const int8_t *kc, const uint16_t *ks, const int8_t *vc,
                                const uint16_t *vs, int ncells, const int32_t *ids, int nq, int k, float *out,
                                cudaStream_t stream);
+cudaError_t launch_sparse_attn_tc(const float *q, const int8_t *kc, const uint16_t *ks, const int8_t *vc,
+                                  const uint16_t *vs, int ncells, const int32_t *ids, int nq, int k, float *out,
+                                  cudaStream_t stream);
 
 // ids[i][j] = j < active ? j : -1 (the k >= active case).
 cudaError_t launch_topk_all(int nq, int active, int k, int32_t *ids, cudaStream_t stream);

@@ -11,8 +11,15 @@ expf within 2 ulp) adds at most ~256 u of the largest value. So
 
     |out - out64| <= max_c |v[c]| * (32 u max_c S_c + 256 u)
 
-per (query, head), with the maxima over the query's attended cells. CPU tests
-check the argument errors (nothing is launched for them)."""
+per (query, head), with the maxima over the query's attended cells.
+
+Queries at least as many as the SMs take the tensor-core kernel: q (scaled
+per head by a power of two) and the weights p * vs (likewise) enter the
+MMAs as binary16 high parts plus remainders times 2^11, about 2^-22
+relative each, and the MMAs accumulate in fp32; the logits and the weighted
+sums then stay within the same bound. Its cases use nq >= 152 (the GB300's
+SM count; the test asserts the device has no more). CPU tests check the
+argument errors (nothing is launched for them)."""
 import numpy as np
 import pytest
 
@@ -97,11 +104,19 @@ def _check(W, out):
                                              (2, 17, 5, 0),             # every block, ragged
                                              (5, 4096, 1, 0),           # one block
                                              (2, 262144, 4096, 0),      # long lists: 16,384 cells per query
-                                             (7, 65536, 300, 290)])     # mostly padding
+                                             (7, 65536, 300, 290),      # mostly padding
+                                             # tensor-core kernel (nq >= SMs):
+                                             (256, 262144, 512, 0),     # the bench's many-query shape
+                                             (152, 4099 * 4 + 3, 60, 7),
+                                             (160, 17, 5, 0),
+                                             (152, 4096, 1, 0),
+                                             (153, 65536, 300, 290),
+                                             (152, 262144, 4096, 0)])   # 16,384 cells per query
 def test_sparse_attn_matches_oracle(nq, ncells, k, pad):
     import torch
     from sparse_attention_kv_qsa_gb300 import workloads as w
     dev = torch.device("cuda:0")
+    assert torch.cuda.get_device_properties(dev).multi_processor_count <= 152
     W = w.attn_case(nq, ncells, k, pad=pad)
     out = _run(W, dev)
     torch.cuda.synchronize()
@@ -113,13 +128,14 @@ def test_sparse_attn_matches_oracle(nq, ncells, k, pad):
 
 
 @pytest.mark.gpu
-def test_sparse_attn_padding_duplicates_and_empty():
+@pytest.mark.parametrize("nq", [4, 160])        # CUDA-core / tensor-core kernel
+def test_sparse_attn_padding_duplicates_and_empty(nq):
     """All-padding rows give zeros; ids past the last block are skipped; a
     block listed twice counts twice; no cells at all gives zeros."""
     import torch
     from sparse_attention_kv_qsa_gb300 import workloads as w
     dev = torch.device("cuda:0")
-    W = w.attn_case(4, 1000, 6)
+    W = w.attn_case(nq, 1000, 6)
     W.ids[0] = -1
     W.ids[1] = [5, 5, 5, 7, 9999, -3]
     W.ids[2] = [249, 249, 0, 1, 2, 3]        # block 249 = cells 996..999
@@ -127,12 +143,41 @@ def test_sparse_attn_padding_duplicates_and_empty():
     torch.cuda.synchronize()
     _check(W, out)
     assert torch.count_nonzero(out[0]) == 0
-    empty = w.attn_case(2, 8, 2)
+    empty = w.attn_case(nq, 8, 2)
     empty.kc, empty.vc = empty.kc[:0], empty.vc[:0]
     empty.ks, empty.vs = empty.ks[:0], empty.vs[:0]
     z = _run(empty, dev)
     torch.cuda.synchronize()
     assert torch.count_nonzero(z) == 0
+
+
+def _rescale_half(bits, mul):
+    return (bits.view(np.float16).astype(np.float64) * mul).astype(np.float16).view(np.uint16)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("nq", [8, 160])        # CUDA-core / tensor-core kernel
+@pytest.mark.parametrize("qmul,vsmul,ksmul", [(1e5, 1.0, 1.0),     # near one-hot softmax
+                                              (1e-20, 1.0, 1.0),   # uniform softmax, tiny q
+                                              (1.0, 6.0e5, 1.0),   # value scales up to 6e4
+                                              (1.0, 1e-4, 1.0),    # binary16-subnormal value scales
+                                              (1.0, 1.0, 1e-4)])   # binary16-subnormal key scales
+def test_sparse_attn_input_ranges(nq, qmul, vsmul, ksmul):
+    """Inputs far from the recipe's ranges: the tensor-core kernel's power-of-two
+    scalings keep its binary16 operands finite and normal, so both kernels
+    stay within the derived bound."""
+    import torch
+    from sparse_attention_kv_qsa_gb300 import workloads as w
+    dev = torch.device("cuda:0")
+    W = w.attn_case(nq, 4099 * 4 + 1, 40, pad=3)
+    W.q = (W.q.astype(np.float64) * qmul).astype(np.float32)
+    W.vs = _rescale_half(W.vs, vsmul)
+    W.ks = _rescale_half(W.ks, ksmul)
+    assert np.all(np.isfinite(W.vs.view(np.float16))) and np.all(W.vs.view(np.float16) != 0)
+    out = _run(W, dev)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    _check(W, out)
 
 
 @pytest.mark.gpu
