@@ -324,11 +324,12 @@ def run_reference(args, world, rank):
 
 def attention_side_measurement(dev, stream, sm_mhz: float):
     """qsa_sparse_attn over the selected blocks' int8 KV cells (262,144 cells,
-    binary16 scales): decode shapes (nq = 1 and 4, k = 128) per call of a CUDA
-    graph of 20 calls, and a prompt-like shape (256 queries, k = 512, L2
-    flushed before each call) with its HBM and FP32 fractions. The FP32 peak
-    is the device's SM count x 128 lanes x 2 FLOP x `sm_mhz` (the SM clock
-    sampled during the timed steps)."""
+    binary16 scales): decode shapes (nq = 1 and 4, k = 128: the CUDA-core
+    kernel) per call of a CUDA graph of 20 calls, and a prompt-like shape
+    (256 queries, k = 512, L2 flushed before each call: the tensor-core
+    kernel) with its HBM fraction and its rate in FP32-equivalent FLOPs
+    against the CUDA cores' FP32 peak (the device's SM count x 128 lanes x 2
+    FLOP x `sm_mhz`, the SM clock sampled during the timed steps)."""
     import torch
     import sparse_attention_kv_qsa_gb300 as qsa
     from sparse_attention_kv_qsa_gb300 import workloads as w
@@ -363,7 +364,7 @@ def attention_side_measurement(dev, stream, sm_mhz: float):
             g.replay()
             e1.record(stream)
             torch.cuda.synchronize()
-            out[name] = {"graph_call_us": 1e3 * e0.elapsed_time(e1) / 20}
+            out[name] = {"graph_call_us": 1e3 * e0.elapsed_time(e1) / 20, "kernel": "attn_kernel (CUDA cores)"}
             continue
         ts = []
         for i in range(30):
@@ -382,7 +383,9 @@ def attention_side_measurement(dev, stream, sm_mhz: float):
         peak_fp32 = sms * 128 * 2 * sm_mhz * 1e6
         out[name] = {"call_us_p50": us, "algorithmic_bytes": bytes_, "hbm_gbs": bytes_ / us / 1e3,
                      "fp32_tflops": flops / us / 1e6, "fp32_frac": flops / (us * 1e-6) / peak_fp32,
-                     "fp32_peak_note": f"{sms} SMs x 128 lanes x 2 FLOP x {sm_mhz:.0f} MHz (sampled)"}
+                     "fp32_peak_note": f"{sms} SMs x 128 lanes x 2 FLOP x {sm_mhz:.0f} MHz (sampled)",
+                     "kernel": ("attn_tc_kernel (tensor cores, mma.sync)" if nq >= sms
+                                else "attn_kernel (CUDA cores)")}
     return out
 
 

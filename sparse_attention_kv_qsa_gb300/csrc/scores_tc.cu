@@ -166,7 +166,9 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
     return static_cast<uint32_t>(r) * 128u + (static_cast<uint32_t>(c ^ (r & 7)) << 4);
 }
 
-template <bool kInt8>
+// kSelect: the fused select's list and gated modes (sel), compiled apart so
+// that the plain scorer carries none of their code.
+template <bool kInt8, bool kSelect>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     scores_tc_kernel(const float *__restrict__ q, const __half *__restrict__ kscale, int nq, int active,
                      int ntiles, int ctas_per_group, float *__restrict__ scores, uint32_t *__restrict__ gmax,
@@ -184,13 +186,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int q0 = group * QGROUP;
     const int qn = min(QGROUP, nq - q0);
     const int nlocal = j0 < ntiles ? (ntiles - 1 - j0) / ctas_per_group + 1 : 0;
-    if (sel.gate != nullptr) {
+    if (kSelect && sel.gate != nullptr) {
         // Gated (the fused select's fallback): only query groups with a
         // flagged row; both CTAs of a pair belong to the same group.
         grid_dependency_wait();
         if (ld_in(sel.gate + group) == 0u) return;
     }
-    const bool list_mode = !kInt8 && sel.thr != nullptr;
+    const bool list_mode = kSelect && !kInt8 && sel.thr != nullptr;
     constexpr uint32_t PIECE_BYTES = PIECE_ROWS * KHALF * (kInt8 ? 1 : 4);
     auto tile_b0 = [&](int li) { return (j0 + li * ctas_per_group) * TILE_N; };
 
@@ -732,10 +734,13 @@ cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(scores_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(TC_SMEM));
+        cudaError_t e = cudaFuncSetAttribute(scores_tc_kernel<false, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(TC_SMEM));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(scores_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(scores_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(TC_SMEM));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(scores_tc_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(TC_SMEM));
         if (e != cudaSuccess) return e;
         configured_device = dev;
@@ -774,11 +779,15 @@ cudaError_t launch_scores_tc(const float *q, const float *kblk, const int8_t *kq
                         int8))
         return cudaErrorNotSupported;
     if (int8)
-        return cudaLaunchKernelEx(&cfg, scores_tc_kernel<true>, q, reinterpret_cast<const __half *>(kscale), nq,
+        return cudaLaunchKernelEx(&cfg, scores_tc_kernel<true, false>, q, reinterpret_cast<const __half *>(kscale), nq,
                                   active, ntiles, per, scores, gmax, key_map, out_map, use_tma, pair,
                                   wait_limit_ns(), debug_inject(), TcSelect());
-    return cudaLaunchKernelEx(&cfg, scores_tc_kernel<false>, q, static_cast<const __half *>(nullptr), nq, active,
-                              ntiles, per, scores, gmax, key_map, out_map, use_tma, pair, wait_limit_ns(),
+    if (sel.thr != nullptr || sel.gate != nullptr)
+        return cudaLaunchKernelEx(&cfg, scores_tc_kernel<false, true>, q, static_cast<const __half *>(nullptr), nq,
+                                  active, ntiles, per, scores, gmax, key_map, out_map, use_tma, pair,
+                                  wait_limit_ns(), debug_inject(), sel);
+    return cudaLaunchKernelEx(&cfg, scores_tc_kernel<false, false>, q, static_cast<const __half *>(nullptr), nq,
+                              active, ntiles, per, scores, gmax, key_map, out_map, use_tma, pair, wait_limit_ns(),
                               debug_inject(), sel);
 }
 

@@ -322,7 +322,7 @@ def block_select(q: torch.Tensor, kblk: torch.Tensor, active_blocks: int, k: int
 
 def block_select_static(q: torch.Tensor, kblk: torch.Tensor, active_blocks: int, k: int,
                         scores_out: torch.Tensor | None = None, ids_out: torch.Tensor | None = None):
-    """``qsa_block_select_static``: ``(scores, ids)`` as block_select, with
+    """``qsa_block_select_static``: ``(scores, ids)`` as block_select_gmax, with
     the group maxima in the library's fixed device scratch (the call
     allocates nothing; calls on one device must be ordered)."""
     _check_q(q)
