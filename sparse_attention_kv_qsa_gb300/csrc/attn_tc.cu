@@ -25,9 +25,12 @@
 //          x 8 d, sixteen m16n8k8 MMAs over d = 0..127.
 // High + remainder / 2^11 combine across the lanes 16 apart. Each warp keeps
 // an online softmax per head (running maximum, normaliser, the head's 128
-// outputs), in base 2, rescaling only in steps where a maximum moved; the
-// next step's rows load while the current step runs. The warps' partials
-// merge in warp order, so the output does not depend on scheduling.
+// outputs), in base 2, rescaling only in steps where a maximum moved. The K
+// and V rows of a warp's next 3 steps are in flight at once: asynchronous
+// 16-byte copies (through L2) into a 4-step ring in shared memory, so no
+// registers wait for them; the cell scales load one step ahead. The warps'
+// partials merge in warp order, so the output does not depend on
+// scheduling.
 #include <cuda_fp16.h>
 
 #include "ptx.cuh"
@@ -39,6 +42,11 @@ namespace {
 constexpr int AT_WARPS = 16;
 constexpr int AT_THREADS = AT_WARPS * 32;
 constexpr int STEP_IDS = 2;                              // listed blocks per warp step
+constexpr int STAGES = 4;                                // steps in each warp's ring (a power of two)
+// Dynamic shared memory: the warps' rings (16-byte slots [warp][stage][4][32])
+// and each slot's first V cell per lane ([warp][stage][32]).
+constexpr int RING_BYTES = AT_WARPS * STAGES * 4 * 32 * 16;
+constexpr int DYN_BYTES = RING_BYTES + AT_WARPS * STAGES * 32 * 4;
 // Logits are kept in base-2 units: (q . k) * ks / sqrt(128) * log2(e), so the
 // softmax weights are 2^(logit - max) (the same weights as e^ of the natural
 // logits); log2(e) / sqrt(128), rounded to fp32.
@@ -120,6 +128,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 const int8_t *__restrict__ vc, const __half *__restrict__ vs, int ncells,
                 const int32_t *__restrict__ ids, int k, float *__restrict__ out) {
     __shared__ AttnShared sh;
+    extern __shared__ __align__(16) uint8_t attn_dyn[];   // DYN_BYTES
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int i = static_cast<int>(blockIdx.x);   // query
     const int32_t *ids_i = ids + static_cast<size_t>(i) * k;
@@ -169,39 +178,60 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
 
     const int nsteps = (k - 1) / STEP_IDS + 1;   // k >= 1
+    // This warp's steps are wg, wg + nw, ...: the j-th is wg + j * nw.
     const int wg = warp, nw = AT_WARPS;
+    const int nj = wg < nsteps ? (nsteps - 1 - wg) / nw + 1 : 0;
 
-    // A step: two listed blocks (-1 when past k, padding or past the last
-    // block), this lane's 32 bytes (d = 32 t .. +31) of K cell g, and its 16
-    // bytes (d = 16 g .. +15) of V cells 2t and 2t+1 (zero for dead cells).
-    struct Step {
-        int b[STEP_IDS];
-        uint4 k0, k1, va, vb;
+    // Block ids 16 steps at a time: lane l holds block l % 2 of the warp's
+    // step 16 c + l / 2 of chunk c (raw; -1 past k); the next chunk's ids
+    // load while this one's are used. Blocks are checked when taken.
+    auto chunk_ids = [&](int c) -> int {
+        const int st = wg + (16 * c + (lane >> 1)) * nw, slot = STEP_IDS * st + (lane & 1);
+        return st < nsteps && slot < k ? ld_in(ids_i + slot) : -1;
     };
-    // ids and K words of step st (at the top of the previous step), V words
-    // (once the previous step's K words are no longer needed).
-    auto load_k = [&](int st, Step &sp) {
-#pragma unroll
-        for (int j = 0; j < STEP_IDS; ++j) {
-            const int slot = STEP_IDS * st + j;
-            const int b = st < nsteps && slot < k ? ld_in(ids_i + slot) : -1;
-            sp.b[j] = b >= 0 && b < nblocks ? b : -1;
+    int id_chunk = 0, id_cur = chunk_ids(0), id_next = chunk_ids(1);
+    auto step_block = [&](int j, int which) {   // warp-uniform j, nondecreasing over calls
+        if ((j >> 4) != id_chunk) {
+            id_chunk = j >> 4;
+            id_cur = id_next;
+            id_next = chunk_ids(id_chunk + 1);
         }
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-        const int b = sp.b[g >> 2], cell = 4 * b + (g & 3);
-        const bool live = b >= 0 && cell < ncells;
-        const uint4 *row = reinterpret_cast<const uint4 *>(kc + static_cast<size_t>(live ? cell : 0) * D + 32 * t);
-        sp.k0 = live ? ld_in(row) : z;
-        sp.k1 = live ? ld_in(row + 1) : z;
+        const int b = __shfl_sync(FULL_MASK, id_cur, 2 * (j & 15) + which);
+        return b >= 0 && b < nblocks ? b : -1;
     };
-    auto load_v = [&](Step &sp) {
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-        {
-            const int b = sp.b[t >> 1], c0 = 4 * b + 2 * (t & 1);
-            const bool l0 = b >= 0 && c0 < ncells, l1 = b >= 0 && c0 + 1 < ncells;
-            sp.va = l0 ? ld_in(reinterpret_cast<const uint4 *>(vc + static_cast<size_t>(c0) * D + 16 * g)) : z;
-            sp.vb = l1 ? ld_in(reinterpret_cast<const uint4 *>(vc + static_cast<size_t>(c0 + 1) * D + 16 * g)) : z;
+
+    // The warp's ring of STAGES steps: each lane copies its own rows into its
+    // own slots, 16 bytes at a time, asynchronously through L2 (so only the
+    // lane's own copies need waiting for): slot c of lane l at [c][l], c = 0, 1
+    // its K bytes (cell g, d = 32 t .. +31), c = 2, 3 its V bytes (cells 2t,
+    // 2t+1, d = 16 g .. +15); dead cells are not copied (their logits are
+    // masked and their weights are 0, so stale bytes never count). cellv: the
+    // lane's first V cell of the step, or -1.
+    uint4 *ring = reinterpret_cast<uint4 *>(attn_dyn) + static_cast<size_t>(warp) * STAGES * 4 * 32;
+    int *cellv = reinterpret_cast<int *>(attn_dyn + RING_BYTES) + warp * STAGES * 32;
+    auto issue = [&](int j) {
+        const int b0 = step_block(j, 0), b1 = step_block(j, 1);
+        const int sl = j & (STAGES - 1);
+        uint4 *slot = ring + sl * 128;
+        const int bk = (g >> 2) ? b1 : b0, ck = 4 * bk + (g & 3);
+        if (bk >= 0 && ck < ncells) {
+            const int8_t *src = kc + static_cast<size_t>(ck) * D + 32 * t;
+            cp_async_16(slot + lane, src);
+            cp_async_16(slot + 32 + lane, src + 16);
         }
+        const int bv = (t >> 1) ? b1 : b0, cv = 4 * bv + 2 * (t & 1);
+        if (bv >= 0 && cv < ncells) cp_async_16(slot + 64 + lane, vc + static_cast<size_t>(cv) * D + 16 * g);
+        if (bv >= 0 && cv + 1 < ncells) cp_async_16(slot + 96 + lane, vc + static_cast<size_t>(cv + 1) * D + 16 * g);
+        cp_async_commit();
+        cellv[sl * 32 + lane] = bv >= 0 ? cv : -1;
+    };
+    // The binary16 scales of the lane's two V cells (K scales low, V scales
+    // high half each): loaded one step before they are used.
+    auto load_scales = [&](int j, uint32_t &kk, uint32_t &vv) {
+        const int c0 = j < nj ? cellv[(j & (STAGES - 1)) * 32 + lane] : -1;
+        const bool l0 = c0 >= 0 && c0 < ncells, l1 = c0 >= 0 && c0 + 1 < ncells;
+        kk = (l0 ? ld_in_u16(ks + c0) : 0u) | (l1 ? static_cast<uint32_t>(ld_in_u16(ks + c0 + 1)) << 16 : 0u);
+        vv = (l0 ? ld_in_u16(vs + c0) : 0u) | (l1 ? static_cast<uint32_t>(ld_in_u16(vs + c0 + 1)) << 16 : 0u);
     };
 
     float m = -INFINITY, lsum = 0.0f;   // head hd: running maximum; this lane's normaliser part
@@ -216,25 +246,30 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
     for (int u = 0; u < 16; ++u) acc[u][0] = acc[u][1] = 0.0f;
 
-    auto run_step = [&](const Step &sp, Step &next) {
+    auto run_step = [&](int j, uint32_t ksc, uint32_t vsc) {
+        const int sl = j & (STAGES - 1);
+        const uint4 *slot = ring + sl * 128;
         // Logits of cells 2t, 2t+1 for head hd: eight m16n8k16 MMAs.
         float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
-        const uint32_t kw[8] = {sp.k0.x, sp.k0.y, sp.k0.z, sp.k0.w, sp.k1.x, sp.k1.y, sp.k1.z, sp.k1.w};
+        {
+            const uint4 ka = slot[lane], kb = slot[32 + lane];
+            const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-        for (int st = 0; st < 8; ++st) {
-            const uint32_t wx = kw[st] ^ 0x80808080u;
-            mma_16816(c0, c1, c2, c3, aq[(2 * st) * 32 + lane], aq[(2 * st + 1) * 32 + lane], i8x2_h2(wx, 0x4140u),
-                      i8x2_h2(wx, 0x4342u));
+            for (int st = 0; st < 8; ++st) {
+                const uint32_t wx = kw[st] ^ 0x80808080u;
+                mma_16816(c0, c1, c2, c3, aq[(2 * st) * 32 + lane], aq[(2 * st + 1) * 32 + lane],
+                          i8x2_h2(wx, 0x4140u), i8x2_h2(wx, 0x4342u));
+            }
         }
-        load_v(next);
         // High part + remainder (from the lane 16 apart), in the same order in both lanes.
         const float o0 = __shfl_xor_sync(FULL_MASK, c0, 16), o1 = __shfl_xor_sync(FULL_MASK, c1, 16);
         const float dot0 = (lo_row ? o0 : c0) + (lo_row ? c0 : o0) * (1.0f / 2048.0f);
         const float dot1 = (lo_row ? o1 : c1) + (lo_row ? c1 : o1) * (1.0f / 2048.0f);
-        const int b = sp.b[t >> 1], cell0 = 4 * b + 2 * (t & 1);
-        const bool live0 = b >= 0 && cell0 < ncells, live1 = b >= 0 && cell0 + 1 < ncells;
-        const float lg0 = live0 ? dot0 * __half2float(__ushort_as_half(ld_in_u16(ks + cell0))) * qs : -INFINITY;
-        const float lg1 = live1 ? dot1 * __half2float(__ushort_as_half(ld_in_u16(ks + cell0 + 1))) * qs : -INFINITY;
+        const int cell0 = cellv[sl * 32 + lane];
+        const bool live0 = cell0 >= 0 && cell0 < ncells, live1 = cell0 >= 0 && cell0 + 1 < ncells;
+        const float lg0 = live0 ? dot0 * __half2float(__ushort_as_half(static_cast<unsigned short>(ksc))) * qs : -INFINITY;
+        const float lg1 = live1 ? dot1 * __half2float(__ushort_as_half(static_cast<unsigned short>(ksc >> 16))) * qs
+                                : -INFINITY;
         // Online softmax of head hd over the step's 8 cells (lanes 4g .. 4g+3).
         float bm = fmaxf(lg0, lg1);
         bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 1));
@@ -245,7 +280,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const float p1 = live1 ? exp2f(lg1 - mn) : 0.0f;
         m = mn;
         lsum = fmaf(lsum, alpha, p0 + p1);
-        const uint32_t v0 = live0 ? ld_in_u16(vs + cell0) : 0u, v1 = live1 ? ld_in_u16(vs + cell0 + 1) : 0u;
+        const uint32_t v0 = vsc & 0xFFFFu, v1 = vsc >> 16;   // 0 for dead cells
         const uint32_t f = __reduce_max_sync(FULL_MASK, max(half_exponent(v0), half_exponent(v1)));
         float shrink = 1.0f;
         if (f > vf) {   // warp-uniform: a larger value scale than any before
@@ -268,10 +303,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const float w1 = p1 * __half2float(__ushort_as_half(static_cast<unsigned short>(v1))) * sw;
         const uint32_t ap = split_pack(w0, w1, lo_row, 2048.0f);
         // p . v: sixteen m16n8k8 MMAs, n-tile u takes byte u of cells 2t and 2t+1.
-        const uint32_t va[4] = {sp.va.x ^ 0x80808080u, sp.va.y ^ 0x80808080u, sp.va.z ^ 0x80808080u,
-                                sp.va.w ^ 0x80808080u};
-        const uint32_t vb[4] = {sp.vb.x ^ 0x80808080u, sp.vb.y ^ 0x80808080u, sp.vb.z ^ 0x80808080u,
-                                sp.vb.w ^ 0x80808080u};
+        const uint4 sa = slot[64 + lane], sb = slot[96 + lane];
+        const uint32_t va[4] = {sa.x ^ 0x80808080u, sa.y ^ 0x80808080u, sa.z ^ 0x80808080u, sa.w ^ 0x80808080u};
+        const uint32_t vb[4] = {sb.x ^ 0x80808080u, sb.y ^ 0x80808080u, sb.z ^ 0x80808080u, sb.w ^ 0x80808080u};
 #pragma unroll
         for (int wd = 0; wd < 4; ++wd) {
             const uint32_t lo2 = __byte_perm(va[wd], vb[wd], 0x5140u);   // a0 b0 a1 b1
@@ -283,20 +317,23 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
     };
 
-    // Two step buffers in turn: the next step's rows load while this one runs.
-    Step s0, s1;
-    int st = wg;
-    load_k(st, s0);
-    load_v(s0);
-    while (st < nsteps) {   // warp-uniform
-        load_k(st + nw, s1);
-        run_step(s0, s1);
-        st += nw;
-        if (st >= nsteps) break;
-        load_k(st + nw, s0);
-        run_step(s1, s0);
-        st += nw;
+    // STAGES - 1 steps in flight ahead of the one being computed; every issue
+    // commits one group (empty past the warp's last step), so waiting for all
+    // but the STAGES - 1 newest groups leaves step j's rows in place. A stale
+    // V byte of a dead cell stays a finite int8 value times a zero weight.
+    for (int a = 0; a < STAGES - 1; ++a) issue(a);
+    uint32_t ksc, vsc;
+    load_scales(0, ksc, vsc);
+    for (int j = 0; j < nj; ++j) {   // warp-uniform
+        issue(j + STAGES - 1);
+        cp_async_wait<STAGES - 1>();
+        uint32_t nks, nvs;
+        load_scales(j + 1, nks, nvs);
+        run_step(j, ksc, vsc);
+        ksc = nks;
+        vsc = nvs;
     }
+    cp_async_wait<0>();
 
     // Warp partials: head hd's normaliser sums over its 4 lanes; its outputs
     // are high part + remainder / 2^11 (from the lane 16 apart), / 2^(29 - vf).
@@ -346,10 +383,19 @@ cudaError_t launch_sparse_attn_tc(const float *q, const int8_t *kc, const uint16
                                   const uint16_t *vs, int ncells, const int32_t *ids, int nq, int k, float *out,
                                   cudaStream_t stream) {
     if (ncells > 0x7FFFFFFF - 4) return cudaErrorInvalidValue;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DYN_BYTES);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(nq));
     cfg.blockDim = dim3(AT_THREADS);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = DYN_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[1];
     attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

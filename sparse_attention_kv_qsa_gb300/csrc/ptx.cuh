@@ -178,6 +178,20 @@ __device__ __forceinline__ bool wait_word_reaches(const uint32_t *p, uint32_t ta
 
 // Asks the TMA unit to bring [src, src + bytes) into L2 (no destination, no
 // completion to wait for). src 16-byte aligned; bytes % 16 == 0.
+// 16-byte asynchronous copy global -> shared that reads through L2 only
+// (cp.async.cg), grouped by commit and waited for by the issuing thread.
+__device__ __forceinline__ void cp_async_16(void *dst_smem, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)),
+                 "l"(__cvta_generic_to_global(src))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's most recent groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
