@@ -13,7 +13,7 @@
 // key byte is used nq times, so the tensor-core tile (128 query rows) would be
 // almost all padding. A key row is split over TPR threads (fp32: 4 threads x
 // 32 values; int8: 2 threads x 64 values); each thread streams its part with
-// 16-byte read-only loads and accumulates one fp32 FMA chain per query
+// 16-byte L2-only loads and accumulates one fp32 FMA chain per query
 // against the head-summed queries in shared memory (read as broadcasts), and
 // the TPR partial sums meet by warp shuffles. Rows at or beyond `active` are
 // never read.

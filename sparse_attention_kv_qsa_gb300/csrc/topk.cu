@@ -27,7 +27,7 @@
 //  digits below run on that list.
 //  Without them, rows of at least 8,192 scores first try a listing path. A strided 1/32
 //  sample of the row fixes a threshold expected to pass about 1.8k scores;
-//  one pass of 16-byte read-only loads then lists every score at or above
+//  one pass of 16-byte L2-only loads then lists every score at or above
 //  the threshold, and the digits below run on that list alone. A list shorter than k or longer
 //  than its capacity sends the row to the exact passes, so the result is
 //  exact either way.
@@ -218,7 +218,7 @@ __device__ __forceinline__ void warp_select_2048(uint32_t target, RowShared &sh,
 
 // Calls fn(i, bits) once for every element of the row (row index i, raw
 // fp32 bits), each from some thread; every thread must call it. The aligned
-// body moves as 16-byte read-only loads, UNROLL in flight per thread; the
+// body moves as 16-byte L2-only loads, UNROLL in flight per thread; the
 // <= 3 ragged scores at either end as single words.
 template <bool kCoherent, typename Fn>
 __device__ __forceinline__ void stream_row(const uint32_t *g, int n, int head, int nvec, int tid, Fn &&fn) {
