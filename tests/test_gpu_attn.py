@@ -99,13 +99,14 @@ def _check(W, out):
                                              (4, 262144, 128, 0),
                                              (30, 65536, 256, 3),       # clusters of 4
                                              (60, 16384, 64, 0),        # pairs
-                                             (200, 16384, 512, 17),     # one CTA per query
+                                             (100, 16384, 512, 17),     # one CTA per query (CUDA cores)
                                              (3, 4099 * 4 + 3, 60, 7),  # partial last block
                                              (2, 17, 5, 0),             # every block, ragged
                                              (5, 4096, 1, 0),           # one block
                                              (2, 262144, 4096, 0),      # long lists: 16,384 cells per query
                                              (7, 65536, 300, 290),      # mostly padding
                                              # tensor-core kernel (nq >= SMs):
+                                             (200, 16384, 512, 17),
                                              (256, 262144, 512, 0),     # the bench's many-query shape
                                              (152, 4099 * 4 + 3, 60, 7),
                                              (160, 17, 5, 0),
