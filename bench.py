@@ -469,8 +469,10 @@ def main():
                     help="only launch qsa_block_summary this many times over a 262,144-cell pool (65,536 "
                          "blocks, both key forms; a short run for a profiler to capture), then exit")
     ap.add_argument("--attn-launches", type=int, default=0,
-                    help="only launch qsa_sparse_attn this many times on 256 queries x k=512 over 262,144 "
-                         "cells (a short run for a profiler to capture), then exit")
+                    help="only launch qsa_sparse_attn this many times on --attn-nq queries x k=512 over "
+                         "262,144 cells (a short run for a profiler to capture), then exit")
+    ap.add_argument("--attn-nq", type=int, default=256,
+                    help="queries of the --attn-launches run (below the SM count: the CUDA-core kernel)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -514,7 +516,7 @@ def main():
         print(json.dumps({"summary_launches": args.summary_launches, "workload": "262,144 cells"}), flush=True)
         return
     if args.attn_launches > 0:
-        A = workloads.attn_case(256, 262144, 512)
+        A = workloads.attn_case(args.attn_nq, 262144, 512)
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
         ks, vs = t(A.ks.view(np.int16)), t(A.vs.view(np.int16))
         q, kc, vc, ids = t(A.q), t(A.kc), t(A.vc), t(A.ids)
