@@ -712,8 +712,10 @@ def main():
                     "steps": len(t_step)},
         "roofline": roof,
         "step_roofline": {"floor_us": floor_us, "frac": floor_us / (step_ms * 1e3),
-                          "note": "algorithmic step bytes at the HBM peak (the step's binding roof when "
-                                  "scoring runs on tensor cores)"},
+                          "note": "algorithmic step bytes at the measured HBM copy peak (the step's binding "
+                                  "roof when scoring runs on tensor cores)",
+                          "floor_us_nominal_8tbs": alg["step_bytes"] / 8e12 * 1e6,
+                          "frac_nominal_8tbs": alg["step_bytes"] / 8e12 * 1e6 / (step_ms * 1e3)},
         "gpu_launches": 2 * K_,
         "other_path": other,
         "select": select,
