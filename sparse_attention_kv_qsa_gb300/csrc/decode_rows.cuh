@@ -48,16 +48,45 @@ __device__ __forceinline__ void dec_build_queries(const float *__restrict__ q, i
     }
 }
 
+// This thread's part of its key row in a chunk (16-byte words: 8 of fp32
+// keys, 4 of int8 keys), loaded by dec_load_keys before the queries are built
+// so that the two loads' round trips overlap.
+template <bool kInt8>
+struct DecKeys {
+    uint4 w[kInt8 ? D / 2 / 16 : D / 4 / 4];
+};
+
+template <bool kInt8, int THREADS>
+__device__ __forceinline__ void dec_load_keys(long long chunk, const float *__restrict__ kblk,
+                                              const int8_t *__restrict__ kq8, int active, DecKeys<kInt8> &kv) {
+    constexpr int TPR = dec_tpr<kInt8>();
+    constexpr int PER = D / TPR;
+    constexpr int ROWS = THREADS / TPR;
+    const long long b = chunk * ROWS + threadIdx.x / TPR;   // key row
+    const int part = static_cast<int>(threadIdx.x % TPR);
+    constexpr int NW = sizeof(kv.w) / sizeof(uint4);
+    if (b < active) {
+        const uint4 *row = kInt8 ? reinterpret_cast<const uint4 *>(kq8 + b * D + part * PER)
+                                 : reinterpret_cast<const uint4 *>(kblk + b * D + part * PER);
+#pragma unroll
+        for (int c = 0; c < NW; ++c) kv.w[c] = ld_in(row + c);
+    } else {
+#pragma unroll
+        for (int c = 0; c < NW; ++c) kv.w[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 // Scores of key rows chunk * ROWS .. + ROWS - 1 (ROWS = THREADS / TPR) for
-// all queries, and, when gmax is given, the key of each of the chunk's
-// 32-block groups' largest score (the chunk's rows are whole groups; their
-// keys meet in gk and one warp per (query, group) takes the maximum). Every
-// thread of the CTA calls this; it ends with the CTA synchronised.
+// all queries, from the keys dec_load_keys loaded for the same chunk, and,
+// when gmax is given, the key of each of the chunk's 32-block groups'
+// largest score (the chunk's rows are whole groups; their keys meet in gk and
+// one warp per (query, group) takes the maximum). Every thread of the CTA
+// calls this; it ends with the CTA synchronised.
 template <int NQ, bool kInt8, int THREADS>
 __device__ __forceinline__ void dec_score_chunk(const float (*qs)[DEC_QROW], long long chunk,
-                                                const float *__restrict__ kblk, const int8_t *__restrict__ kq8,
-                                                const __half *__restrict__ kscale, int nq, int active,
-                                                float *__restrict__ scores, uint32_t *__restrict__ gmax,
+                                                const DecKeys<kInt8> &keys, const __half *__restrict__ kscale,
+                                                int nq, int active, float *__restrict__ scores,
+                                                uint32_t *__restrict__ gmax,
                                                 uint32_t (*gk)[THREADS / dec_tpr<kInt8>()]) {
     constexpr int TPR = dec_tpr<kInt8>();
     constexpr int PER = D / TPR;                // values per thread: 64 (int8) or 32 (fp32)
@@ -71,10 +100,11 @@ __device__ __forceinline__ void dec_score_chunk(const float (*qs)[DEC_QROW], lon
     for (int r = 0; r < NQ; ++r) acc[r] = 0.0f;
     if (live) {
         if constexpr (!kInt8) {
-            const float4 *row = reinterpret_cast<const float4 *>(kblk + b * D + part * PER);
             float4 kv[PER / 4];
 #pragma unroll
-            for (int c = 0; c < PER / 4; ++c) kv[c] = ld_in(row + c);
+            for (int c = 0; c < PER / 4; ++c)
+                kv[c] = make_float4(__uint_as_float(keys.w[c].x), __uint_as_float(keys.w[c].y),
+                                    __uint_as_float(keys.w[c].z), __uint_as_float(keys.w[c].w));
 #pragma unroll
             for (int c = 0; c < PER / 4; ++c) {
 #pragma unroll
@@ -87,19 +117,20 @@ __device__ __forceinline__ void dec_score_chunk(const float (*qs)[DEC_QROW], lon
                 }
             }
         } else {
-            const uint4 *row = reinterpret_cast<const uint4 *>(kq8 + b * D + part * PER);
-            uint4 kv[PER / 16];
-#pragma unroll
-            for (int c = 0; c < PER / 16; ++c) kv[c] = ld_in(row + c);
 #pragma unroll
             for (int c = 0; c < PER / 16; ++c) {
-                const uint32_t w4[4] = {kv[c].x, kv[c].y, kv[c].z, kv[c].w};
+                const uint32_t w4[4] = {keys.w[c].x, keys.w[c].y, keys.w[c].z, keys.w[c].w};
 #pragma unroll
                 for (int wi = 0; wi < 4; ++wi) {
+                    // int8 -> fp32 exactly, without a conversion instruction:
+                    // the byte + 128 becomes the low mantissa bits of 2^23,
+                    // and subtracting 2^23 + 128 leaves the value.
+                    const uint32_t wx = w4[wi] ^ 0x80808080u;
                     float kf[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        kf[e] = static_cast<float>(static_cast<int8_t>((w4[wi] >> (8 * e)) & 0xFFu));
+                        kf[e] = __uint_as_float(__byte_perm(wx, 0x4B000000u, 0x7540u | static_cast<uint32_t>(e))) -
+                                8388736.0f;
 #pragma unroll
                     for (int r = 0; r < NQ; ++r) {
                         const float4 qv =

@@ -16,9 +16,11 @@ __global__ void __launch_bounds__(ROWS_THREADS)
     __shared__ uint32_t gk[NQ][ROWS_THREADS / dec_tpr<kInt8>()];
     grid_dependency_wait();   // q and the keys may come from the previous grid
     grid_launch_dependents();
+    DecKeys<kInt8> kv;
+    dec_load_keys<kInt8, ROWS_THREADS>(blockIdx.x, kblk, kq8, active, kv);   // in flight during the build
     dec_build_queries<NQ, ROWS_THREADS>(q, nq, qs);
     __syncthreads();
-    dec_score_chunk<NQ, kInt8, ROWS_THREADS>(qs, blockIdx.x, kblk, kq8, kscale, nq, active, scores, gmax, gk);
+    dec_score_chunk<NQ, kInt8, ROWS_THREADS>(qs, blockIdx.x, kv, kscale, nq, active, scores, gmax, gk);
 }
 
 template <int NQ>

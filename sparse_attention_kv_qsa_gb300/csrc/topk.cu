@@ -953,11 +953,16 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
     grid_launch_dependents();
     uint32_t gen = 0u;
     if (threadIdx.x == 0) gen = ld_acquire_gpu(&g_decode_sync[2]);
+    const long long nchunks = (static_cast<long long>(active) + ROWS - 1) / ROWS;
+    DecKeys<kInt8> kv;
+    long long c = blockIdx.x;
+    if (c < nchunks) dec_load_keys<kInt8, ROW_THREADS>(c, kblk, kq8, active, kv);   // in flight during the build
     dec_build_queries<NQ, ROW_THREADS>(q, nq, qs);
     __syncthreads();
-    const long long nchunks = (static_cast<long long>(active) + ROWS - 1) / ROWS;
-    for (long long c = blockIdx.x; c < nchunks; c += gridDim.x)
-        dec_score_chunk<NQ, kInt8, ROW_THREADS>(qs, c, kblk, kq8, kscale, nq, active, scores, g_decode_gmax, gk);
+    for (; c < nchunks; c += gridDim.x) {
+        if (c != blockIdx.x) dec_load_keys<kInt8, ROW_THREADS>(c, kblk, kq8, active, kv);
+        dec_score_chunk<NQ, kInt8, ROW_THREADS>(qs, c, kv, kscale, nq, active, scores, g_decode_gmax, gk);
+    }
     if (threadIdx.x == 0) {
         // The arrival releases this CTA's scores and group maxima (ordered
         // before it by the CTA barrier that ends the scoring); a top-k CTA's
