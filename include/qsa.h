@@ -18,9 +18,12 @@
  *
  * Conventions for every call below:
  *  - All pointers are DEVICE pointers owned by the caller; the library keeps
- *    no state between calls (beyond a per-device error word, see
- *    qsa_get_device_error), allocates nothing, never synchronises, and
- *    enqueues its kernels on `stream` (0 = the legacy default stream).
+ *    no state between calls beyond a per-device error word (see
+ *    qsa_get_device_error), the fixed device arrays of the two
+ *    allocation-free calls (qsa_block_select_static, qsa_block_select_small)
+ *    and the process-wide wait settings of qsa_debug_inject; it allocates
+ *    nothing, never synchronises (except qsa_get_device_error), and enqueues
+ *    its kernels on `stream` (0 = the legacy default stream).
  *  - Every pointer that is dereferenced must be 16-byte aligned.
  *  - Arguments are checked before anything is launched; a bad argument
  *    returns QSA_ERR_INVALID and launches nothing. A launch failure returns
