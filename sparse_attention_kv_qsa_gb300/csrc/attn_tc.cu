@@ -115,6 +115,8 @@ __device__ __forceinline__ void mma_16816(float &c0, float &c1, float &c2, float
 
 // Row g of D (columns 2t, 2t+1) += A (16 x 8, rows g+8 zero) x B (8 x 8); the
 // zero rows' results are dropped.
+// (d2 and d3 are asm outputs that nothing reads: the diagnostic for that is off here.)
+#pragma nv_diag_suppress 550
 __device__ __forceinline__ void mma_1688(float &c0, float &c1, uint32_t a0, uint32_t b0) {
     float d2, d3;   // rows g + 8 (zero): dropped
     asm volatile(
@@ -122,6 +124,7 @@ __device__ __forceinline__ void mma_1688(float &c0, float &c1, uint32_t a0, uint
         : "+f"(c0), "+f"(c1), "=f"(d2), "=f"(d3)
         : "r"(a0), "r"(0u), "r"(b0), "f"(0.0f));
 }
+#pragma nv_diag_default 550
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
     attn_tc_kernel(const float *__restrict__ q, const int8_t *__restrict__ kc, const __half *__restrict__ ks,
