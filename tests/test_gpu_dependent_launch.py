@@ -62,11 +62,12 @@ def test_static_select_back_to_back(dev, nq, active, k):
     assert qsa.device_error(dev) == 0
 
 
-def test_graph_scores_topk_attention(dev):
+@pytest.mark.parametrize("nq", [4, 160])   # decode scorer + CUDA-core attention / tensor cores for both
+def test_graph_scores_topk_attention(dev, nq):
     """One graph: scores (with group maxima), top-k, attention over the
     selected blocks. The attention reads the ids of the grid before it."""
     o = oracle.get()
-    nq, k, cells = 4, 96, 32768
+    k, cells = 96, 32768
     A = w.attn_case(nq, cells, k)
     W = w.normal_case(nq, cells // 4, k)
     q, kb = to_dev(A.q, dev), to_dev(W.kblk, dev)
