@@ -106,7 +106,9 @@ def decode_side_measurement(dev, stream, cells_list=(2048, 16384, 65536, 262144)
     with a CUDA-event pair per step (L2 flushed first) and once per step of a
     CUDA graph of 20 back-to-back steps; for the one-launch call (fused:
     qsa_block_select_small), the group-maximum calls (gmax) and the plain
-    ones. Rows of at most 16,384 blocks take the register-resident top-k."""
+    ones. Rows of at most 8,192 blocks take the register-resident top-k.
+    `layer`: the whole decode layer of the pages' breakdown (append, scores,
+    top-k, attention) as one CUDA graph per step."""
     import torch
     import sparse_attention_kv_qsa_gb300 as qsa
     from sparse_attention_kv_qsa_gb300 import workloads as w
@@ -165,6 +167,66 @@ def decode_side_measurement(dev, stream, cells_list=(2048, 16384, 65536, 262144)
             res[name] = {"step_p50": pct(ts, 50), "step_p10": pct(ts, 10), "step_p90": pct(ts, 90),
                          "graph_step": 1e3 * e0.elapsed_time(e1) / 20}
         out[f"nq{nq}_c{cells}"] = res
+    out["layer"] = decode_layer_measurement(dev, stream)
+    return out
+
+
+def decode_layer_measurement(dev, stream, cells=262144, k=128):
+    """One decode layer per step, as the pages break it down (append +
+    scores + top-k + attention), on one int8 KV pool: the summary keys of the
+    block the new cell fell into are refreshed (qsa_block_summary, one
+    block), the queries are scored against the int8 summary keys and the top
+    k selected (the two group-maximum calls), and the 4 heads attend the
+    selected blocks' cells (qsa_sparse_attn). Microseconds per step of a CUDA
+    graph of 20 steps; the four calls run as programmatic dependents."""
+    import torch
+    import sparse_attention_kv_qsa_gb300 as qsa
+    from sparse_attention_kv_qsa_gb300 import workloads as w
+    nblocks = cells // 4
+    out = {"workload": f"decode layer: {cells:,} int8 KV cells, k={k}, append of one block's keys + "
+                       "scores + top-k + attention", "unit": "us"}
+    for nq in (1, 4):
+        A = w.attn_case(nq, cells, k)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        q, kc, vc = t(A.q), t(A.kc), t(A.vc)
+        ks, vs = t(A.ks.view(np.int16)), t(A.vs.view(np.int16))
+        kq = torch.empty((nblocks + 2, 128), dtype=torch.int8, device=dev)
+        ksc = torch.empty((nblocks + 2,), dtype=torch.int16, device=dev)
+        qsa.block_summary(kc, ks, 0, nblocks, kblk_q8=kq, kblk_scale_f16=ksc)
+        s = torch.empty((nq, nblocks), dtype=torch.float32, device=dev)
+        gm = torch.empty((nq, qsa.groups(nblocks)), dtype=torch.int32, device=dev)
+        ids = torch.empty((nq, k), dtype=torch.int32, device=dev)
+        o = torch.empty((nq, 4, 128), dtype=torch.float32, device=dev)
+
+        def layer():
+            qsa.block_summary(kc, ks, nblocks - 1, nblocks, kblk_q8=kq, kblk_scale_f16=ksc)
+            qsa.block_scores_q8_gmax(q, kq, ksc, nblocks, out=s, gmax_out=gm)
+            qsa.block_topk_gmax(s, gm, k, out=ids)
+            qsa.sparse_attn(q, kc, ks, vc, vs, ids, out=o)
+
+        for _ in range(5):
+            layer()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            layer()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(20):
+                    layer()
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            v = 1e3 * e0.elapsed_time(e1) / 20
+            best = v if best is None else min(best, v)
+        out[f"nq{nq}"] = {"graph_step": best}
     return out
 
 
