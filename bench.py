@@ -171,7 +171,7 @@ def decode_side_measurement(dev, stream, cells_list=(2048, 16384, 65536, 262144)
     return out
 
 
-def decode_layer_measurement(dev, stream, cells=262144, k=128):
+def decode_layer_measurement(dev, stream, cells=262144, k=128, nqs=(1, 4), graph=True, launches=0):
     """One decode layer per step, as the pages break it down (append +
     scores + top-k + attention), on one int8 KV pool: the summary keys of the
     block the new cell fell into are refreshed (qsa_block_summary, one
@@ -185,7 +185,7 @@ def decode_layer_measurement(dev, stream, cells=262144, k=128):
     nblocks = cells // 4
     out = {"workload": f"decode layer: {cells:,} int8 KV cells, k={k}, append of one block's keys + "
                        "scores + top-k + attention", "unit": "us"}
-    for nq in (1, 4):
+    for nq in nqs:
         A = w.attn_case(nq, cells, k)
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
         q, kc, vc = t(A.q), t(A.kc), t(A.vc)
@@ -204,9 +204,11 @@ def decode_layer_measurement(dev, stream, cells=262144, k=128):
             qsa.block_topk_gmax(s, gm, k, out=ids)
             qsa.sparse_attn(q, kc, ks, vc, vs, ids, out=o)
 
-        for _ in range(5):
+        for _ in range(5 if graph else launches):
             layer()
         torch.cuda.synchronize()
+        if not graph:
+            continue
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream(dev)
         side.wait_stream(torch.cuda.current_stream(dev))
@@ -533,6 +535,9 @@ def main():
     ap.add_argument("--attn-launches", type=int, default=0,
                     help="only launch qsa_sparse_attn this many times on --attn-nq queries x k=512 over "
                          "262,144 cells (a short run for a profiler to capture), then exit")
+    ap.add_argument("--layer-launches", type=int, default=0,
+                    help="only run the decode layer (append + scores + top-k + attention, nq = 4, 262,144 cells, "
+                         "k=128) this many times (a short run for a profiler to capture), then exit")
     ap.add_argument("--attn-nq", type=int, default=256,
                     help="queries of the --attn-launches run (below the SM count: the CUDA-core kernel)")
     args = ap.parse_args()
@@ -576,6 +581,13 @@ def main():
             qsa.block_summary(kc, ks, 0, 65536, kblk=key, kblk_q8=q8, kblk_scale_f16=sc)
         torch.cuda.synchronize()
         print(json.dumps({"summary_launches": args.summary_launches, "workload": "262,144 cells"}), flush=True)
+        return
+    if args.layer_launches > 0:
+        decode_layer_measurement(dev, torch.cuda.current_stream(dev), nqs=(4,), graph=False,
+                                 launches=args.layer_launches)
+        torch.cuda.synchronize()
+        print(json.dumps({"layer_launches": args.layer_launches, "workload": "decode layer, nq=4, 262,144 cells"}),
+              flush=True)
         return
     if args.attn_launches > 0:
         A = workloads.attn_case(args.attn_nq, 262144, 512)
