@@ -295,15 +295,24 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = [l.split(", ") for l in self.lines if l and l[0].isdigit()]
+        return self.summarise(self.lines)
+
+    @staticmethod
+    def summarise(lines: list[str]) -> dict | None:
+        """Median SM clock, maximum SM clock and the throttle reasons seen
+        Active in nvidia-smi's csv,noheader,nounits rows of FIELDS; rows that
+        do not start with a GPU index and fields that are not numbers (such
+        as [N/A]) are skipped."""
+        rows = [l.split(", ") for l in lines if l and l[0].isdigit()]
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        smax = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        num = lambda x: x.replace(".", "", 1).isdigit()
+        sm = [float(r[1]) for r in rows if len(r) > 1 and num(r[1])]
+        smaxs = [float(r[2]) for r in rows if len(r) > 2 and num(r[2])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[j] for r in rows for j in range(4) if len(r) > 5 + j and r[5 + j] == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": reasons,
-                "samples": len(rows)}
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smaxs) if smaxs else None,
+                "reasons": reasons, "samples": len(rows)}
 
 
 def cpu_oracle_baseline(W, budget_s: float = 20.0, nq_sample: int | None = None) -> dict:
