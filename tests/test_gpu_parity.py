@@ -129,6 +129,39 @@ def test_int8_ragged(dev, o, scorer, nq, active, k):
     check_select(o, W, gpu_scores(W, dev, scorer))
 
 
+def _wide_magnitudes(W, seed=11):
+    """Query rows and key rows rescaled by 10^u, u uniform in [-15, 15] per
+    row (far outside the binary16 range the tensor-core scorer's operand
+    parts use), plus one query row dominated by a single element, one zero
+    key and one key with a single nonzero element."""
+    u = w.uniform(seed, 91, W.nq)
+    q = (W.q.astype(np.float64) * (10.0 ** (30.0 * u - 15.0))[:, None, None]).astype(np.float32)
+    q[0, :, 0] = 1e12
+    W.q = q
+    if W.kblk is not None:
+        v = w.uniform(seed, 92, W.active)
+        kb = W.kblk.copy()
+        kb[:W.active] = (kb[:W.active].astype(np.float64) * (10.0 ** (30.0 * v - 15.0))[:, None]).astype(np.float32)
+        kb[min(5, W.active - 1)] = 0.0
+        if W.active > 7:
+            kb[7] = 0.0
+            kb[7, 3] = 2.5e-20
+        W.kblk = kb
+    return W
+
+
+@pytest.mark.parametrize("nq,active,k", [(160, 4099, 64), (256, 65536, 512), (7, 1000, 17)])
+def test_wide_magnitude_ranges(dev, o, nq, active, k):
+    W = _wide_magnitudes(w.normal_case(nq, active, k, max_blocks=active + 2))
+    check_select(o, W, gpu_scores(W, dev))
+
+
+@pytest.mark.parametrize("nq,active,k", [(160, 4099, 64), (4, 2048, 32)])
+def test_wide_query_magnitudes_int8_keys(dev, o, nq, active, k):
+    W = _wide_magnitudes(w.int8_case(nq, active, k, max_blocks=active + 2))
+    check_select(o, W, gpu_scores(W, dev))
+
+
 @pytest.mark.parametrize("nq,active", [(1, 1), (2, 63), (3, 4099), (4, 65536), (1, 70001)])
 def test_small_nq_fp32_keys(dev, o, nq, active):
     """nq <= 4 takes the CUDA-core row scorer (grid over key rows)."""
