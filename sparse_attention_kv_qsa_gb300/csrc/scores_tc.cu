@@ -528,6 +528,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         gmax[static_cast<size_t>(q0 + row) * ngr + (b0 + col0) / GROUP_BLOCKS + g] = gk[g];
             }
             if (gvec && team == 1) st_shared_v2(base + GX_OFF + row * 8, gk[0], gk[1]);
+            if (use_tma && li == nlocal - 1) {
+                // The CTA's last tile: its MMAs have completed (acc_full[1]),
+                // so the key stages are idle. Each team stages its half in one
+                // of them and both halves leave at once: no wait for earlier
+                // stores to finish reading a shared staging.
+                const uint32_t stg = base + KS_OFF + team * KS_STAGE_BYTES;
+#pragma unroll
+                for (int j = 0; j < TILE_N / 8; ++j) {
+                    const int box = j >> 3, chunk = j & 7;
+                    st_shared_v4(stg + box * OUT_BOX_BYTES + row * 128 + ((chunk ^ (row & 7)) << 4),
+                                 __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                 __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(2, EPI_THREADS);
+                if (gvec && team == 0 && row < qn) {
+                    const uint2 o = ld_shared_v2(base + GX_OFF + row * 8);
+                    *reinterpret_cast<uint4 *>(gmax + static_cast<size_t>(q0 + row) * ngr + b0 / GROUP_BLOCKS) =
+                        make_uint4(gk[0], gk[1], o.x, o.y);
+                }
+                if (epi_tid == 0) {
+#pragma unroll
+                    for (int tm = 0; tm < 2; ++tm) {
+                        const uint32_t src = base + KS_OFF + tm * KS_STAGE_BYTES;
+                        const int x0 = b0 + 64 * tm;
+                        if (x0 < active) tma_store_2d(&out_map, src, x0, q0);
+                        if (x0 + OUT_BOX_COLS < active)
+                            tma_store_2d(&out_map, src + OUT_BOX_BYTES, x0 + OUT_BOX_COLS, q0);
+                    }
+                    bulk_commit();
+                }
+                continue;
+            }
             if (use_tma) {
 #pragma unroll 1
                 for (int tm = 0; tm < 2; ++tm) {
