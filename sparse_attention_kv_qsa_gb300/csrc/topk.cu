@@ -411,6 +411,7 @@ __device__ __forceinline__ void topk_row(const float *__restrict__ scores, const
 
     uint32_t kk = static_cast<uint32_t>(k);
     bool listed = false;
+    bool first_hist = false;   // the first refinement digit was counted while gathering the list
     uint32_t tg = 0u, kmax = 0u;
     if (try_list) {
         const uint32_t gk[4] = {sx[0].x, sx[0].y, sx[0].z, sx[0].w};   // group-maximum mode's keys
@@ -638,10 +639,21 @@ __device__ __forceinline__ void topk_row(const float *__restrict__ scores, const
         if (listed && use_gmax) {
             // The listed scores are gathered (one L2 round trip for the whole
             // list) as keys (their maximum, the row's, is known from the group
-            // maxima).
+            // maxima). Every listed key lies in [tg, kmax], so all of them
+            // match the digit search's starting prefix and the first
+            // refinement digit's histogram is counted in the same loop (when
+            // that search will run).
+            const uint32_t diff = tg ^ kmax;
+            const int s0 = diff == 0u ? 0 : 32 - __clz(static_cast<int>(diff));
+            const int w0 = min(8, s0);
+            const uint32_t dm0 = (1u << w0) - 1u;
+            first_hist = s0 > 0 && nc != kk;
 #pragma unroll 4
-            for (int j = tid; j < static_cast<int>(nc); j += ROW_THREADS)
-                sh.cand_key[j] = float_bits_to_key(ld_word<kCoherent>(g + sh.cand_idx[j]));
+            for (int j = tid; j < static_cast<int>(nc); j += ROW_THREADS) {
+                const uint32_t key = float_bits_to_key(ld_word<kCoherent>(g + sh.cand_idx[j]));
+                sh.cand_key[j] = key;
+                if (first_hist) atomicAdd(&sh.histR[(key >> (s0 - w0)) & dm0], 1u);
+            }
             __syncthreads();
         } else if (listed) {
             // The listed scores are gathered as keys; the largest is kept.
@@ -729,7 +741,9 @@ __device__ __forceinline__ void topk_row(const float *__restrict__ scores, const
         const int width = min(8, shift);
         shift -= width;
         const uint32_t dmask = (1u << width) - 1u;
-        if (compact) {
+        if (first_hist) {
+            first_hist = false;   // this digit's histogram is complete already
+        } else if (compact) {
             for (int j = tid; j < m; j += ROW_THREADS) {
                 const uint32_t key = sh.cand_key[j];
                 if ((key & mask) == prefix) atomicAdd(&sh.histR[(key >> shift) & dmask], 1u);
