@@ -457,7 +457,9 @@ def attention_side_measurement(dev, stream, sm_mhz: float):
         out[name] = {"call_us_p50": us, "algorithmic_bytes": bytes_, "hbm_gbs": bytes_ / us / 1e3,
                      "fp32_tflops": flops / us / 1e6, "fp32_frac": flops / (us * 1e-6) / peak_fp32,
                      "fp32_peak_note": f"{sms} SMs x 128 lanes x 2 FLOP x {sm_mhz:.0f} MHz (sampled)",
-                     "kernel": ("attn_tc_kernel (tensor cores, mma.sync)" if nq >= sms
+                     "kernel": (f"attn_tc_kernel (tensor cores, mma.sync; "
+                                f"{16 if nq <= sms else 8 if nq <= 2 * sms else 4}-warp CTAs, "
+                                f"{1 if nq <= sms else 2 if nq <= 2 * sms else 4} per SM)" if nq >= sms
                                 else "attn_kernel (CUDA cores)")}
     return out
 

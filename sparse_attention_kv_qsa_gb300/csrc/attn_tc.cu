@@ -13,9 +13,11 @@
 // prompt attention runs on the matrix cores with q and p split into FP16
 // high and low parts and is gated against an FP64 reference.
 //
-// GB300 mapping. One CTA of 16 warps per query (this path is taken when the
-// queries alone fill the GPU). A warp step covers two listed blocks (8
-// cells). The int8 K and V bytes are exact in fp16; q (per head) and the
+// GB300 mapping. One CTA per query (this path is taken when the queries alone
+// fill the GPU): 16 warps up to the SM count, 8 warps (two CTAs per SM) up to
+// twice it, 4 warps (four per SM) beyond, so every query of a call of up to
+// 4x the SM count is resident at once and each SM runs 16 warps. A warp step
+// covers two listed blocks (8 cells). The int8 K and V bytes are exact in fp16; q (per head) and the
 // weights p * vs are split into a binary16 high part and a remainder scaled
 // by 2^11, so two fp16 rows per head carry about 22 significant bits and the
 // products accumulate in fp32:
@@ -39,14 +41,16 @@
 namespace qsa {
 namespace {
 
-constexpr int AT_WARPS = 16;
-constexpr int AT_THREADS = AT_WARPS * 32;
+// A CTA of kWarps warps per query, 16 / kWarps CTAs per SM (the registers of
+// 16 warps at most 128 each): 16 warps while the queries fit one CTA per SM,
+// then 8 and 4, so that every query of a call up to 4 times the SM count is
+// resident at once (one wave) and each SM holds 16 warps.
 constexpr int STEP_IDS = 2;                              // listed blocks per warp step
 constexpr int STAGES = 4;                                // steps in each warp's ring (a power of two)
 // Dynamic shared memory: the warps' rings (16-byte slots [warp][stage][4][32])
 // and each slot's first V cell per lane ([warp][stage][32]).
-constexpr int RING_BYTES = AT_WARPS * STAGES * 4 * 32 * 16;
-constexpr int DYN_BYTES = RING_BYTES + AT_WARPS * STAGES * 32 * 4;
+__host__ __device__ constexpr int ring_bytes(int warps) { return warps * STAGES * 4 * 32 * 16; }
+__host__ __device__ constexpr int dyn_bytes(int warps) { return ring_bytes(warps) + warps * STAGES * 32 * 4; }
 // Logits are kept in base-2 units: (q . k) * ks / sqrt(128) * log2(e), so the
 // softmax weights are 2^(logit - max) (the same weights as e^ of the natural
 // logits); log2(e) / sqrt(128), rounded to fp32.
@@ -59,13 +63,14 @@ __host__ __device__ constexpr int acc_off(int h, int d) {
 }
 static_assert(ACC_WORDS >= 16 * 32, "the q fragments fit a warp's accumulator rows");
 
+template <int kWarps>
 struct AttnShared {
-    float m[AT_WARPS][HEADS];                   // warp partials: running maximum,
-    float l[AT_WARPS][HEADS];                   // normaliser,
+    float m[kWarps][HEADS];                     // warp partials: running maximum,
+    float l[kWarps][HEADS];                     // normaliser,
     // and unnormalised outputs, head h, d = 32 t + 16 e + u at acc_off(h, d):
     // rows padded so that the 16 lanes holding a (e, u) pair write distinct
     // banks (during the loop: the warp's q fragments).
-    alignas(16) float acc[AT_WARPS][ACC_WORDS];
+    alignas(16) float acc[kWarps][ACC_WORDS];
 };
 
 // Two signed bytes of wx (bytes 0,1: sel 0x4140; bytes 2,3: sel 0x4342; wx
@@ -126,12 +131,14 @@ __device__ __forceinline__ void mma_1688(float &c0, float &c1, uint32_t a0, uint
 }
 #pragma nv_diag_default 550
 
-__global__ void __launch_bounds__(AT_THREADS, 1)
+template <int kWarps>
+__global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
     attn_tc_kernel(const float *__restrict__ q, const int8_t *__restrict__ kc, const __half *__restrict__ ks,
                 const int8_t *__restrict__ vc, const __half *__restrict__ vs, int ncells,
                 const int32_t *__restrict__ ids, int k, float *__restrict__ out) {
-    __shared__ AttnShared sh;
-    extern __shared__ __align__(16) uint8_t attn_dyn[];   // DYN_BYTES
+    constexpr int AT_THREADS = kWarps * 32;
+    __shared__ AttnShared<kWarps> sh;
+    extern __shared__ __align__(16) uint8_t attn_dyn[];   // dyn_bytes(kWarps)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int i = static_cast<int>(blockIdx.x);   // query
     const int32_t *ids_i = ids + static_cast<size_t>(i) * k;
@@ -182,7 +189,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
     const int nsteps = (k - 1) / STEP_IDS + 1;   // k >= 1
     // This warp's steps are wg, wg + nw, ...: the j-th is wg + j * nw.
-    const int wg = warp, nw = AT_WARPS;
+    const int wg = warp, nw = kWarps;
     const int nj = wg < nsteps ? (nsteps - 1 - wg) / nw + 1 : 0;
 
     // Block ids 16 steps at a time: lane l holds block l % 2 of the warp's
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     // masked and their weights are 0, so stale bytes never count). cellv: the
     // lane's first V cell of the step, or -1.
     uint4 *ring = reinterpret_cast<uint4 *>(attn_dyn) + static_cast<size_t>(warp) * STAGES * 4 * 32;
-    int *cellv = reinterpret_cast<int *>(attn_dyn + RING_BYTES) + warp * STAGES * 32;
+    int *cellv = reinterpret_cast<int *>(attn_dyn + ring_bytes(kWarps)) + warp * STAGES * 32;
     auto issue = [&](int j) {
         const int b0 = step_block(j, 0), b1 = step_block(j, 1);
         const int sl = j & (STAGES - 1);
@@ -359,25 +366,55 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
     __syncthreads();
 
-    // The CTA's warps merged in warp order: thread = (head, d).
-    const int h = threadIdx.x >> 7, d = threadIdx.x & (D - 1);
-    float M = -INFINITY;
+    // The CTA's warps merged in warp order: thread = (head, d), HEADS * D / AT_THREADS each.
+#pragma unroll 1
+    for (int hd_i = threadIdx.x; hd_i < HEADS * D; hd_i += AT_THREADS) {
+        const int h = hd_i >> 7, d = hd_i & (D - 1);
+        float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < AT_WARPS; ++w) M = fmaxf(M, sh.m[w][h]);
-    float A = 0.0f, L = 0.0f;
-    if (M != -INFINITY) {
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sh.m[w][h]);
+        float A = 0.0f, L = 0.0f;
+        if (M != -INFINITY) {
 #pragma unroll
-        for (int w = 0; w < AT_WARPS; ++w) {
-            const float mw = sh.m[w][h];
-            if (mw != -INFINITY) {
-                const float f = exp2f(mw - M);
-                A = fmaf(sh.acc[w][acc_off(h, d)], f, A);
-                L = fmaf(sh.l[w][h], f, L);
+            for (int w = 0; w < kWarps; ++w) {
+                const float mw = sh.m[w][h];
+                if (mw != -INFINITY) {
+                    const float f = exp2f(mw - M);
+                    A = fmaf(sh.acc[w][acc_off(h, d)], f, A);
+                    L = fmaf(sh.l[w][h], f, L);
+                }
             }
         }
+        float *o = out + (static_cast<size_t>(i) * HEADS + h) * D + d;
+        *o = L > 0.0f ? A / L : 0.0f;
     }
-    float *o = out + (static_cast<size_t>(i) * HEADS + h) * D + d;
-    *o = L > 0.0f ? A / L : 0.0f;
+}
+
+template <int kWarps>
+cudaError_t launch_attn_tc(const float *q, const int8_t *kc, const uint16_t *ks, const int8_t *vc,
+                           const uint16_t *vs, int ncells, const int32_t *ids, int nq, int k, float *out,
+                           cudaStream_t stream) {
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kWarps>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_bytes(kWarps));
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nq));
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = dyn_bytes(kWarps);
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<kWarps>, q, kc, reinterpret_cast<const __half *>(ks), vc,
+                              reinterpret_cast<const __half *>(vs), ncells, ids, k, out);
 }
 
 }  // namespace
@@ -386,27 +423,10 @@ cudaError_t launch_sparse_attn_tc(const float *q, const int8_t *kc, const uint16
                                   const uint16_t *vs, int ncells, const int32_t *ids, int nq, int k, float *out,
                                   cudaStream_t stream) {
     if (ncells > 0x7FFFFFFF - 4) return cudaErrorInvalidValue;
-    static thread_local int configured_device = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DYN_BYTES);
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(nq));
-    cfg.blockDim = dim3(AT_THREADS);
-    cfg.dynamicSmemBytes = DYN_BYTES;
-    cfg.stream = stream;
-    cudaLaunchAttribute attrs[1];
-    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attrs[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attrs;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel, q, kc, reinterpret_cast<const __half *>(ks), vc,
-                              reinterpret_cast<const __half *>(vs), ncells, ids, k, out);
+    const int sms = device_sm_count();
+    if (nq <= sms) return launch_attn_tc<16>(q, kc, ks, vc, vs, ncells, ids, nq, k, out, stream);
+    if (nq <= 2 * sms) return launch_attn_tc<8>(q, kc, ks, vc, vs, ncells, ids, nq, k, out, stream);
+    return launch_attn_tc<4>(q, kc, ks, vc, vs, ncells, ids, nq, k, out, stream);
 }
 
 }  // namespace qsa

@@ -112,7 +112,12 @@ def _check(W, out):
                                              (160, 17, 5, 0),
                                              (152, 4096, 1, 0),
                                              (153, 65536, 300, 290),
-                                             (152, 262144, 4096, 0)])   # 16,384 cells per query
+                                             (152, 262144, 4096, 0),    # 16,384 cells per query
+                                             # 8-warp CTAs, two per SM (SMs < nq <= 2 SMs) and
+                                             # 4-warp CTAs, four per SM (beyond; 640: more than one wave):
+                                             (305, 16384, 512, 17),
+                                             (400, 65536, 300, 290),
+                                             (640, 4099 * 4 + 3, 64, 0)])
 def test_sparse_attn_matches_oracle(nq, ncells, k, pad):
     import torch
     from sparse_attention_kv_qsa_gb300 import workloads as w
@@ -129,7 +134,7 @@ def test_sparse_attn_matches_oracle(nq, ncells, k, pad):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("nq", [4, 160])        # CUDA-core / tensor-core kernel
+@pytest.mark.parametrize("nq", [4, 160, 320])   # CUDA-core / tensor-core kernel (8- and 4-warp CTAs)
 def test_sparse_attn_padding_duplicates_and_empty(nq):
     """All-padding rows give zeros; ids past the last block are skipped; a
     block listed twice counts twice; no cells at all gives zeros."""
@@ -157,7 +162,7 @@ def _rescale_half(bits, mul):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("nq", [8, 160])        # CUDA-core / tensor-core kernel
+@pytest.mark.parametrize("nq", [8, 160, 320])   # CUDA-core / tensor-core kernel (8- and 4-warp CTAs)
 @pytest.mark.parametrize("qmul,vsmul,ksmul", [(1e5, 1.0, 1.0),     # near one-hot softmax
                                               (1e-20, 1.0, 1.0),   # uniform softmax, tiny q
                                               (1.0, 6.0e5, 1.0),   # value scales up to 6e4
