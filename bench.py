@@ -39,6 +39,7 @@ data path); timing is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import math
@@ -678,6 +679,10 @@ def main():
 
     score, topk = calls[path]
     K_ = args.steps
+    # No garbage-collection pause may land inside a timed event pair: a host
+    # stall between a step's launches leaves the GPU idle inside that step.
+    gc.collect()
+    gc.disable()
     # The clock sampler runs from before the warm-up to after the timed steps.
     sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
     if sampler:
@@ -914,6 +919,7 @@ def main():
             sweep[f"k{ks}"] = {"step_us": 1e3 * statistics.mean(t_st), "topk_us": 1e3 * statistics.mean(t_k)}
         line["k_sweep"] = sweep
 
+    gc.enable()
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_baseline(W)
     if world > 1:

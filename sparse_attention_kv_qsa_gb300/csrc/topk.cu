@@ -1006,7 +1006,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
 }
 
 // ---- fused select: scores and top-k without the scores ----------------------
-// Step 1 (select_threshold_kernel, one CTA per query row): a threshold that
+// Step 1 (select_threshold_kernel, one CTA per SEL_ROWS query rows): a threshold that
 // about 1.8 k + 8 n / S of the row's n scores are expected to reach: the
 // r-th largest key, r = ceil(1.8 k S / n) + 8, of a strided sample of S =
 // LIST_SAMPLE blocks scored on CUDA cores (the same head-summed query and
@@ -1022,76 +1022,107 @@ constexpr int LIST_SAMPLE = 1024;
 constexpr int LIST_PER = LIST_CAP / ROW_THREADS;   // list entries per thread in step 3
 static_assert(LIST_CAP % ROW_THREADS == 0 && LIST_PER <= 32, "list entries in registers");
 
-__global__ void __launch_bounds__(ROW_THREADS, 2)
-    select_threshold_kernel(const float *__restrict__ q, const float *__restrict__ kblk, int active, int k,
+// SEL_ROWS query rows per CTA share each sample key row (read once from L2 for
+// all of them); a warp scores one sample block per step, SEL_BATCH blocks'
+// loads in flight.
+constexpr int SEL_ROWS = 2;
+constexpr int SEL_BATCH = 16;
+static_assert(LIST_SAMPLE % (ROW_WARPS * SEL_BATCH) == 0, "whole sample batches");
+static_assert(SEL_ROWS * D <= ROW_THREADS, "one thread per query value");
+
+__global__ void __launch_bounds__(ROW_THREADS, 1)
+    select_threshold_kernel(const float *__restrict__ q, const float *__restrict__ kblk, int nq, int active, int k,
                             float *__restrict__ thr, uint32_t *__restrict__ cnt, uint32_t *__restrict__ fail,
                             uint32_t *__restrict__ gfail) {
-    __shared__ __align__(16) float qs[D];
-    __shared__ uint32_t keys[LIST_SAMPLE];
+    __shared__ __align__(16) float qs[SEL_ROWS][D];
+    __shared__ uint32_t keys[SEL_ROWS][LIST_SAMPLE];
     __shared__ __align__(16) uint32_t hist[BINS_R];
     __shared__ uint32_t sel[3];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int row = blockIdx.x;
+    const int row0 = blockIdx.x * SEL_ROWS;
+    const int nr = min(SEL_ROWS, nq - row0);
     if (tid < BINS_R) hist[tid] = 0u;
     // q and the keys may come from the previous grid; the scorer that follows
     // may start once every CTA is past this wait (it reads q and the keys,
     // not these thresholds, before waiting for this grid).
     grid_dependency_wait();
     grid_launch_dependents();
-    if (tid < D) {
-        const float *p = q + static_cast<size_t>(row) * (HEADS * D) + tid;
-        qs[tid] = __fadd_rn(__fadd_rn(__fadd_rn(ld_in(p), ld_in(p + D)), ld_in(p + 2 * D)), ld_in(p + 3 * D));
+    if (tid < SEL_ROWS * D) {
+        const int r = tid / D, d = tid % D;
+        float v = 0.0f;
+        if (r < nr) {
+            const float *p = q + static_cast<size_t>(row0 + r) * (HEADS * D) + d;
+            v = __fadd_rn(__fadd_rn(__fadd_rn(ld_in(p), ld_in(p + D)), ld_in(p + 2 * D)), ld_in(p + 3 * D));
+        }
+        qs[r][d] = v;
     }
-    if (tid == 0) {
+    if (tid < nr) {
+        const int row = row0 + tid;
         cnt[row] = 0u;
         fail[row] = 0u;
         if (row % 128 == 0) gfail[row / 128] = 0u;
     }
     __syncthreads();
     // Sample block j: j * n / S (a warp per block: 16 bytes of the key row per lane).
-    const float4 qv = *reinterpret_cast<const float4 *>(qs + 4 * lane);
-#pragma unroll 4
-    for (int j = warp; j < LIST_SAMPLE; j += ROW_WARPS) {
-        const long long b = static_cast<long long>(j) * active / LIST_SAMPLE;
-        const float4 kv = ld_in(reinterpret_cast<const float4 *>(kblk + b * D) + lane);
-        float acc = fmaf(qv.w, kv.w, fmaf(qv.z, kv.z, fmaf(qv.y, kv.y, qv.x * kv.x)));
+    float4 qv[SEL_ROWS];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, o);
-        if (lane == 0) keys[j] = score_key(acc);
-    }
-    __syncthreads();
-    // The r-th largest sample key, 8 bits at a time (two keys per thread).
-    static_assert(LIST_SAMPLE == 2 * ROW_THREADS, "two sample keys per thread");
-    const uint32_t k0 = keys[tid], k1 = keys[tid + ROW_THREADS];
-    uint32_t r = static_cast<uint32_t>((9ull * static_cast<uint64_t>(k) * LIST_SAMPLE + 5ull * active - 1) /
-                                       (5ull * active)) + 8u;
-    if (r > LIST_SAMPLE) r = LIST_SAMPLE;
-    uint32_t prefix = 0u, mask = 0u;
+    for (int r = 0; r < SEL_ROWS; ++r) qv[r] = *reinterpret_cast<const float4 *>(&qs[r][4 * lane]);
 #pragma unroll 1
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        if ((k0 & mask) == prefix) atomicAdd(&hist[(k0 >> shift) & 255u], 1u);
-        if ((k1 & mask) == prefix) atomicAdd(&hist[(k1 >> shift) & 255u], 1u);
-        __syncthreads();
-        if (warp == 0) {
-            uint32_t bin, above, c;
-            warp_find_256(hist, r, true, lane, bin, above, c);
-            if (lane == 0) {
-                sel[0] = bin;
-                sel[1] = above;
-                sel[2] = c;
+    for (int j0 = warp; j0 < LIST_SAMPLE; j0 += ROW_WARPS * SEL_BATCH) {
+        float4 kv[SEL_BATCH];
+#pragma unroll
+        for (int u = 0; u < SEL_BATCH; ++u) {
+            const long long b = static_cast<long long>(j0 + u * ROW_WARPS) * active / LIST_SAMPLE;
+            kv[u] = ld_in(reinterpret_cast<const float4 *>(kblk + b * D) + lane);
+        }
+#pragma unroll
+        for (int u = 0; u < SEL_BATCH; ++u) {
+#pragma unroll
+            for (int r = 0; r < SEL_ROWS; ++r) {
+                float acc = fmaf(qv[r].w, kv[u].w, fmaf(qv[r].z, kv[u].z, fmaf(qv[r].y, kv[u].y, qv[r].x * kv[u].x)));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, o);
+                if (lane == 0) keys[r][j0 + u * ROW_WARPS] = score_key(acc);
             }
         }
-        __syncthreads();
-        r -= sel[1];
-        prefix |= sel[0] << shift;
-        mask |= 255u << shift;
-        const bool whole = sel[2] == r;   // every key of the bin is among the r largest
-        __syncthreads();                   // sel read by all before the next digit rewrites it
-        if (whole) break;                  // (uniform) prefix is a key at least r sample keys reach
     }
-    if (tid == 0) {
-        // x >= ft exactly when key(x) >= prefix (NaN, key of -inf, fails it).
-        thr[row] = __uint_as_float(prefix >= 0x80000000u ? (prefix ^ 0x80000000u) : ~prefix);
+    __syncthreads();
+    // Per row, the r-th largest sample key, 8 bits at a time (two keys per
+    // thread); each digit's find clears the histogram for the next.
+    static_assert(LIST_SAMPLE == 2 * ROW_THREADS, "two sample keys per thread");
+#pragma unroll 1
+    for (int rr = 0; rr < nr; ++rr) {   // uniform
+        const uint32_t k0 = keys[rr][tid], k1 = keys[rr][tid + ROW_THREADS];
+        uint32_t r = static_cast<uint32_t>((9ull * static_cast<uint64_t>(k) * LIST_SAMPLE + 5ull * active - 1) /
+                                           (5ull * active)) + 8u;
+        if (r > LIST_SAMPLE) r = LIST_SAMPLE;
+        uint32_t prefix = 0u, mask = 0u;
+#pragma unroll 1
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            if ((k0 & mask) == prefix) atomicAdd(&hist[(k0 >> shift) & 255u], 1u);
+            if ((k1 & mask) == prefix) atomicAdd(&hist[(k1 >> shift) & 255u], 1u);
+            __syncthreads();
+            if (warp == 0) {
+                uint32_t bin, above, c;
+                warp_find_256(hist, r, true, lane, bin, above, c);
+                if (lane == 0) {
+                    sel[0] = bin;
+                    sel[1] = above;
+                    sel[2] = c;
+                }
+            }
+            __syncthreads();
+            r -= sel[1];
+            prefix |= sel[0] << shift;
+            mask |= 255u << shift;
+            const bool whole = sel[2] == r;   // every key of the bin is among the r largest
+            __syncthreads();                   // sel read by all before the next digit rewrites it
+            if (whole) break;                  // (uniform) prefix is a key at least r sample keys reach
+        }
+        if (tid == 0) {
+            // x >= ft exactly when key(x) >= prefix (NaN, key of -inf, fails it).
+            thr[row0 + rr] = __uint_as_float(prefix >= 0x80000000u ? (prefix ^ 0x80000000u) : ~prefix);
+        }
     }
 }
 
@@ -1254,7 +1285,7 @@ cudaError_t launch_select_decode(const float *q, const float *kblk, const int8_t
 cudaError_t launch_select_threshold(const float *q, const float *kblk, int nq, int active, int k, float *thr,
                                     uint32_t *cnt, uint32_t *fail, uint32_t *gfail, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(nq));
+    cfg.gridDim = dim3(static_cast<unsigned>((nq + SEL_ROWS - 1) / SEL_ROWS));
     cfg.blockDim = dim3(ROW_THREADS);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1262,7 +1293,7 @@ cudaError_t launch_select_threshold(const float *q, const float *kblk, int nq, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, select_threshold_kernel, q, kblk, active, k, thr, cnt, fail, gfail);
+    return cudaLaunchKernelEx(&cfg, select_threshold_kernel, q, kblk, nq, active, k, thr, cnt, fail, gfail);
 }
 
 cudaError_t launch_select_list(const uint2 *cand, const uint32_t *cnt, int nq, int active, int k, int32_t *ids,
