@@ -117,7 +117,7 @@ uint32_t *select_scratch() {
 }
 
 // The fused select's scratch: per row a threshold, a list count, a failure
-// flag and a list of LIST_CAP (key, id) pairs; per query group a flag.
+// flag and a list of LIST_CAP (fp32 score bits, block id) pairs; per query group a flag.
 struct SelectScratch {
     float *thr;
     uint32_t *cnt, *fail, *gfail;

@@ -29,12 +29,12 @@ cudaError_t launch_scores_ffma(const float *q, const float *kblk, const int8_t *
                                const uint16_t *kscale, int nq, int active, float *scores,
                                cudaStream_t stream);
 
-// The fused select's per-row candidate lists: LIST_CAP (key, block id) pairs.
+// The fused select's per-row candidate lists: LIST_CAP (fp32 score bits, block id) pairs.
 constexpr int LIST_CAP = 4096;
 
 // Extra modes of the tensor-core scorer for the fused select (fp32 keys):
 // list mode (thr set): no scores are stored; every score >= thr[row] is
-// appended to the row's list cand[row][0 .. LIST_CAP) as (key, id), counted
+// appended to the row's list cand[row][0 .. LIST_CAP) as (fp32 bits, id), counted
 // in cnt[row]; the scorer waits for the previous grid (which writes thr and
 // clears cnt) only before its first append. Gated mode (gate set): only the
 // CTAs of query groups g with gate[g] != 0 run (after waiting for the

@@ -27,12 +27,12 @@
 //    (192 of the 512 columns), written once by the epilogue warps.
 //  - B: key tiles in K-halves. A producer warp loads raw key pieces of
 //    64 rows x 64 d with 2-D tensor copies (16 KiB fp32) into a 6-slot
-//    ring; 5 converter warps split them into three 128-byte-swizzled
+//    ring; 6 converter warps split them into three 128-byte-swizzled
 //    K-major bf16 slices of a K-half stage (3 x 16 KiB), 2 stages in flight.
 //  - One thread issues tcgen05.mma into two accumulators (hi*hi;
 //    corrections), 128 columns each, and frees each K-half stage and hands
 //    the finished tile to the epilogue with tcgen05.commit. Its SM
-//    sub-partition holds no converter warp.
+//    sub-partition also holds two epilogue warps and one converter.
 //  - 8 epilogue warps (two per TMEM lane quarter, one per column half;
 //    thread = query row) read both accumulators out at once, so the next
 //    tile's MMAs can start, add them, and store the scores by 2-D tensor
@@ -472,13 +472,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             if (list_mode) {
                 // Append the scores at or above the threshold (x >= ft: NaN
-                // fails) to the row's list, as (key, block id); one atomic per
-                // thread and tile reserves the slots.
+                // fails) to the row's list, as (fp32 bits, block id: the list
+                // select takes the keys); one atomic per thread and tile
+                // reserves the slots.
                 uint32_t h0 = 0u, h1 = 0u;
+                if (nb == TILE_N) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    h0 |= static_cast<uint32_t>(col0 + j < nb && v[j] >= ft) << j;
-                    h1 |= static_cast<uint32_t>(col0 + 32 + j < nb && v[32 + j] >= ft) << j;
+                    for (int j = 0; j < 32; ++j) {
+                        h0 |= v[j] >= ft ? 1u << j : 0u;
+                        h1 |= v[32 + j] >= ft ? 1u << j : 0u;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        h0 |= static_cast<uint32_t>(col0 + j < nb && v[j] >= ft) << j;
+                        h1 |= static_cast<uint32_t>(col0 + 32 + j < nb && v[32 + j] >= ft) << j;
+                    }
                 }
                 const uint32_t c = __popc(h0) + __popc(h1);
                 if (c != 0u && row < qn) {
@@ -488,7 +497,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     for (int j = 0; j < TILE_N / 2; ++j) {
                         if (((j < 32 ? h0 : h1) >> (j & 31)) & 1u) {
                             if (slot < static_cast<uint32_t>(LIST_CAP))
-                                dst[slot] = make_uint2(score_key(v[j]), static_cast<uint32_t>(b0 + col0 + j));
+                                dst[slot] = make_uint2(__float_as_uint(v[j]), static_cast<uint32_t>(b0 + col0 + j));
                             ++slot;
                         }
                     }

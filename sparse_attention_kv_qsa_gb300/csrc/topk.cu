@@ -1012,7 +1012,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
 // LIST_SAMPLE blocks scored on CUDA cores (the same head-summed query and
 // fp32 FMA; its rounding only moves the threshold). Step 2 (the tensor-core
 // scorer in list mode) appends every score at or above its row's threshold,
-// as (key, block id), to the row's list instead of storing scores. Step 3
+// as (fp32 bits, block id), to the row's list instead of storing scores. Step 3
 // (select_list_kernel): when a row's list holds at least k entries and did
 // not overflow, it holds every score at or above the threshold and therefore
 // the whole top-k, ties included, and the exact digit search runs on it;
@@ -1126,7 +1126,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 1)
     }
 }
 
-// Step 3: one CTA per row; the row's list (at most LIST_CAP (key, id) pairs,
+// Step 3: one CTA per row; the row's list (at most LIST_CAP (score bits, id) pairs,
 // LIST_PER per thread) is read into registers and selected exactly, the ids
 // marked in bitmaps over [0, active) and written ascending. A row whose list
 // is short or overflowed is flagged (and its query group), and left to the
@@ -1163,7 +1163,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
         id[j] = 0u;
         if (e < n) {
             const uint2 v = __ldcg(c + e);
-            key[j] = v.x;
+            key[j] = score_key(__uint_as_float(v.x));
             id[j] = v.y;
             valid |= 1u << j;
         }
