@@ -137,7 +137,10 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, int lane) {
 }
 
 // Block-wide exclusive prefix sum over threads (every thread must call).
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *tot, int lane, int warp) {
+// With trailing_sync false the warp totals are left as they are for good (the
+// caller's last use of tot before the CTA ends).
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *tot, int lane, int warp,
+                                                    bool trailing_sync = true) {
     static_assert(ROW_WARPS == 16, "warp totals are read as four 16-byte words");
     const uint32_t incl = warp_incl_scan(v, lane);
     if (lane == 31) tot[warp] = incl;
@@ -149,7 +152,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *tot, i
         before += (4 * q + 0 < warp ? t.x : 0u) + (4 * q + 1 < warp ? t.y : 0u) + (4 * q + 2 < warp ? t.z : 0u) +
                   (4 * q + 3 < warp ? t.w : 0u);
     }
-    __syncthreads();
+    if (trailing_sync) __syncthreads();
     return before + incl - v;
 }
 
@@ -250,7 +253,9 @@ __device__ __forceinline__ void stream_row(const uint32_t *g, int n, int head, i
 
 // The end of one row's selection, shared by every path: selbits marks the
 // selected ids; when `ties` is set, the first kk ids marked in tiebits (in id
-// order) join them. Writes the row's k ids in ascending order to out.
+// order) join them. Writes the row's k ids in ascending order to out. It is
+// the CTA's last step (one row per CTA), so its final block scan leaves the
+// warp totals without a closing barrier.
 __device__ __forceinline__ void finish_row(uint32_t *selbits, const uint32_t *tiebits, int nwords, bool ties,
                                            uint32_t kk, int k, int32_t *__restrict__ out, RowShared &sh, int tid,
                                            int lane, int warp) {
@@ -282,7 +287,7 @@ __device__ __forceinline__ void finish_row(uint32_t *selbits, const uint32_t *ti
         const uint32_t wv[4] = {w4.x, wb + 1 < nwords ? w4.y : 0u, wb + 2 < nwords ? w4.z : 0u,
                                 wb + 3 < nwords ? w4.w : 0u};
         uint32_t pos = block_excl_scan(__popc(wv[0]) + __popc(wv[1]) + __popc(wv[2]) + __popc(wv[3]), sh.scan_tot,
-                                       lane, warp);
+                                       lane, warp, false);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             uint32_t bits = wv[e];
@@ -296,7 +301,7 @@ __device__ __forceinline__ void finish_row(uint32_t *selbits, const uint32_t *ti
     } else {
         uint32_t c = 0u;
         for (int wd = wb; wd < we; ++wd) c += __popc(selbits[wd]);
-        uint32_t pos = block_excl_scan(c, sh.scan_tot, lane, warp);
+        uint32_t pos = block_excl_scan(c, sh.scan_tot, lane, warp, false);
         for (int wd = wb; wd < we; ++wd) {
             uint32_t bits = selbits[wd];
             while (bits != 0u) {
@@ -364,6 +369,7 @@ __device__ __forceinline__ void topk_row(const float *__restrict__ scores, const
         static_assert(HIST_A == 4 * ROW_THREADS, "one 16-byte store per thread clears histA");
         reinterpret_cast<uint4 *>(sh.histA)[tid] = make_uint4(0u, 0u, 0u, 0u);
     }
+    if (use_gmax && tid < HIST_A / GROUP) sh.groupA[tid] = 0u;   // counted with histA below
     for (int i = tid; i < BINS_R; i += ROW_THREADS) sh.histR[i] = 0u;
     for (int i = tid; i < nwords; i += ROW_THREADS) {
         selbits[i] = 0u;
@@ -433,14 +439,11 @@ __device__ __forceinline__ void topk_row(const float *__restrict__ scores, const
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const uint32_t d = smax - gk[e];
-                if (4 * tid + e < ngr && d < (static_cast<uint32_t>(HIST_A) << GMAX_SHIFT))
-                    atomicAdd(&sh.histA[HIST_A - 1 - (d >> GMAX_SHIFT)], 1u);
-            }
-            __syncthreads();
-            if (tid < HIST_A / GROUP) {
-                const uint4 a = *reinterpret_cast<const uint4 *>(&sh.histA[GROUP * tid]);
-                const uint4 b = *reinterpret_cast<const uint4 *>(&sh.histA[GROUP * tid + 4]);
-                sh.groupA[tid] = a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w;
+                if (4 * tid + e < ngr && d < (static_cast<uint32_t>(HIST_A) << GMAX_SHIFT)) {
+                    const uint32_t bin = HIST_A - 1 - (d >> GMAX_SHIFT);
+                    atomicAdd(&sh.histA[bin], 1u);
+                    atomicAdd(&sh.groupA[bin / GROUP], 1u);   // the group sums, without a pass of their own
+                }
             }
             __syncthreads();
             if (warp == 0) warp_select_2048(kk, sh, lane);
