@@ -460,7 +460,7 @@ def attention_side_measurement(dev, stream, sm_mhz: float):
                      "fp32_peak_note": f"{sms} SMs x 128 lanes x 2 FLOP x {sm_mhz:.0f} MHz (sampled)",
                      "kernel": (f"attn_tc_kernel (tensor cores, mma.sync; "
                                 f"{16 if nq <= sms else 8 if nq <= 2 * sms else 4}-warp CTAs, "
-                                f"{1 if nq <= sms else 2 if nq <= 2 * sms else 4} per SM)" if nq >= sms
+                                f"{1 if nq <= sms else 2 if nq <= 2 * sms else 4} per SM)" if 2 * nq > sms
                                 else "attn_kernel (CUDA cores)")}
     return out
 
@@ -551,7 +551,7 @@ def main():
                     help="only run the decode layer (append + scores + top-k + attention, nq = 4, 262,144 cells, "
                          "k=128) this many times (a short run for a profiler to capture), then exit")
     ap.add_argument("--attn-nq", type=int, default=256,
-                    help="queries of the --attn-launches run (below the SM count: the CUDA-core kernel)")
+                    help="queries of the --attn-launches run (at most half the SM count: the CUDA-core kernel)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 

@@ -214,9 +214,9 @@ qsa_status qsa_block_select_small(const float *q, const float *kblk, const int8_
  *   logit[h][c] = (sum_d q[i][h][d] * k_cells[c][d]) * k_scale[c] / sqrt(128)
  *   out[i][h][d] = sum_c softmax_c(logit[h][.]) * v_cells[c][d] * v_scale[c]
  * and out = 0 for a query with no attended cell. Accumulation is fp32 in a
- * fixed order (the result does not depend on scheduling). With fewer queries
- * than the device has SMs the products are fp32 on CUDA cores; with more,
- * they run on the tensor cores (mma.sync): q (per head) and the softmax
+ * fixed order (the result does not depend on scheduling). With at most half
+ * as many queries as the device has SMs the products are fp32 on CUDA cores;
+ * with more, they run on the tensor cores (mma.sync): q (per head) and the softmax
  * weights times v_scale, each scaled by a power of two chosen from the data,
  * enter as binary16 high parts plus remainders (about 22 significant bits),
  * the int8 cells exactly, with fp32 accumulation.

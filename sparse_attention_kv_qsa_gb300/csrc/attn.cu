@@ -17,9 +17,10 @@
 // This file is the CUDA-core path, taken when there are fewer queries than
 // SMs; csrc/attn_tc.cu holds the tensor-core path for more.
 //
-// GB300 mapping. One CTA of 16 warps per query, or a cluster of up to 4 CTAs
-// per query when there are few queries (decode), so that the cells of one
-// query stream through several SMs. A warp step covers two listed blocks
+// GB300 mapping. A cluster of 2 or 4 CTAs of 16 warps per query (this kernel
+// runs for at most half as many queries as SMs, decode included), so that
+// the cells of one query stream through several SMs; a single CTA per query
+// (no cluster) is kept for generality. A warp step covers two listed blocks
 // (8 cells): every lane loads its 4 bytes (d = 4 lane .. +3) of each cell's
 // K and V row (one 128-byte line per row and warp), forms the 8 x 4 partial
 // dot products against its slice of the 4 head queries, and a butterfly
@@ -290,11 +291,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 cudaError_t launch_sparse_attn(const float *q, const int8_t *kc, const uint16_t *ks, const int8_t *vc,
                                const uint16_t *vs, int ncells, const int32_t *ids, int nq, int k, float *out,
                                cudaStream_t stream) {
-    // As many queries as SMs or more: the tensor-core kernel (csrc/attn_tc.cu),
-    // measured faster there; fewer: this one, whose cells per step are
-    // fewer instructions away from the softmax (lower latency per step).
+    // More queries than half the SMs (where this kernel would run one CTA per
+    // query, without a cluster): the tensor-core kernel (csrc/attn_tc.cu),
+    // measured faster there (100 queries: 35.5 against 41.6 us); fewer: this
+    // one, whose clusters spread each query over 2 or 4 SMs (64 queries: 27.3
+    // against 35.5 us).
     const int sms = device_sm_count();
-    if (nq >= sms) return launch_sparse_attn_tc(q, kc, ks, vc, vs, ncells, ids, nq, k, out, stream);
+    if (2 * nq > sms) return launch_sparse_attn_tc(q, kc, ks, vc, vs, ncells, ids, nq, k, out, stream);
     // Few queries: a cluster per query spreads its cells over several SMs.
     int csize = 1;
     for (int c = MAX_CLUSTER; c > 1; c >>= 1) {

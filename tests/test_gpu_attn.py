@@ -99,7 +99,7 @@ def _check(W, out):
                                              (4, 262144, 128, 0),
                                              (30, 65536, 256, 3),       # clusters of 4
                                              (60, 16384, 64, 0),        # pairs
-                                             (100, 16384, 512, 17),     # one CTA per query (CUDA cores)
+                                             (100, 16384, 512, 17),     # tensor cores: more than half the SMs
                                              (3, 4099 * 4 + 3, 60, 7),  # partial last block
                                              (2, 17, 5, 0),             # every block, ragged
                                              (5, 4096, 1, 0),           # one block
