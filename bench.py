@@ -458,11 +458,20 @@ def attention_side_measurement(dev, stream, sm_mhz: float):
         out[name] = {"call_us_p50": us, "algorithmic_bytes": bytes_, "hbm_gbs": bytes_ / us / 1e3,
                      "fp32_tflops": flops / us / 1e6, "fp32_frac": flops / (us * 1e-6) / peak_fp32,
                      "fp32_peak_note": f"{sms} SMs x 128 lanes x 2 FLOP x {sm_mhz:.0f} MHz (sampled)",
-                     "kernel": (f"attn_tc_kernel (tensor cores, mma.sync; "
-                                f"{16 if nq <= sms else 8 if nq <= 2 * sms else 4}-warp CTAs, "
-                                f"{1 if nq <= sms else 2 if nq <= 2 * sms else 4} per SM)" if 2 * nq > sms
-                                else "attn_kernel (CUDA cores)")}
+                     "kernel": attn_kernel_label(nq, sms)}
     return out
+
+
+def attn_kernel_label(nq: int, sms: int) -> str:
+    """Which attention kernel and CTA form qsa_sparse_attn launches for nq
+    queries on a device with `sms` SMs (the launchers' rule): CUDA cores
+    with clusters of 4 or 2 CTAs per query up to half the SM count; beyond
+    it the tensor cores, 16-warp CTAs up to the SM count, then 8-warp CTAs
+    two per SM up to twice it, then 4-warp CTAs four per SM."""
+    if 2 * nq <= sms:
+        return f"attn_kernel (CUDA cores, clusters of {4 if 4 * nq <= sms else 2} CTAs per query)"
+    warps = 16 if nq <= sms else 8 if nq <= 2 * sms else 4
+    return f"attn_tc_kernel (tensor cores, mma.sync; {warps}-warp CTAs, {16 // warps} per SM)"
 
 
 def summary_side_measurement(dev, stream):

@@ -125,3 +125,17 @@ def test_clock_summary_empty_and_all_na():
     assert bench.ClockSampler.summarise([]) is None
     s = bench.ClockSampler.summarise([_row("[N/A]", "[N/A]")])
     assert s["sm_mhz"] is None and s["sm_max_mhz"] is None and s["samples"] == 1
+
+
+def test_attn_kernel_label_follows_the_dispatch():
+    # 152 SMs: clusters of 4 up to 38 queries, pairs up to 76, tensor cores beyond
+    sms = 152
+    assert bench.attn_kernel_label(1, sms).startswith("attn_kernel (CUDA cores, clusters of 4")
+    assert bench.attn_kernel_label(38, sms).startswith("attn_kernel (CUDA cores, clusters of 4")
+    assert bench.attn_kernel_label(39, sms).startswith("attn_kernel (CUDA cores, clusters of 2")
+    assert bench.attn_kernel_label(76, sms).startswith("attn_kernel (CUDA cores, clusters of 2")
+    assert "16-warp CTAs, 1 per SM" in bench.attn_kernel_label(77, sms)
+    assert "16-warp CTAs, 1 per SM" in bench.attn_kernel_label(152, sms)
+    assert "8-warp CTAs, 2 per SM" in bench.attn_kernel_label(153, sms)
+    assert "8-warp CTAs, 2 per SM" in bench.attn_kernel_label(304, sms)
+    assert "4-warp CTAs, 4 per SM" in bench.attn_kernel_label(305, sms)
