@@ -1,6 +1,7 @@
 """Host-side helpers of bench.py on CPU: the algorithmic byte counts the
-roofline divides by, the percentile, the peaks and traffic records, and the
-clock-sample summary that decides whether a timed run is kept."""
+roofline divides by, the percentile, the peaks and traffic records, the
+clock-sample summary that decides whether a timed run is kept, and the
+attention kernel label (the launchers' dispatch rule)."""
 import hashlib
 import os
 import sys
